@@ -1,0 +1,371 @@
+// k2_prefill_tcgen05.cu -- K2: causal grouped-query flash attention over the
+// prompt (prefill), on the 5th-generation tensor cores.
+//
+// "Prefill ... is a large share of total time" for prompts of 512-2048 tokens
+// and 32-128 generated tokens (dryft-flash-infer agent guide, "Where the wins
+// are", prefill bullet).  The result is exact causal softmax attention; only
+// the order of the arithmetic differs from the definition ("reorderings are
+// affordable", same guide, "Numerics").
+//
+// One CTA = one 128-row query block of one sequence for TWO query heads of the
+// same kv head (GQA: both share every K/V tile).  Warp roles (320 threads):
+//   warps 0-3  softmax warpgroup 0 (query head h0): thread r owns row r
+//   warps 4-7  softmax warpgroup 1 (query head h1)
+//   warp  8    TMA producer: Q0/Q1 once, then K_j, V_j tiles into a ring
+//   warp  9    tcgen05 issuer (one thread) and TMEM owner
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [0,128) S0/P0   [128,256) S1/P1   [256,256+D) O0   [256+D,256+2D) O1
+// S_t = Q_t K_j^T (both operands K-major, 128-byte swizzled smem); the softmax
+// threads read their row of S_t with tcgen05.ld, compute p = 2^(s*c - m*c) in
+// fp32, write P as bf16 over the first 64 columns of S_t, rescale O_t when the
+// running max grew, and signal; O_t += P_t V_j reads P from TMEM and V
+// (MN-major) from smem.  The issuer waits for PV_t(j) to finish before the
+// next S_t overwrites P_t.
+//
+// K and V come straight out of the cache through one 3-D tensor map per
+// sequence, (D, L_b, Hkv), so rows at or past the sequence's length read as
+// zero; the causal mask on the diagonal tile removes them from the softmax.
+// Every mbarrier wait is bounded (qa_device.cuh): a stuck pipeline records a
+// timeout in the error word and the CTA still frees its TMEM and exits.
+#include "qa_device.cuh"
+
+namespace qa {
+
+template <int D>
+struct K2Layout {
+    static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 64 bf16
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D
+    static constexpr int kStages = (D == 128) ? 4 : 6;
+    static constexpr int kQBytes = 2 * kTileBytes;
+    static constexpr int kSmemBytes = kQBytes + kStages * kTileBytes + 1024;  // + alignment slack
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+__device__ __forceinline__ float k2_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Heaviest-first work order: query blocks with more key tiles start first.
+__device__ __forceinline__ bool k2_decode_item(const K2Params &p, int idx, int &b, int &kvh,
+                                               int &pair, int &qb) {
+    for (int lvl = p.max_qblocks - 1; lvl >= 0; --lvl) {
+        int eligible = 0;
+        for (int s = 0; s < p.nseq; ++s) eligible += ((p.len[s] + 127) / 128 > lvl);
+        const int cnt = eligible * p.Hkv * p.npairs;
+        if (idx < cnt) {
+            const int per_seq = p.Hkv * p.npairs;
+            int which = idx / per_seq;
+            const int rem = idx % per_seq;
+            for (int s = 0; s < p.nseq; ++s) {
+                if ((p.len[s] + 127) / 128 > lvl) {
+                    if (which == 0) {
+                        b = s;
+                        break;
+                    }
+                    --which;
+                }
+            }
+            kvh = rem / p.npairs;
+            pair = rem % p.npairs;
+            qb = lvl;
+            return true;
+        }
+        idx -= cnt;
+    }
+    return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kK2Threads, 1)
+    k2_prefill_kernel(const __grid_constant__ K2Params p) {
+    using Lay = K2Layout<D>;
+    constexpr int NS = Lay::kStages;
+    const unsigned FULL = 0xffffffffu;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_q, bar_kv_full[NS], bar_kv_empty[NS];
+    __shared__ __align__(8) uint64_t bar_s[2], bar_p[2], bar_pv[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sKV = sQ + Lay::kQBytes;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int b = 0, kvh = 0, pair = 0, qb = 0;
+    if (!k2_decode_item(p, blockIdx.x, b, kvh, pair, qb)) return;  // uniform per CTA
+    const bool two = 2 * pair + 1 < p.G;
+    const int h0 = kvh * p.G + 2 * pair;
+    const int nkv = qb + 1;  // key tiles 0..qb; tile qb is the diagonal
+    const int L = p.len[b];
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar_q), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(&bar_kv_full[s]), 1);
+            mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&bar_s[t]), 1);
+            mbar_init(smem_u32(&bar_p[t]), 128);
+            mbar_init(smem_u32(&bar_pv[t]), 1);
+        }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(&s_tmem), Lay::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&p.tm_q);
+            prefetch_tmap(&p.tm_k[b]);
+            prefetch_tmap(&p.tm_v[b]);
+            const uint32_t bq = smem_u32(&bar_q);
+            mbar_expect_tx(bq, (two ? 2 : 1) * Lay::kTileBytes);
+            const int row0 = p.cu[b] + qb * 128;
+            for (int t = 0; t < (two ? 2 : 1); ++t)
+                for (int x = 0; x < Lay::kBoxes; ++x)
+                    tma_load_3d(sQ + t * Lay::kTileBytes + x * Lay::kBoxBytes, &p.tm_q, x * 64,
+                                h0 + t, row0, bq);
+            int issued = 0;
+            for (int idx = 0; idx < 2 * nkv; ++idx, ++issued) {
+                const int st = idx % NS;
+                if (idx >= NS &&
+                    !mbar_wait(smem_u32(&bar_kv_empty[st]), ((idx / NS) - 1) & 1, &s_abort, p.err,
+                               kKernK2, 1))
+                    break;
+                const uint32_t fb = smem_u32(&bar_kv_full[st]);
+                mbar_expect_tx(fb, Lay::kTileBytes);
+                const CUtensorMap *tm = (idx & 1) ? &p.tm_v[b] : &p.tm_k[b];
+                for (int x = 0; x < Lay::kBoxes; ++x)
+                    tma_load_3d(sKV + st * Lay::kTileBytes + x * Lay::kBoxBytes, tm, x * 64,
+                                (idx >> 1) * 128, kvh, fb);
+            }
+            // Never leave a copy in flight: bounded wait for the last ones and Q.
+            int dummy = 0;
+            for (int i = max(0, issued - NS); i < issued; ++i)
+                mbar_wait(smem_u32(&bar_kv_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2, 2);
+            mbar_wait(bq, 0, &dummy, p.err, kKernK2, 3);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ tcgen05 issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+            const uint32_t tS[2] = {tmem + Lay::kColS0, tmem + Lay::kColS1};
+            const uint32_t tO[2] = {tmem + Lay::kColO0, tmem + Lay::kColO1};
+            const int ntiles = two ? 2 : 1;
+            bool ok = mbar_wait(smem_u32(&bar_q), 0, &s_abort, p.err, kKernK2, 4);
+            tc_fence_after();
+
+            // S_t = Q_t K^T: K-major A and B, 128-byte swizzle, 8-row groups 1024 B apart;
+            // K-step k of 16 elements = 32 bytes inside the 128-byte row of box k/4.
+            auto issue_s = [&](int t, int st) {
+                const uint32_t qa = sQ + t * Lay::kTileBytes;
+                const uint32_t ka = sKV + st * Lay::kTileBytes;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k / 4) * Lay::kBoxBytes + (k % 4) * 32;
+                    mma_ss(tS[t], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                           idesc_qk, k > 0 ? 1u : 0u);
+                }
+            };
+            // O_t += P_t V: P (bf16, 2 per column) from TMEM, V MN-major in smem:
+            // 64-wide d blocks one box (16 KB) apart, 8-row key groups 1024 B apart;
+            // K-step k of 16 keys = 16 rows = 2048 bytes.
+            auto issue_pv = [&](int t, int st, bool acc) {
+                const uint32_t va = sKV + st * Lay::kTileBytes;
+#pragma unroll
+                for (int k = 0; k < 128 / 16; ++k)
+                    mma_ts(tO[t], tS[t] + k * 8, sdesc_sw128(va + k * 2048, Lay::kBoxBytes, 1024),
+                           idesc_pv, (acc || k > 0) ? 1u : 0u);
+            };
+
+            if (ok) ok = mbar_wait(smem_u32(&bar_kv_full[0]), 0, &s_abort, p.err, kKernK2, 5);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < ntiles; ++t) {
+                    issue_s(t, 0);
+                    mma_commit(smem_u32(&bar_s[t]));
+                }
+                mma_commit(smem_u32(&bar_kv_empty[0]));
+            }
+            int committed = ok ? 1 : 0;  // ring slots handed back (for the final drain)
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int iv = 2 * j + 1, sv = iv % NS;
+                ok = mbar_wait(smem_u32(&bar_kv_full[sv]), (iv / NS) & 1, &s_abort, p.err, kKernK2, 6);
+                for (int t = 0; ok && t < ntiles; ++t) {
+                    ok = mbar_wait(smem_u32(&bar_p[t]), j & 1, &s_abort, p.err, kKernK2, 7);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(t, sv, j > 0);
+                    mma_commit(smem_u32(&bar_pv[t]));
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&bar_kv_empty[sv]));
+                ++committed;
+                if (j + 1 < nkv) {
+                    const int ik = 2 * (j + 1), sk = ik % NS;
+                    ok = mbar_wait(smem_u32(&bar_kv_full[sk]), (ik / NS) & 1, &s_abort, p.err,
+                                   kKernK2, 8);
+                    for (int t = 0; ok && t < ntiles; ++t) {
+                        // P_t(j) lives in the S_t columns: PV_t(j) must be done first.
+                        ok = mbar_wait(smem_u32(&bar_pv[t]), j & 1, &s_abort, p.err, kKernK2, 9);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(t, sk);
+                        mma_commit(smem_u32(&bar_s[t]));
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&bar_kv_empty[sk]));
+                    ++committed;
+                }
+            }
+            // Drain: every commit above must have arrived before the CTA exits.
+            int dummy = 0;
+            for (int i = max(0, committed - NS); i < committed; ++i)
+                mbar_wait(smem_u32(&bar_kv_empty[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2, 10);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = warp >> 2;  // 0 or 1
+        if (t == 0 || two) {
+            const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
+            const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            const uint32_t tS = tmem + (t ? Lay::kColS1 : Lay::kColS0) + lane_off;
+            const uint32_t tO = tmem + (t ? Lay::kColO1 : Lay::kColO0) + lane_off;
+            const float c = p.scale_log2;
+            float m = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nkv; ++j) {
+                ok = mbar_wait(smem_u32(&bar_s[t]), j & 1, &s_abort, p.err, kKernK2, 11);
+                ok = __all_sync(FULL, ok);
+                if (!ok) break;
+                tc_fence_after();
+                float s[128];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t u[32];
+                    tmem_ld32(tS + ch * 32, u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(u[i]);
+                }
+                if (j == nkv - 1) {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        if (i > r) s[i] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+                const float m_new = fmaxf(m, mx);
+                const float neg = m_new * c;
+                const float alpha = (m == -INFINITY) ? 0.f : k2_ex2(m * c - neg);
+                float sum = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = k2_ex2(fmaf(s[ch * 64 + 2 * i], c, -neg));
+                        const float p1 = k2_ex2(fmaf(s[ch * 64 + 2 * i + 1], c, -neg));
+                        sum += p0 + p1;
+                        pk[i] = pack_bf16(p0, p1);
+                    }
+                    tmem_st32(tS + ch * 32, pk);
+                }
+                l = fmaf(l, alpha, sum);
+                if (j > 0 && __any_sync(FULL, m_new > m)) {
+                    // PV_t(j-1) is complete: S_t(j) was issued after it finished.
+#pragma unroll
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t u[32];
+                        tmem_ld32(tO + ch * 32, u);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                        tmem_st32(tO + ch * 32, u);
+                    }
+                }
+                m = m_new;
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bar_p[t]));
+            }
+            if (ok) {
+                ok = mbar_wait(smem_u32(&bar_pv[t]), (nkv - 1) & 1, &s_abort, p.err, kKernK2, 12);
+                ok = __all_sync(FULL, ok);
+            }
+            if (ok) {
+                tc_fence_after();
+                const float inv = 1.f / l;
+                const int row = qb * 128 + r;
+                const bool valid = row < L;
+                __nv_bfloat16 *dst =
+                    p.out + (static_cast<int64_t>(p.cu[b] + row) * p.Hq + h0 + t) * D;
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t u[32];
+                    tmem_ld32(tO + ch * 32, u);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack_bf16(__uint_as_float(u[2 * i]) * inv,
+                                         __uint_as_float(u[2 * i + 1]) * inv);
+                    if (valid) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Lay::kTmemCols);
+    }
+}
+
+template <int D>
+static cudaError_t launch_k2_t(const K2Params &p, int nitems, cudaStream_t stream) {
+    constexpr int smem = K2Layout<D>::kSmemBytes;
+    static int configured_mask = 0;  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 31 && !(configured_mask & (1 << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(k2_prefill_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_mask |= 1 << dev;
+    }
+    k2_prefill_kernel<D><<<nitems, kK2Threads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_k2(const K2Params &p, int D, int nitems, cudaStream_t stream) {
+    if (nitems <= 0) return cudaSuccess;
+    if (D == 128) return launch_k2_t<128>(p, nitems, stream);
+    if (D == 64) return launch_k2_t<64>(p, nitems, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qa

@@ -1,0 +1,468 @@
+// k3_decode_splitkv.cu -- K3: one fused launch per decode step of one layer.
+//
+// For every (sequence b, kv head, head group, split) CTA:
+//   1. read pos = lens[b] (device lengths; the host never passes positions),
+//   2. RMSNorm + RoPE the HPC query heads of the group at pos (kept in
+//      registers, rounded to bf16 like the prefill path),
+//   3. the CTA owning the last split also norms + rotates k, appends k' and v
+//      to cache slot pos and attends to that new key from shared memory,
+//   4. stream its share of cache keys [0, pos) through a ring of shared-memory
+//      stages filled by bulk TMA copies (one contiguous copy for K and one
+//      for V per 32-key chunk; the K/V rows of one (sequence, kv head) are
+//      contiguous in the cache), all HPC query heads sharing every load,
+//   5. online softmax in fp32 per warp, CTA combine through shared memory,
+//   6. partial (m, l, o) to scratch; the last CTA of the group (atomic
+//      counter, no spinning) merges the splits with a warp-level log-sum-exp
+//      reduction in a fixed order, writes out[b][h] in bf16, and the last
+//      group of the sequence advances lens[b].
+// This serves the decode step of the dryft-flash-infer agent guide ("Where the
+// wins are": per-step overhead is the largest cost at batch 1 and 4, so the
+// step is one launch) against the preallocated cache of the same section.
+//
+// Lane mapping inside a consumer warp: a key row of D bf16 is read by
+// LPR = D/8 lanes (16 bytes each); RPW = 32/LPR rows are read per
+// instruction; a 32-key chunk is LPR iterations.  Partial dot products are
+// reduce-scattered over the LPR lanes so that each lane ends with the full
+// score of one key for every head.
+#include "qa_device.cuh"
+
+namespace qa {
+
+constexpr int kK3Stages = 6;
+
+template <int D, int HPC>
+struct K3Shape {
+    static constexpr int LPR = D / 8;
+    static constexpr int RPW = 32 / LPR;
+    static constexpr int NIT = kK3Chunk / RPW;
+    static_assert(NIT == LPR, "a chunk must give one key per lane");
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kChunkBytes = kK3Chunk * kRowBytes;
+    static constexpr int kRingBytes = kK3Stages * 2 * kChunkBytes;
+    static constexpr int kNewKVBytes = 2 * kRowBytes;
+    static constexpr int kRedFloats = kK3ConsumerWarps * HPC * (D + 2);
+    static constexpr int kSmemBytes = kRingBytes + kNewKVBytes + kRedFloats * 4;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+// RMSNorm + RoPE of one head row at `pos`, distributed over the LPR lanes of
+// a row group; returns this lane's 8 values rounded to bf16 (as fp32) and the
+// packed words.  Cast placement as in K1.
+template <int D>
+__device__ __forceinline__ void norm_rope_row(const __nv_bfloat16 *src, const __nv_bfloat16 *w,
+                                              const float4 *tab, float eps, int sub, float (&out)[8],
+                                              uint4 &packed) {
+    constexpr int LPR = D / 8, HALF = LPR / 2;
+    const unsigned FULL = 0xffffffffu;
+    const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(src) + sub);
+    const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(w) + sub);
+    float x[8], wf[8];
+    unpack8(xv, x);
+    unpack8(wv, wf);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+    for (int o = HALF; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+    const float r = rsqrtf(ss * (1.0f / D) + eps);
+    uint32_t yw[4], pw[4], ow[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        yw[e] = pack_bf16(wf[2 * e] * round_bf16(x[2 * e] * r),
+                          wf[2 * e + 1] * round_bf16(x[2 * e + 1] * r));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pw[e] = __shfl_xor_sync(FULL, yw[e], HALF);
+    const bool lower = sub < HALF;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float4 cs = __ldg(tab + e);
+        const float y0 = bf16lo(yw[e]), y1 = bf16hi(yw[e]);
+        const float q0 = bf16lo(pw[e]), q1 = bf16hi(pw[e]);
+        const float r0 = lower ? y0 * cs.x - q0 * cs.y : y0 * cs.x + q0 * cs.y;
+        const float r1 = lower ? y1 * cs.z - q1 * cs.w : y1 * cs.z + q1 * cs.w;
+        ow[e] = pack_bf16(r0, r1);
+        out[2 * e] = bf16lo(ow[e]);
+        out[2 * e + 1] = bf16hi(ow[e]);
+    }
+    packed = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
+// Online-softmax update of one warp with a chunk of nk (1..32) keys whose K
+// and V rows sit at Ks / Vs (row pitch D elements) in shared memory.
+template <int D, int HPC>
+__device__ __forceinline__ void consume_chunk(const __nv_bfloat16 *Ks, const __nv_bfloat16 *Vs,
+                                              int nk, const float (&qf)[HPC][8], float scale_log2,
+                                              float (&m)[HPC], float (&l)[HPC],
+                                              float (&o)[HPC][8], int sub, int grp) {
+    using Sh = K3Shape<D, HPC>;
+    constexpr int LPR = Sh::LPR, RPW = Sh::RPW, NIT = Sh::NIT;
+    const unsigned FULL = 0xffffffffu;
+
+    float acc[NIT][HPC];
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int key = it * RPW + grp;
+        uint4 kv = make_uint4(0, 0, 0, 0);
+        if (key < nk) kv = *reinterpret_cast<const uint4 *>(Ks + key * D + 8 * sub);
+        float kf[8];
+        unpack8(kv, kf);
+#pragma unroll
+        for (int g = 0; g < HPC; ++g) {
+            float a = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
+            acc[it][g] = a;
+        }
+    }
+    // Reduce-scatter over the LPR lanes of the row group: afterwards acc[0][g]
+    // holds the full dot product of key (sub * RPW + grp).
+#pragma unroll
+    for (int mk = LPR / 2; mk >= 1; mk >>= 1) {
+        const bool upper = (sub & mk) != 0;
+#pragma unroll
+        for (int i = 0; i < mk; ++i) {
+#pragma unroll
+            for (int g = 0; g < HPC; ++g) {
+                const float keep = upper ? acc[i + mk][g] : acc[i][g];
+                const float send = upper ? acc[i][g] : acc[i + mk][g];
+                acc[i][g] = keep + __shfl_xor_sync(FULL, send, mk);
+            }
+        }
+    }
+    const int my_key = sub * RPW + grp;
+    const bool my_valid = my_key < nk;
+    float pexp[HPC];
+#pragma unroll
+    for (int g = 0; g < HPC; ++g) {
+        const float s = my_valid ? acc[0][g] : -INFINITY;
+        float mx = s;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
+        const float m_new = fmaxf(m[g], mx);
+        const float alpha = (m[g] == -INFINITY) ? 0.f : ex2((m[g] - m_new) * scale_log2);
+        pexp[g] = my_valid ? ex2(fmaf(s, scale_log2, -m_new * scale_log2)) : 0.f;
+        l[g] = fmaf(l[g], alpha, pexp[g]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[g][e] *= alpha;
+        m[g] = m_new;
+    }
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int key = it * RPW + grp;
+        float pk[HPC];
+#pragma unroll
+        for (int g = 0; g < HPC; ++g) pk[g] = __shfl_sync(FULL, pexp[g], grp * LPR + it);
+        if (key < nk) {
+            const uint4 vv = *reinterpret_cast<const uint4 *>(Vs + key * D + 8 * sub);
+            float vf[8];
+            unpack8(vv, vf);
+#pragma unroll
+            for (int g = 0; g < HPC; ++g)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[g][e] = fmaf(pk[g], vf[e], o[g][e]);
+        }
+    }
+}
+
+template <int D, int HPC>
+__global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
+    k3_decode_kernel(const __grid_constant__ K3Params p) {
+    using Sh = K3Shape<D, HPC>;
+    constexpr int LPR = Sh::LPR, RPW = Sh::RPW;
+    constexpr int NW = kK3ConsumerWarps;
+    constexpr int NS = kK3Stages;
+    const unsigned FULL = 0xffffffffu;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS];
+    __shared__ int s_abort;
+    __shared__ int s_last;
+
+    uint8_t *ring = smem;
+    __nv_bfloat16 *newk = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes);
+    __nv_bfloat16 *newv = newk + D;
+    float *red = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kNewKVBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x;
+    const int kvh = blockIdx.y / p.HG, hg = blockIdx.y % p.HG;
+    const int b = blockIdx.z;
+    const int S = p.S;
+    const int pos = p.lens[b];
+    if (pos < 0 || pos >= p.cap) {
+        if (threadIdx.x == 0) set_error(p.err, kErrBounds, kKernK3, 1);
+        return;
+    }
+    const int nchunks = (pos + kK3Chunk - 1) / kK3Chunk;
+    const int cps = (nchunks + S - 1) / S;
+    const int c_begin = min(split * cps, nchunks);
+    const int c_end = min(c_begin + cps, nchunks);
+    const bool owner = split == S - 1;
+    const int64_t kv_base = static_cast<int64_t>(b) * p.seq_stride + kvh * p.head_stride;
+    const __nv_bfloat16 *Kg = p.kc + kv_base;
+    const __nv_bfloat16 *Vg = p.vc + kv_base;
+    const int h_first = kvh * p.G + hg * HPC;  // first query head of this CTA
+
+    auto ring_k = [&](int st) { return ring + st * 2 * Sh::kChunkBytes; };
+    auto ring_v = [&](int st) { return ring + st * 2 * Sh::kChunkBytes + Sh::kChunkBytes; };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NW) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t policy = policy_evict_first();
+            int issued = 0;
+            for (int c = c_begin; c < c_end; ++c, ++issued) {
+                const int st = issued % NS;
+                if (issued >= NS &&
+                    !mbar_wait(smem_u32(&bar_empty[st]), ((issued / NS) - 1) & 1, &s_abort, p.err,
+                               kKernK3, 2))
+                    break;
+                const int nk = min(kK3Chunk, pos - c * kK3Chunk);
+                const uint32_t bytes = static_cast<uint32_t>(nk) * Sh::kRowBytes;
+                const uint32_t fb = smem_u32(&bar_full[st]);
+                mbar_expect_tx(fb, 2 * bytes);
+                const int64_t off = static_cast<int64_t>(c) * kK3Chunk * D;
+                bulk_g2s_evict_first(smem_u32(ring_k(st)), Kg + off, bytes, fb, policy);
+                bulk_g2s_evict_first(smem_u32(ring_v(st)), Vg + off, bytes, fb, policy);
+            }
+            // No copy may land after the CTA exits: wait (bounded) for the last ones.
+            for (int i = max(0, issued - NS); i < issued; ++i) {
+                int dummy = 0;
+                mbar_wait(smem_u32(&bar_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK3, 3);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int sub = lane % LPR, grp = lane / LPR;
+        const float4 *tab = reinterpret_cast<const float4 *>(
+            p.rope + static_cast<int64_t>(pos) * (D / 2) + 8 * (sub % (LPR / 2)));
+        float qf[HPC][8];
+#pragma unroll
+        for (int g = 0; g < HPC; ++g) {
+            uint4 unused;
+            norm_rope_row<D>(p.q + (static_cast<int64_t>(b) * p.Hq + h_first + g) * D, p.wq, tab,
+                             p.eps, sub, qf[g], unused);
+        }
+        if (owner && warp == 0) {
+            float kf[8];
+            uint4 kp;
+            norm_rope_row<D>(p.k + (static_cast<int64_t>(b) * p.Hkv + kvh) * D, p.wk, tab, p.eps,
+                             sub, kf, kp);
+            const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(
+                                       p.v + (static_cast<int64_t>(b) * p.Hkv + kvh) * D) +
+                                   sub);
+            if (grp == 0) {
+                reinterpret_cast<uint4 *>(newk)[sub] = kp;
+                reinterpret_cast<uint4 *>(newv)[sub] = vv;
+                // Slot pos is read only by later launches.  With several head
+                // groups the first one writes.
+                if (hg == 0) {
+                    reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[sub] = kp;
+                    reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[sub] = vv;
+                }
+            }
+            __syncwarp();
+        }
+
+        float m[HPC], l[HPC], o[HPC][8];
+#pragma unroll
+        for (int g = 0; g < HPC; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+        }
+        for (int c = c_begin + warp, i = warp; c < c_end; c += NW, i += NW) {
+            const int st = i % NS;
+            bool ok = mbar_wait(smem_u32(&bar_full[st]), (i / NS) & 1, &s_abort, p.err, kKernK3, 4);
+            ok = __all_sync(FULL, ok);
+            if (!ok) break;
+            const int nk = min(kK3Chunk, pos - c * kK3Chunk);
+            consume_chunk<D, HPC>(reinterpret_cast<const __nv_bfloat16 *>(ring_k(st)),
+                                  reinterpret_cast<const __nv_bfloat16 *>(ring_v(st)), nk, qf,
+                                  p.scale_log2, m, l, o, sub, grp);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_empty[st]));
+        }
+        if (owner && warp == 0)
+            consume_chunk<D, HPC>(newk, newv, 1, qf, p.scale_log2, m, l, o, sub, grp);
+
+        // Sum the RPW row groups (same sub, different grp) and the lane sums of l.
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1)
+#pragma unroll
+            for (int g = 0; g < HPC; ++g)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[g][e] += __shfl_xor_sync(FULL, o[g][e], off);
+#pragma unroll
+        for (int g = 0; g < HPC; ++g)
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) l[g] += __shfl_xor_sync(FULL, l[g], off);
+        // Warp results -> shared memory: red[w][g][0..D) = o, [D] = m, [D+1] = l.
+#pragma unroll
+        for (int g = 0; g < HPC; ++g) {
+            float *dst = red + (warp * HPC + g) * (D + 2);
+            if (grp == 0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dst[8 * sub + e] = o[g][e];
+            }
+            if (lane == 0) {
+                dst[D] = m[g];
+                dst[D + 1] = l[g];
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- CTA combine
+    // Thread t (of the 160) combines elements (g, d) of the CTA's HPC x D partial.
+    const bool single = (S == 1);
+    const int64_t part_row = (static_cast<int64_t>(b) * p.Hq + h_first) * S + split;  // head g at + g*S
+    for (int idx = threadIdx.x; idx < HPC * D; idx += blockDim.x) {
+        const int g = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, red[(w * HPC + g) * (D + 2) + D]);
+        float Lsum = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float *src = red + (w * HPC + g) * (D + 2);
+                const float mw = src[D];
+                if (mw == -INFINITY) continue;
+                const float sc = ex2((mw - M) * p.scale_log2);
+                Lsum = fmaf(sc, src[D + 1], Lsum);
+                O = fmaf(sc, src[d], O);
+            }
+        }
+        if (single) {
+            p.out[(static_cast<int64_t>(b) * p.Hq + h_first + g) * D + d] =
+                __float2bfloat16_rn(O / Lsum);
+        } else {
+            const int64_t prow = part_row + static_cast<int64_t>(g) * S;
+            p.part_o[prow * D + d] = O;
+            if (d == 0) {
+                p.part_m[prow] = M;
+                p.part_l[prow] = Lsum;
+            }
+        }
+    }
+
+    if (!single) {
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t *cnt = p.grp_cnt + static_cast<int64_t>(b) * p.Hkv * p.HG + blockIdx.y;
+            const uint32_t prev = atomicAdd(cnt, 1u);
+            s_last = (prev == static_cast<uint32_t>(S - 1));
+            if (s_last) *cnt = 0u;  // ready for the next launch
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        // ------------------------------------------------------------ split merge
+        // Warp g merges query head g: lanes own splits (m, l) and D/32 dims of o.
+        if (warp < HPC) {
+            const int g = warp;
+            const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h_first + g) * S;
+            float ms[2], ls[2], ws[2];
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int s = lane + 32 * k2;
+                ms[k2] = s < S ? __ldcg(p.part_m + row0 + s) : -INFINITY;
+                ls[k2] = s < S ? __ldcg(p.part_l + row0 + s) : 0.f;
+            }
+            float M = fmaxf(ms[0], ms[1]);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
+            float Lsum = 0.f;
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                ws[k2] = ms[k2] == -INFINITY ? 0.f : ex2((ms[k2] - M) * p.scale_log2);
+                Lsum = fmaf(ws[k2], ls[k2], Lsum);
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) Lsum += __shfl_xor_sync(FULL, Lsum, off);
+            constexpr int DPL = D / 32;
+            float acc[DPL];
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+            for (int s = 0; s < S; ++s) {
+                const float wsv = __shfl_sync(FULL, s < 32 ? ws[0] : ws[1], s & 31);
+                const float *po = p.part_o + (row0 + s) * D + lane * DPL;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wsv, __ldcg(po + e), acc[e]);
+            }
+            const float inv = 1.f / Lsum;
+            __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(b) * p.Hq + h_first + g) * D + lane * DPL;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
+        }
+    }
+    // ---------------------------------------------------------------- length update
+    // This CTA finished its group; the last group of sequence b advances lens[b].
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t groups = static_cast<uint32_t>(p.Hkv * p.HG);
+        const uint32_t prev = atomicAdd(p.seq_cnt + b, 1u);
+        if (prev == groups - 1) {
+            p.lens[b] = pos + 1;
+            p.seq_cnt[b] = 0u;
+        }
+    }
+}
+
+template <int D, int HPC>
+static cudaError_t launch_k3_t(const K3Params &p, cudaStream_t stream) {
+    constexpr int smem = K3Shape<D, HPC>::kSmemBytes;
+    static int configured_mask = 0;  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 31 && !(configured_mask & (1 << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(k3_decode_kernel<D, HPC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_mask |= 1 << dev;
+    }
+    const dim3 grid(p.S, p.Hkv * p.HG, p.B);
+    k3_decode_kernel<D, HPC><<<grid, (kK3ConsumerWarps + 1) * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream) {
+    if (D == 128) {
+        if (HPC == 4) return launch_k3_t<128, 4>(p, stream);
+        if (HPC == 2) return launch_k3_t<128, 2>(p, stream);
+        if (HPC == 1) return launch_k3_t<128, 1>(p, stream);
+    } else if (D == 64) {
+        if (HPC == 4) return launch_k3_t<64, 4>(p, stream);
+        if (HPC == 2) return launch_k3_t<64, 2>(p, stream);
+        if (HPC == 1) return launch_k3_t<64, 1>(p, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qa

@@ -1,0 +1,547 @@
+// qa_api.cu -- the C ABI declared in include/qa.h: cache object, argument
+// validation, host mirror of the lengths, tensor-map creation and launch
+// ordering on the caller's stream.  No fallback path exists: an unsupported
+// shape or an invalid argument returns a status before anything is enqueued
+// (the boundary rule of the pegainfer PR #862 review, "add SM120 FlashInfer
+// GDN prefill candidate": invalid geometry fails validation instead of
+// silently running something else).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "qa.h"
+#include "qa_internal.h"
+
+#define QA_API extern "C" __attribute__((visibility("default")))
+
+using qa::K1Params;
+using qa::K2Params;
+using qa::K3Params;
+
+struct qa_cache {
+    qa_config cfg{};
+    int device = 0;
+    int num_sms = 0;
+    int G = 1, HPC = 1, HG = 1;
+    int64_t layer_elems = 0;   // elements of one layer's K (or V)
+    __nv_bfloat16 *K = nullptr, *V = nullptr;
+    int32_t *lens_dev = nullptr;
+    float2 *rope = nullptr;
+    float *part_m = nullptr, *part_l = nullptr, *part_o = nullptr;
+    uint32_t *grp_cnt = nullptr, *seq_cnt = nullptr;
+    uint32_t *err = nullptr;
+    std::vector<int32_t> lens_host;
+    uint64_t kv_bytes = 0, scratch_bytes = 0;
+    std::atomic<uint64_t> launches[QA_NUM_KERNELS];
+};
+
+namespace {
+
+__global__ void qa_reset_kernel(int32_t *lens, int n_lens, uint32_t *grp_cnt, int n_grp,
+                                uint32_t *seq_cnt, int n_seq) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_lens; i += gridDim.x * blockDim.x)
+        lens[i] = 0;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_grp; i += gridDim.x * blockDim.x)
+        grp_cnt[i] = 0;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_seq; i += gridDim.x * blockDim.x)
+        seq_cnt[i] = 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_shape(const qa_config &c) {
+    if (c.head_dim != 64 && c.head_dim != 128) return false;
+    if (c.n_kv_heads <= 0 || c.n_q_heads <= 0 || c.n_q_heads % c.n_kv_heads) return false;
+    const int G = c.n_q_heads / c.n_kv_heads;
+    return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+void free_all(qa_cache *c) {
+    cudaFree(c->K);
+    cudaFree(c->V);
+    cudaFree(c->lens_dev);
+    cudaFree(c->rope);
+    cudaFree(c->part_m);
+    cudaFree(c->part_l);
+    cudaFree(c->part_o);
+    cudaFree(c->grp_cnt);
+    cudaFree(c->seq_cnt);
+    cudaFree(c->err);
+}
+
+template <typename T>
+bool dev_alloc(T **p, size_t count, uint64_t &acct) {
+    const size_t bytes = std::max<size_t>(count, 1) * sizeof(T);
+    if (cudaMalloc(reinterpret_cast<void **>(p), bytes) != cudaSuccess) {
+        *p = nullptr;
+        return false;
+    }
+    acct += bytes;
+    return cudaMemset(*p, 0, bytes) == cudaSuccess;
+}
+
+qa_status check_layer(const qa_cache *c, int layer, int batch) {
+    if (!c) return QA_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= c->cfg.num_layers) return QA_ERR_INVALID_ARG;
+    if (batch < 1 || batch > c->cfg.max_batch) return QA_ERR_INVALID_ARG;
+    return QA_OK;
+}
+
+// Per-sequence K (or V) tensor map over one layer's cache: (D, L, Hkv) with the
+// head stride of the cache, 64 x 128 x 1 boxes, 128-byte swizzle; rows at or
+// beyond L read as zero.
+bool encode_kv_map(CUtensorMap *m, void *base, int D, int L, int Hkv, int cap) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                                static_cast<cuuint64_t>(Hkv)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(cap) * D * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Query tensor map over q' rows: (D, Hq, T) with 64 x 1 x 128 boxes.
+bool encode_q_map(CUtensorMap *m, void *base, int D, int Hq, int T) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                                static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(Hq) * D * 2};
+    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int choose_splits(const qa_cache *c, int batch, int pos_max) {
+    const int nchunks = (pos_max + qa::kK3Chunk - 1) / qa::kK3Chunk;
+    const int groups = batch * c->cfg.n_kv_heads * c->HG;
+    const int target = 2 * c->num_sms;  // about one wave at two CTAs per SM
+    int S = (target + groups - 1) / groups;
+    S = std::min(S, std::max(1, nchunks));
+    S = std::min(S, qa::kK3MaxSplits);
+    if (S > 1) {  // equal whole-chunk shares; drop splits that would be empty
+        const int cps = (nchunks + S - 1) / S;
+        S = (nchunks + cps - 1) / cps;
+    }
+    return std::max(S, 1);
+}
+
+// Validation shared by qa_prefill and qa_prefill_transform.
+qa_status check_prefill(const qa_cache *c, int layer, int batch, const int32_t *prompt_lens,
+                        const void *q, const void *k, const void *v, const void *wq,
+                        const void *wk, const void *dst, int64_t *T_out) {
+    qa_status st = check_layer(c, layer, batch);
+    if (st != QA_OK) return st;
+    if (!prompt_lens) return QA_ERR_INVALID_ARG;
+    int64_t T = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (prompt_lens[b] < 0) return QA_ERR_INVALID_ARG;
+        if (prompt_lens[b] > c->cfg.capacity) return QA_ERR_CAPACITY;
+        T += prompt_lens[b];
+    }
+    for (int b = 0; b < batch; ++b)
+        if (c->lens_host[static_cast<size_t>(layer) * c->cfg.max_batch + b] != 0) return QA_ERR_STATE;
+    if (T > 0) {
+        if (!q || !k || !v || !wq || !wk || !dst) return QA_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(wq) || !aligned16(wk) ||
+            !aligned16(dst))
+            return QA_ERR_ALIGNMENT;
+        if (T > (int64_t(1) << 30)) return QA_ERR_INVALID_ARG;
+    }
+    *T_out = T;
+    return QA_OK;
+}
+
+K1Params make_k1(qa_cache *c, int layer, const void *q, const void *k, const void *v,
+                 const void *wq, const void *wk, void *qp) {
+    const qa_config &g = c->cfg;
+    K1Params p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.wq = static_cast<const __nv_bfloat16 *>(wq);
+    p.wk = static_cast<const __nv_bfloat16 *>(wk);
+    p.qp = static_cast<__nv_bfloat16 *>(qp);
+    p.kc = c->K + layer * c->layer_elems;
+    p.vc = c->V + layer * c->layer_elems;
+    p.lens = c->lens_dev + static_cast<int64_t>(layer) * g.max_batch;
+    p.rope = c->rope;
+    p.err = c->err;
+    p.head_stride = static_cast<int64_t>(g.capacity) * g.head_dim;
+    p.seq_stride = p.head_stride * g.n_kv_heads;
+    p.Hq = g.n_q_heads;
+    p.Hkv = g.n_kv_heads;
+    p.cap = g.capacity;
+    p.eps = g.rms_eps;
+    return p;
+}
+
+// K1 over all prompt rows, in launches of up to kMaxSeqPerLaunch sequences.
+qa_status run_k1(qa_cache *c, int layer, int batch, const int32_t *lens, const void *q,
+                 const void *k, const void *v, const void *wq, const void *wk, void *qp,
+                 cudaStream_t s) {
+    const qa_config &g = c->cfg;
+    const int D = g.head_dim;
+    int64_t row0 = 0;
+    for (int s0 = 0; s0 < batch; s0 += qa::kMaxSeqPerLaunch) {
+        const int n = std::min(qa::kMaxSeqPerLaunch, batch - s0);
+        K1Params p = make_k1(c, layer, static_cast<const __nv_bfloat16 *>(q) + row0 * g.n_q_heads * D,
+                             static_cast<const __nv_bfloat16 *>(k) + row0 * g.n_kv_heads * D,
+                             static_cast<const __nv_bfloat16 *>(v) + row0 * g.n_kv_heads * D, wq,
+                             wk, static_cast<__nv_bfloat16 *>(qp) + row0 * g.n_q_heads * D);
+        p.nseq = n;
+        p.seq_slot0 = s0;
+        p.cu[0] = 0;
+        for (int i = 0; i < n; ++i) p.cu[i + 1] = p.cu[i] + lens[s0 + i];
+        p.T = p.cu[n];
+        if (p.T > 0) {
+            if (qa::launch_k1(p, D, s) != cudaSuccess) return QA_ERR_CUDA;
+            c->launches[QA_KERNEL_NORM_ROPE_APPEND]++;
+        }
+        row0 += p.T;
+    }
+    return QA_OK;
+}
+
+}  // namespace
+
+// ============================================================== public API
+
+QA_API int qa_abi_version(void) { return QA_ABI_VERSION; }
+
+QA_API const char *qa_status_str(qa_status s) {
+    switch (s) {
+        case QA_OK: return "ok";
+        case QA_ERR_INVALID_ARG: return "invalid argument";
+        case QA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case QA_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+        case QA_ERR_CAPACITY: return "cache capacity exceeded";
+        case QA_ERR_STATE: return "layer already holds tokens";
+        case QA_ERR_CUDA: return "CUDA runtime error";
+        case QA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case QA_ERR_DEVICE_BOUNDS: return "device position out of bounds";
+    }
+    return "unknown status";
+}
+
+QA_API qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out) {
+    if (!cfg || !out) return QA_ERR_INVALID_ARG;
+    *out = nullptr;
+    const qa_config g = *cfg;
+    if (g.num_layers <= 0 || g.max_batch <= 0 || g.capacity <= 0 || g.n_q_heads <= 0 ||
+        g.n_kv_heads <= 0 || g.head_dim <= 0 || !(g.rope_theta > 0.f) || !(g.rms_eps >= 0.f))
+        return QA_ERR_INVALID_ARG;
+    if (!supported_shape(g)) return QA_ERR_UNSUPPORTED_SHAPE;
+    if (g.capacity > (1 << 24) || g.max_batch > 65535) return QA_ERR_UNSUPPORTED_SHAPE;
+
+    qa_cache *c = new (std::nothrow) qa_cache();
+    if (!c) return QA_ERR_CUDA;
+    c->cfg = g;
+    for (auto &x : c->launches) x = 0;
+    c->G = g.n_q_heads / g.n_kv_heads;
+    c->HPC = std::min(c->G, 4);
+    c->HG = c->G / c->HPC;
+    if (cudaGetDevice(&c->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) !=
+            cudaSuccess) {
+        delete c;
+        return QA_ERR_CUDA;
+    }
+    const int D = g.head_dim;
+    c->layer_elems = static_cast<int64_t>(g.max_batch) * g.n_kv_heads * g.capacity * D;
+    const size_t kv = static_cast<size_t>(c->layer_elems) * g.num_layers;
+    const size_t parts = static_cast<size_t>(g.max_batch) * g.n_q_heads * qa::kK3MaxSplits;
+    uint64_t kvb = 0, scr = 0;
+    bool ok = dev_alloc(&c->K, kv, kvb) && dev_alloc(&c->V, kv, kvb) &&
+              dev_alloc(&c->lens_dev, static_cast<size_t>(g.num_layers) * g.max_batch, scr) &&
+              dev_alloc(&c->rope, static_cast<size_t>(g.capacity) * (D / 2), scr) &&
+              dev_alloc(&c->part_m, parts, scr) && dev_alloc(&c->part_l, parts, scr) &&
+              dev_alloc(&c->part_o, parts * D, scr) &&
+              dev_alloc(&c->grp_cnt, static_cast<size_t>(g.max_batch) * g.n_kv_heads * c->HG, scr) &&
+              dev_alloc(&c->seq_cnt, static_cast<size_t>(g.max_batch), scr) &&
+              dev_alloc(&c->err, 1, scr);
+    if (ok) {
+        // Rotary table in fp64, stored as fp32 (cos, sin): angle = pos * theta^(-2i/D).
+        std::vector<float2> tab(static_cast<size_t>(g.capacity) * (D / 2));
+        for (int pos = 0; pos < g.capacity; ++pos)
+            for (int i = 0; i < D / 2; ++i) {
+                const double a = static_cast<double>(pos) *
+                                 std::pow(static_cast<double>(g.rope_theta), -2.0 * i / D);
+                tab[static_cast<size_t>(pos) * (D / 2) + i] =
+                    make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+            }
+        ok = cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) ==
+                 cudaSuccess &&
+             cudaDeviceSynchronize() == cudaSuccess;
+    }
+    if (!ok) {
+        free_all(c);
+        delete c;
+        cudaGetLastError();
+        return QA_ERR_CUDA;
+    }
+    c->lens_host.assign(static_cast<size_t>(g.num_layers) * g.max_batch, 0);
+    c->kv_bytes = kvb;
+    c->scratch_bytes = scr;
+    *out = c;
+    return QA_OK;
+}
+
+QA_API qa_status qa_cache_free(qa_cache *c) {
+    if (!c) return QA_OK;
+    cudaDeviceSynchronize();
+    free_all(c);
+    delete c;
+    return QA_OK;
+}
+
+QA_API qa_status qa_cache_reset(qa_cache *c, void *stream) {
+    if (!c) return QA_ERR_INVALID_ARG;
+    const qa_config &g = c->cfg;
+    const int n_lens = g.num_layers * g.max_batch;
+    const int n_grp = g.max_batch * g.n_kv_heads * c->HG;
+    qa_reset_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        c->lens_dev, n_lens, c->grp_cnt, n_grp, c->seq_cnt, g.max_batch);
+    if (cudaGetLastError() != cudaSuccess) return QA_ERR_CUDA;
+    c->launches[QA_KERNEL_RESET]++;
+    std::fill(c->lens_host.begin(), c->lens_host.end(), 0);
+    return QA_OK;
+}
+
+QA_API qa_status qa_prefill_transform(qa_cache *c, int layer, int batch,
+                                      const int32_t *prompt_lens, const void *q, const void *k,
+                                      const void *v, const void *q_norm_w, const void *k_norm_w,
+                                      void *qprime_out, void *stream) {
+    int64_t T = 0;
+    qa_status st = check_prefill(c, layer, batch, prompt_lens, q, k, v, q_norm_w, k_norm_w,
+                                 qprime_out, &T);
+    if (st != QA_OK) return st;
+    st = run_k1(c, layer, batch, prompt_lens, q, k, v, q_norm_w, k_norm_w, qprime_out,
+                static_cast<cudaStream_t>(stream));
+    if (st != QA_OK) return st;
+    for (int b = 0; b < batch; ++b)
+        c->lens_host[static_cast<size_t>(layer) * c->cfg.max_batch + b] = prompt_lens[b];
+    return QA_OK;
+}
+
+QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *prompt_lens,
+                            const void *q, const void *k, const void *v, const void *q_norm_w,
+                            const void *k_norm_w, void *out, void *stream) {
+    int64_t T = 0;
+    qa_status st =
+        check_prefill(c, layer, batch, prompt_lens, q, k, v, q_norm_w, k_norm_w, out, &T);
+    if (st != QA_OK) return st;
+    const qa_config &g = c->cfg;
+    const int D = g.head_dim;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Build all tensor maps before the first launch so a failure enqueues nothing.
+    std::vector<K2Params> k2s;
+    std::vector<int> k2_items;
+    int64_t row0 = 0;
+    for (int s0 = 0; s0 < batch; s0 += qa::kMaxSeqPerLaunch) {
+        const int n = std::min(qa::kMaxSeqPerLaunch, batch - s0);
+        K2Params p{};
+        int nseq = 0, rows = 0, maxqb = 0;
+        for (int i = 0; i < n; ++i) {
+            const int L = prompt_lens[s0 + i];
+            if (L > 0) {
+                __nv_bfloat16 *kb = c->K + layer * c->layer_elems +
+                                    static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
+                __nv_bfloat16 *vb = c->V + layer * c->layer_elems +
+                                    static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
+                if (!encode_kv_map(&p.tm_k[nseq], kb, D, L, g.n_kv_heads, g.capacity) ||
+                    !encode_kv_map(&p.tm_v[nseq], vb, D, L, g.n_kv_heads, g.capacity))
+                    return QA_ERR_CUDA;
+                p.len[nseq] = L;
+                p.cu[nseq] = rows;
+                maxqb = std::max(maxqb, (L + 127) / 128);
+                ++nseq;
+            }
+            rows += L;
+        }
+        if (nseq > 0) {
+            if (!encode_q_map(&p.tm_q, static_cast<__nv_bfloat16 *>(out) + row0 * g.n_q_heads * D,
+                              D, g.n_q_heads, rows))
+                return QA_ERR_CUDA;
+            p.out = static_cast<__nv_bfloat16 *>(out) + row0 * g.n_q_heads * D;
+            p.err = c->err;
+            p.nseq = nseq;
+            p.Hq = g.n_q_heads;
+            p.Hkv = g.n_kv_heads;
+            p.G = c->G;
+            p.npairs = (c->G + 1) / 2;
+            p.max_qblocks = maxqb;
+            p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+            int items = 0;
+            for (int i = 0; i < nseq; ++i) items += (p.len[i] + 127) / 128;
+            items *= g.n_kv_heads * p.npairs;
+            k2s.push_back(p);
+            k2_items.push_back(items);
+        }
+        row0 += rows;
+    }
+    // K1 stages the normed, rotated queries in `out`; K2 reads them back and
+    // overwrites every row with its attention output (each CTA owns its rows).
+    st = run_k1(c, layer, batch, prompt_lens, q, k, v, q_norm_w, k_norm_w, out, s);
+    if (st != QA_OK) return st;
+    for (size_t i = 0; i < k2s.size(); ++i) {
+        if (qa::launch_k2(k2s[i], D, k2_items[i], s) != cudaSuccess) return QA_ERR_CUDA;
+        c->launches[QA_KERNEL_PREFILL_ATTN]++;
+    }
+    for (int b = 0; b < batch; ++b)
+        c->lens_host[static_cast<size_t>(layer) * g.max_batch + b] = prompt_lens[b];
+    return QA_OK;
+}
+
+QA_API int qa_decode_splits(qa_cache *c, int layer, int batch) {
+    if (check_layer(c, layer, batch) != QA_OK) return 0;
+    int pos_max = 0;
+    for (int b = 0; b < batch; ++b)
+        pos_max = std::max(pos_max, c->lens_host[static_cast<size_t>(layer) * c->cfg.max_batch + b]);
+    return choose_splits(c, batch, pos_max);
+}
+
+QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q, const void *k,
+                                const void *v, const void *q_norm_w, const void *k_norm_w,
+                                void *out, void *stream) {
+    qa_status st = check_layer(c, layer, batch);
+    if (st != QA_OK) return st;
+    if (!q || !k || !v || !q_norm_w || !k_norm_w || !out) return QA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_norm_w) ||
+        !aligned16(k_norm_w) || !aligned16(out))
+        return QA_ERR_ALIGNMENT;
+    const qa_config &g = c->cfg;
+    int32_t *mirror = c->lens_host.data() + static_cast<size_t>(layer) * g.max_batch;
+    int pos_max = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (mirror[b] + 1 > g.capacity) return QA_ERR_CAPACITY;
+        pos_max = std::max(pos_max, mirror[b]);
+    }
+    K3Params p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.wq = static_cast<const __nv_bfloat16 *>(q_norm_w);
+    p.wk = static_cast<const __nv_bfloat16 *>(k_norm_w);
+    p.kc = c->K + layer * c->layer_elems;
+    p.vc = c->V + layer * c->layer_elems;
+    p.lens = c->lens_dev + static_cast<int64_t>(layer) * g.max_batch;
+    p.rope = c->rope;
+    p.part_m = c->part_m;
+    p.part_l = c->part_l;
+    p.part_o = c->part_o;
+    p.grp_cnt = c->grp_cnt;
+    p.seq_cnt = c->seq_cnt;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.err = c->err;
+    p.head_stride = static_cast<int64_t>(g.capacity) * g.head_dim;
+    p.seq_stride = p.head_stride * g.n_kv_heads;
+    p.B = batch;
+    p.Hq = g.n_q_heads;
+    p.Hkv = g.n_kv_heads;
+    p.G = c->G;
+    p.HG = c->HG;
+    p.cap = g.capacity;
+    p.S = choose_splits(c, batch, pos_max);
+    p.eps = g.rms_eps;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.head_dim)));
+    if (qa::launch_k3(p, g.head_dim, c->HPC, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return QA_ERR_CUDA;
+    c->launches[QA_KERNEL_DECODE_ATTN]++;
+    for (int b = 0; b < batch; ++b) mirror[b] += 1;
+    return QA_OK;
+}
+
+QA_API qa_status qa_cache_view(qa_cache *c, int layer, void **k, void **v, int32_t **lens,
+                               int64_t strides[4]) {
+    if (!c || layer < 0 || layer >= c->cfg.num_layers) return QA_ERR_INVALID_ARG;
+    const qa_config &g = c->cfg;
+    if (k) *k = c->K + layer * c->layer_elems;
+    if (v) *v = c->V + layer * c->layer_elems;
+    if (lens) *lens = c->lens_dev + static_cast<int64_t>(layer) * g.max_batch;
+    if (strides) {
+        strides[3] = 1;
+        strides[2] = g.head_dim;
+        strides[1] = static_cast<int64_t>(g.capacity) * g.head_dim;
+        strides[0] = strides[1] * g.n_kv_heads;
+    }
+    return QA_OK;
+}
+
+QA_API qa_status qa_cache_set_lengths(qa_cache *c, int layer, const int32_t *lens_host,
+                                      void *stream) {
+    if (!c || !lens_host || layer < 0 || layer >= c->cfg.num_layers) return QA_ERR_INVALID_ARG;
+    const qa_config &g = c->cfg;
+    for (int b = 0; b < g.max_batch; ++b)
+        if (lens_host[b] < 0 || lens_host[b] > g.capacity) return QA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(c->lens_dev + static_cast<int64_t>(layer) * g.max_batch, lens_host,
+                        sizeof(int32_t) * g.max_batch, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return QA_ERR_CUDA;
+    std::copy(lens_host, lens_host + g.max_batch,
+              c->lens_host.begin() + static_cast<size_t>(layer) * g.max_batch);
+    return QA_OK;
+}
+
+QA_API qa_status qa_cache_lengths(qa_cache *c, int layer, int32_t *lens_host) {
+    if (!c || !lens_host || layer < 0 || layer >= c->cfg.num_layers) return QA_ERR_INVALID_ARG;
+    std::copy(c->lens_host.begin() + static_cast<size_t>(layer) * c->cfg.max_batch,
+              c->lens_host.begin() + static_cast<size_t>(layer + 1) * c->cfg.max_batch, lens_host);
+    return QA_OK;
+}
+
+QA_API qa_status qa_get_device_error(qa_cache *c, uint32_t *detail) {
+    if (!c) return QA_ERR_INVALID_ARG;
+    uint32_t word = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&word, c->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(c->err, 0, sizeof(word)) != cudaSuccess)
+        return QA_ERR_CUDA;
+    if (detail) *detail = word;
+    switch (word & 0xffu) {
+        case 0: return QA_OK;
+        case qa::kErrTimeout: return QA_ERR_DEVICE_TIMEOUT;
+        default: return QA_ERR_DEVICE_BOUNDS;
+    }
+}
+
+QA_API qa_status qa_stats(qa_cache *c, uint64_t launches[QA_NUM_KERNELS]) {
+    if (!c || !launches) return QA_ERR_INVALID_ARG;
+    for (int i = 0; i < QA_NUM_KERNELS; ++i) launches[i] = c->launches[i].load();
+    return QA_OK;
+}
+
+QA_API qa_status qa_memory_info(qa_cache *c, uint64_t *kv_bytes, uint64_t *scratch_bytes) {
+    if (!c) return QA_ERR_INVALID_ARG;
+    if (kv_bytes) *kv_bytes = c->kv_bytes;
+    if (scratch_bytes) *scratch_bytes = c->scratch_bytes;
+    return QA_OK;
+}

@@ -1,0 +1,88 @@
+// qa_internal.h -- definitions shared by the host launchers and the kernels
+// (parameter blocks, limits, error kinds).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the driver is reached through the runtime)
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace qa {
+
+// Error word layout: kind | kernel << 8 | site << 16.
+constexpr uint32_t kErrTimeout = 1;
+constexpr uint32_t kErrBounds = 2;
+constexpr uint32_t kKernK1 = 1, kKernK2 = 2, kKernK3 = 3;
+
+// Every spin on an mbarrier gives up after this long (a normal launch of any
+// kernel here takes well under a millisecond).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// ---------------------------------------------------------------- K1
+// Sequences per prefill launch (K1 and K2 take their per-sequence data as
+// kernel parameters; longer batches are split into several launches).
+constexpr int kMaxSeqPerLaunch = 8;
+
+struct K1Params {
+    const __nv_bfloat16 *q, *k, *v;      // [T][Hq|Hkv][D] packed prompt rows
+    const __nv_bfloat16 *wq, *wk;        // [D]
+    __nv_bfloat16 *qp;                   // [T][Hq][D] normed + rotated queries
+    __nv_bfloat16 *kc, *vc;              // layer base of the cache
+    int32_t *lens;                       // layer base of the device lengths
+    const float2 *rope;                  // [cap][D/2] (cos, sin)
+    uint32_t *err;
+    int64_t seq_stride, head_stride;     // cache strides in elements
+    int T, Hq, Hkv, cap, nseq;
+    int seq_slot0;                       // cache slot of the first sequence of this launch
+    float eps;
+    int cu[kMaxSeqPerLaunch + 1];        // row offsets of the sequences (relative to q/k/v)
+};
+
+// ---------------------------------------------------------------- K2
+constexpr int kK2Threads = 320;   // 2 softmax warpgroups, 1 TMA warp, 1 MMA warp
+constexpr int kK2BlockM = 128;    // query rows per tile
+constexpr int kK2BlockN = 128;    // keys per tile
+
+struct alignas(64) K2Params {
+    CUtensorMap tm_q;                         // q' [T][Hq][D] as (D, Hq, T)
+    CUtensorMap tm_k[kMaxSeqPerLaunch];       // per sequence: (D, L_b, Hkv) over the cache
+    CUtensorMap tm_v[kMaxSeqPerLaunch];
+    __nv_bfloat16 *out;                       // [T][Hq][D]
+    uint32_t *err;
+    int nseq, Hq, Hkv, G, npairs;             // npairs: query-head pairs per kv head
+    int len[kMaxSeqPerLaunch];
+    int cu[kMaxSeqPerLaunch];                 // first row of each sequence in q'/out
+    int max_qblocks;
+    float scale_log2;                         // log2(e) / sqrt(D)
+};
+
+// ---------------------------------------------------------------- K3
+constexpr int kK3ConsumerWarps = 4;
+constexpr int kK3Chunk = 32;        // keys per pipeline chunk
+constexpr int kK3MaxSplits = 64;
+
+struct K3Params {
+    const __nv_bfloat16 *q, *k, *v;  // [B][Hq][D], [B][Hkv][D]
+    const __nv_bfloat16 *wq, *wk;
+    __nv_bfloat16 *kc, *vc;          // layer base
+    int32_t *lens;                   // layer base [max_batch]
+    const float2 *rope;              // [cap][D/2]
+    float *part_m, *part_l, *part_o; // [B][Hq][S] / [B][Hq][S][D]
+    uint32_t *grp_cnt;               // [B][Hkv * HG]
+    uint32_t *seq_cnt;               // [B]
+    __nv_bfloat16 *out;              // [B][Hq][D]
+    uint32_t *err;
+    int64_t seq_stride, head_stride;
+    int B, Hq, Hkv, G, HG, cap, S;
+    float eps, scale_log2;
+};
+
+}  // namespace qa
+
+#include <cuda_runtime.h>
+
+namespace qa {
+// Host launchers, one per kernel file.
+cudaError_t launch_k1(const K1Params &p, int D, cudaStream_t stream);
+cudaError_t launch_k2(const K2Params &p, int D, int nitems, cudaStream_t stream);
+cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream);
+}  // namespace qa

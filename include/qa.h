@@ -1,0 +1,182 @@
+/*
+ * qa.h -- C ABI of the GB300 (sm_103a) attention hot path of a greedy
+ * Qwen3-style decoder: per-head QK-RMSNorm + rotary embedding + KV-cache
+ * append, causal grouped-query prefill attention and single-token decode
+ * attention against a preallocated bf16 KV cache.
+ *
+ * The arguments follow the pages' statement of the problem: a batch of
+ * prompts with their lengths, one new token per sequence per decode step,
+ * and a cache reset for every generate call (dryft-flash-infer agent guide,
+ * sections "What is measured" and "Where the wins are"; the htn.dryft.ai
+ * docs, "What to submit", for the Engine.generate contract of one token per
+ * sequence per step, sequences kept in arrival order).  Following the
+ * pegainfer PR #862 review ("add SM120 FlashInfer GDN prefill candidate",
+ * summary and integration-boundary comments), the kernels sit behind a narrow
+ * C ABI and an unsupported geometry or invalid argument fails validation with
+ * a status code; there is no fallback path of any kind.
+ *
+ * Conventions for every entry point:
+ *  - Tensors are bf16, contiguous, row-major, device pointers, 16-byte
+ *    aligned.  The caller owns q, k, v, the norm weights and out; the library
+ *    owns the cache, its lengths and its scratch until qa_cache_free.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  All device work is enqueued on it asynchronously; the call
+ *    returns once it is enqueued.
+ *  - Host-side validation runs before any launch; a call that returns an
+ *    error status has enqueued nothing and changed no state.
+ *  - Not thread-safe per cache: calls on one cache must come from one thread
+ *    (or be serialised by the caller).
+ */
+#ifndef QA_H_
+#define QA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QA_ABI_VERSION 1
+
+typedef enum {
+    QA_OK = 0,
+    QA_ERR_INVALID_ARG = 1,        /* null pointer, out-of-range layer/batch/length */
+    QA_ERR_UNSUPPORTED_SHAPE = 2,  /* head_dim not in {64,128}, Hq % Hkv != 0, group > 8 ... */
+    QA_ERR_ALIGNMENT = 3,          /* a tensor pointer is not 16-byte aligned */
+    QA_ERR_CAPACITY = 4,           /* a sequence would exceed the cache capacity (no eviction) */
+    QA_ERR_STATE = 5,              /* prefill on a layer that already holds tokens */
+    QA_ERR_CUDA = 6,               /* a CUDA runtime call failed (no device, launch error ...) */
+    QA_ERR_DEVICE_TIMEOUT = 7,     /* a kernel gave up a bounded wait (reported by qa_get_device_error) */
+    QA_ERR_DEVICE_BOUNDS = 8       /* a kernel saw a position outside the cache (qa_get_device_error) */
+} qa_status;
+
+/* Kernels counted by qa_stats (successful launches since qa_cache_alloc). */
+enum {
+    QA_KERNEL_NORM_ROPE_APPEND = 0, /* K1: fused QK-RMSNorm + RoPE + cache append (prefill rows) */
+    QA_KERNEL_PREFILL_ATTN = 1,     /* K2: causal GQA flash attention, TMA + tcgen05 */
+    QA_KERNEL_DECODE_ATTN = 2,      /* K3: fused norm/RoPE/append + split-KV decode + LSE merge */
+    QA_KERNEL_RESET = 3,            /* cache-length reset */
+    QA_NUM_KERNELS = 4
+};
+
+/* Geometry of one cache: num_layers independent layer caches, each holding
+ * max_batch sequences of up to `capacity` positions for n_kv_heads heads of
+ * head_dim.  Supported: head_dim in {64, 128}; n_q_heads % n_kv_heads == 0
+ * with group size n_q_heads / n_kv_heads in {1, 2, 4, 8}; capacity >= 1;
+ * rope_theta > 0; rms_eps >= 0. */
+typedef struct {
+    int num_layers;
+    int max_batch;
+    int n_q_heads;
+    int n_kv_heads;
+    int head_dim;
+    int capacity;
+    float rope_theta;   /* rotary base; angle of pair i at position p is p * theta^(-2i/head_dim) */
+    float rms_eps;      /* RMSNorm epsilon, added to the mean of squares */
+} qa_config;
+
+typedef struct qa_cache qa_cache; /* opaque */
+
+/* Allocate a cache on the current CUDA device: K and V as bf16
+ * [num_layers][max_batch][n_kv_heads][capacity][head_dim] (zero-filled),
+ * int32 lengths [num_layers][max_batch] (all zero), an fp32 rotary table
+ * [capacity][head_dim/2] of (cos, sin) built on the host in fp64, the
+ * split-KV partials of the decode kernel and an error word.  Synchronous.
+ * Errors: INVALID_ARG (cfg or out null, non-positive sizes),
+ * UNSUPPORTED_SHAPE, CUDA (allocation failed; nothing is leaked). */
+qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out);
+
+/* Free everything qa_cache_alloc allocated.  Synchronises the device first.
+ * NULL is accepted and ignored. */
+qa_status qa_cache_free(qa_cache *cache);
+
+/* Start a new generate call: every layer's lengths become 0 (device copy on
+ * `stream`, host mirror immediately).  K/V memory is not cleared; no kernel
+ * ever reads a slot at or beyond its sequence's length. */
+qa_status qa_cache_reset(qa_cache *cache, void *stream);
+
+/* Prefill one layer for `batch` prompts (sequence slots 0..batch-1).
+ * prompt_lens: HOST array [batch], each in [0, capacity].  T = sum of lengths.
+ * q: [T][Hq][D], k, v: [T][Hkv][D], packed in sequence order (sequence b's
+ * tokens follow sequence b-1's), positions restart at 0 per sequence.
+ * q_norm_w, k_norm_w: [D].  out: [T][Hq][D]; it also serves as the staging
+ * buffer for the normed, rotated queries, so it must not alias q, k or v.
+ * Work: K1 writes q' = RoPE(RMSNorm(q)) into out and k' = RoPE(RMSNorm(k)),
+ * v into cache slots 0..L_b-1, and sets the layer's lengths to prompt_lens;
+ * K2 then computes out[t][h] = sum_{j<=i} softmax_j(q'_t,h . K_j / sqrt(D)) V_j
+ * over the same sequence with kv head h / (Hq/Hkv).
+ * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (a length above capacity), STATE
+ * (the layer already holds tokens for one of the sequences: prefill appends to
+ * an empty layer only). */
+qa_status qa_prefill(qa_cache *cache, int layer, int batch, const int32_t *prompt_lens,
+                     const void *q, const void *k, const void *v,
+                     const void *q_norm_w, const void *k_norm_w, void *out, void *stream);
+
+/* One decode step of one layer: one new token for each of sequences
+ * 0..batch-1, at position pos_b = current length of sequence b.
+ * q: [batch][Hq][D], k, v: [batch][Hkv][D], weights [D], out: [batch][Hq][D].
+ * One fused launch: RMSNorm + RoPE of q and k at pos_b, append of k' and v to
+ * slot pos_b, attention of every q head over slots 0..pos_b (the new token
+ * attends to itself) split over the key range, log-sum-exp merge of the
+ * splits, length += 1.  Positions are read from the device lengths, so the
+ * step is position-agnostic on the host side.
+ * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (a sequence already holds
+ * `capacity` tokens; nothing is evicted or wrapped). */
+qa_status qa_decode_step(qa_cache *cache, int layer, int batch,
+                         const void *q, const void *k, const void *v,
+                         const void *q_norm_w, const void *k_norm_w, void *out, void *stream);
+
+/* ---- test and benchmark hooks ------------------------------------------ */
+
+/* Device pointers of one layer's K, V ([max_batch][Hkv][capacity][D] bf16)
+ * and lengths ([max_batch] int32), and the element strides of K/V for
+ * (sequence, head, position, dim).  Any output pointer may be NULL. */
+qa_status qa_cache_view(qa_cache *cache, int layer, void **k, void **v, int32_t **lens,
+                        int64_t strides[4]);
+
+/* Overwrite one layer's lengths (HOST array [max_batch], each in
+ * [0, capacity]); synchronous with respect to `stream`.  Used to decode
+ * against a cache filled through qa_cache_view. */
+qa_status qa_cache_set_lengths(qa_cache *cache, int layer, const int32_t *lens_host,
+                               void *stream);
+
+/* Copy the host mirror of one layer's lengths into lens_host[max_batch]. */
+qa_status qa_cache_lengths(qa_cache *cache, int layer, int32_t *lens_host);
+
+/* Run only K1 of a prefill: like qa_prefill, but the normed, rotated queries
+ * go to qprime_out [T][Hq][D] and no attention is computed. */
+qa_status qa_prefill_transform(qa_cache *cache, int layer, int batch, const int32_t *prompt_lens,
+                               const void *q, const void *k, const void *v,
+                               const void *q_norm_w, const void *k_norm_w, void *qprime_out,
+                               void *stream);
+
+/* Synchronise the device, read and clear the error word the kernels set when
+ * a bounded wait expired or a position fell outside the cache.  Returns
+ * QA_OK, QA_ERR_DEVICE_TIMEOUT or QA_ERR_DEVICE_BOUNDS; *detail (may be NULL)
+ * receives the raw word: bits 0-7 kind, 8-15 kernel, 16-31 site. */
+qa_status qa_get_device_error(qa_cache *cache, uint32_t *detail);
+
+/* Successful-launch counters per kernel (QA_KERNEL_*), proving which native
+ * kernels ran (the launch-counter check of the pegainfer PR #862 review). */
+qa_status qa_stats(qa_cache *cache, uint64_t launches[QA_NUM_KERNELS]);
+
+/* Bytes of device memory the cache owns: K+V, and scratch (decode partials,
+ * counters, rotary table). */
+qa_status qa_memory_info(qa_cache *cache, uint64_t *kv_bytes, uint64_t *scratch_bytes);
+
+/* Number of key-range splits the decode kernel will use for the current
+ * lengths of `layer` and `batch` sequences (a pure host computation). */
+int qa_decode_splits(qa_cache *cache, int layer, int batch);
+
+/* Static description of a status code. */
+const char *qa_status_str(qa_status status);
+
+/* QA_ABI_VERSION of the loaded library. */
+int qa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QA_H_ */

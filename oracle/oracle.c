@@ -203,18 +203,17 @@ int oracle_prefill(const oracle_geom *g, const int *plen,
 }
 
 /*
- * One decode step for every sequence: the new token of sequence b sits at
- * position pos = lens[b].  Its q and k are normed and rotated at pos, k and v
- * are appended to slot pos, lens[b] becomes pos + 1, and every q head attends
- * over slots 0..pos.  q[B][Hq][D], k/v[B][Hkv][D]; writes qp[B][Hq][D] and
- * out[B][Hq][D].  A full cache (lens[b] == cap) is an error: nothing is
- * evicted or wrapped.
+ * Transform and append the new token of every sequence: the token of
+ * sequence b sits at position pos = lens[b]; its q and k are normed and
+ * rotated at pos, k' and the raw v go to slot pos, and lens[b] becomes
+ * pos + 1.  q[B][Hq][D], k/v[B][Hkv][D]; writes qp[B][Hq][D].  A full cache
+ * (lens[b] == cap) is an error: nothing is evicted or wrapped.
  */
-int oracle_decode(const oracle_geom *g, const double *q, const double *k, const double *v,
-                  const double *wq, const double *wk,
-                  double *Kc, double *Vc, int *lens, double *qp, double *out)
+int oracle_decode_transform(const oracle_geom *g, const double *q, const double *k,
+                            const double *v, const double *wq, const double *wk,
+                            double *Kc, double *Vc, int *lens, double *qp)
 {
-    int D = g->D, G = g->Hq / g->Hkv;
+    int D = g->D;
     for (int b = 0; b < g->B; ++b)
         if (lens[b] < 0 || lens[b] >= g->cap)
             return lens[b] >= g->cap ? ORACLE_OVERFLOW : ORACLE_BAD_ARG;
@@ -229,21 +228,39 @@ int oracle_decode(const oracle_geom *g, const double *q, const double *k, const 
             memcpy(Vc + cache_row(g, b, h, pos), v + ((long)b * g->Hkv + h) * D,
                    sizeof(double) * (size_t)D);
         }
-        lens[b] = pos + 1;
         for (int h = 0; h < g->Hq; ++h) {
-            double *qrow = qp + ((long)b * g->Hq + h) * D;
             oracle_rmsnorm(D, q + ((long)b * g->Hq + h) * D, wq, g->eps, tmp);
-            oracle_rope(D, (double)pos, g->theta, tmp, qrow);
-            int rc = oracle_attend(D, pos + 1, qrow, Kc + cache_row(g, b, h / G, 0),
-                                   Vc + cache_row(g, b, h / G, 0), D,
-                                   out + ((long)b * g->Hq + h) * D, NULL);
-            if (rc != ORACLE_OK) {
-                free(tmp);
-                return rc;
-            }
+            oracle_rope(D, (double)pos, g->theta, tmp, qp + ((long)b * g->Hq + h) * D);
         }
+        lens[b] = pos + 1;
     }
     free(tmp);
+    return ORACLE_OK;
+}
+
+/*
+ * One decode step for every sequence: transform and append as above, then
+ * every q head attends over slots 0..pos of its kv head (the new token
+ * attends to itself).  Writes qp[B][Hq][D] and out[B][Hq][D].
+ */
+int oracle_decode(const oracle_geom *g, const double *q, const double *k, const double *v,
+                  const double *wq, const double *wk,
+                  double *Kc, double *Vc, int *lens, double *qp, double *out)
+{
+    int D = g->D, G = g->Hq / g->Hkv;
+    int rc = oracle_decode_transform(g, q, k, v, wq, wk, Kc, Vc, lens, qp);
+    if (rc != ORACLE_OK)
+        return rc;
+    for (int b = 0; b < g->B; ++b) {
+        int n = lens[b];
+        for (int h = 0; h < g->Hq; ++h) {
+            rc = oracle_attend(D, n, qp + ((long)b * g->Hq + h) * D,
+                               Kc + cache_row(g, b, h / G, 0), Vc + cache_row(g, b, h / G, 0), D,
+                               out + ((long)b * g->Hq + h) * D, NULL);
+            if (rc != ORACLE_OK)
+                return rc;
+        }
+    }
     return ORACLE_OK;
 }
 

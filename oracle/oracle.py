@@ -69,6 +69,8 @@ def _load():
         lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_decode.argtypes = [g, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _ip, _dp, _dp]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_decode_transform.argtypes = [g, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _ip, _dp]
+        lib.oracle_decode_transform.restype = ctypes.c_int
         lib.oracle_reset.argtypes = [g, _ip]
         lib.oracle_reset.restype = None
         _lib = lib
@@ -177,6 +179,23 @@ class OracleLayer:
             _p(qp), _p(self.Kc), _p(self.Vc), self.lens.ctypes.data_as(_ip), _p(out))
         _check(rc, "prefill")
         return qp, out
+
+    def decode_transform(self, q, k, v, wq, wk) -> np.ndarray:
+        """Norm + rotate the new tokens, append them; no attention.  Returns q'."""
+        q, k, v, wq, wk = map(_f64, (q, k, v, wq, wk))
+        qp = np.empty_like(q)
+        rc = _load().oracle_decode_transform(
+            ctypes.byref(self._cg), _p(q), _p(k), _p(v), _p(wq), _p(wk), _p(self.Kc), _p(self.Vc),
+            self.lens.ctypes.data_as(_ip), _p(qp))
+        _check(rc, "decode_transform")
+        return qp
+
+    def attend_cached(self, b: int, h: int, qp_row) -> np.ndarray:
+        """Attention of a query of head h over all cached slots of sequence b."""
+        G = self.g.Hq // self.g.Hkv
+        n = int(self.lens[b])
+        out, _ = attend(qp_row, self.Kc[b, h // G, :n], self.Vc[b, h // G, :n])
+        return out
 
     def decode(self, q, k, v, wq, wk):
         q, k, v, wq, wk = map(_f64, (q, k, v, wq, wk))
