@@ -1,0 +1,464 @@
+#!/usr/bin/env python
+"""Benchmark of the GQA attention hot path on GB300.
+
+One step = one generate call's attention work for one layer of the Qwen3-4B
+geometry (32 q / 8 kv heads, head_dim 128) at batch 4: cache reset, prefill of
+four 2048-token prompts (K1 fused norm/RoPE/append + K2 tcgen05 causal
+attention) and 128 decode steps (K3, one fused launch each), all through the
+C ABI.  Inputs are synthetic (seeded N(0,1) bf16, see configs.py) and resident
+in HBM; L2 is flushed (256 MiB write) between steps, outside the timed events.
+
+Prints one JSON line.  `--impl reference` times the fp64 CPU oracle instead
+(single-threaded, a bounded sample of the same step, extrapolated).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step & HBM GB/s; prefill-attn TFLOP/s; fraction of GB300 roofline"
+UNIT = "µs/step"
+STEP_DEF = ("reset + prefill of 4 x 2048-token prompts + 128 decode steps, one attention layer "
+            "(32 q / 8 kv heads, head_dim 128, cache capacity 2176)")
+
+
+# ---------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def git_rev():
+    try:
+        rev = subprocess.run(["git", "rev-parse", "--short", "HEAD"], cwd=ROOT, capture_output=True,
+                             text=True).stdout.strip()
+        dirty = subprocess.run(["git", "status", "--porcelain"], cwd=ROOT, capture_output=True,
+                               text=True).stdout.strip() != ""
+        return rev or None, dirty
+    except OSError:
+        return None, None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "reasons": parts[5:9],
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else None})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        active = sorted({names[i] for r in rows for i, v in enumerate(r["reasons"])
+                         if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": active,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle sample
+class OracleStepModel:
+    """Times the oracle's two parts separately and extrapolates one full step."""
+
+    def __init__(self, w, inp, frac_rows):
+        import numpy as np
+        from gqa_attention_preallocated_qa_gb300.inputs import bf16_bits_to_f64 as F
+        from oracle import oracle
+        self.w, self.frac = w, frac_rows
+        self.o = oracle
+        g = oracle.Geometry(w.B, w.Hq, w.Hkv, w.D, w.cap, w.theta, w.eps)
+        self.lay = oracle.OracleLayer(g)
+        self.q, self.k, self.v, self.wq, self.wk = (F(a) for a in (inp.q, inp.k, inp.v, inp.wq,
+                                                                    inp.wk))
+        self.lay.prefill_transform(w.prompt_lens, self.q, self.k, self.v, self.wq, self.wk)
+        self.lens0 = self.lay.lens.copy()
+        self.cu = np.concatenate([[0], np.cumsum(w.prompt_lens)])
+        # strided rows starting mid-stride: their mean key count is the prompt's mean
+        self.rows = [(b, i) for b in range(w.B)
+                     for i in range(frac_rows // 2, w.prompt_lens[b], frac_rows)]
+        self.d = tuple(F(a) for a in (inp.dq[0], inp.dk[0], inp.dv[0]))
+        self.desc = (f"every {frac_rows}th prompt row (from row {frac_rows // 2}) of each sequence (norm + RoPE + causal "
+                     f"attention, all heads) scaled x{frac_rows}, plus one full decode step "
+                     f"(all 4 x 32 heads over 2049 keys) scaled x{w.steps}")
+
+    def sample(self):
+        w, o, lay = self.w, self.o, self.lay
+        t0 = time.perf_counter()
+        for b, i in self.rows:
+            t = self.cu[b] + i
+            for h in range(w.Hq):
+                lay.prefill_row(b, h, i, o.rope(o.rmsnorm(self.q[t, h], self.wq, w.eps), i, w.theta))
+            for h in range(w.Hkv):
+                o.rope(o.rmsnorm(self.k[t, h], self.wk, w.eps), i, w.theta)
+        t1 = time.perf_counter()
+        lay.lens[...] = self.lens0
+        lay.decode(*self.d, self.wq, self.wk)
+        t2 = time.perf_counter()
+        return (t1 - t0) * self.frac + (t2 - t1) * w.steps, t2 - t0  # (extrapolated s, spent s)
+
+
+# ---------------------------------------------------------------- distributed
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, ws: int) -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from gqa_attention_preallocated_qa_gb300 import binding as qa
+    from gqa_attention_preallocated_qa_gb300.configs import QWEN3_4B_B4 as w
+
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    pk = peaks()
+    inp = w.inputs()
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+    q, k, v, wq, wk = (dev(a) for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+    dq, dk, dv = dev(inp.dq), dev(inp.dk), dev(inp.dv)
+    out = torch.empty_like(q)
+    dout = torch.empty((w.steps, w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    h = qa.qa_cache_alloc(1, w.B, w.Hq, w.Hkv, w.D, w.cap, w.theta, w.eps)
+    lib = qa.lib
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    lens_arr = qa._i32(w.prompt_lens)
+    P = {n: t.data_ptr() for n, t in dict(q=q, k=k, v=v, wq=wq, wk=wk, out=out).items()}
+    dq_p = [dq[s].data_ptr() for s in range(w.steps)]
+    dk_p = [dk[s].data_ptr() for s in range(w.steps)]
+    dv_p = [dv[s].data_ptr() for s in range(w.steps)]
+    do_p = [dout[s].data_ptr() for s in range(w.steps)]
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        st = lib.qa_cache_reset(h, sh)
+        if evs:
+            evs[1].record(stream)
+        st |= lib.qa_prefill(h, 0, w.B, lens_arr, P["q"], P["k"], P["v"], P["wq"], P["wk"],
+                             P["out"], sh)
+        if evs:
+            evs[2].record(stream)
+        for s in range(w.steps):
+            st |= lib.qa_decode_step(h, 0, w.B, dq_p[s], dk_p[s], dv_p[s], P["wq"], P["wk"],
+                                     do_p[s], sh)
+        if evs:
+            evs[3].record(stream)
+        if st:
+            raise RuntimeError(f"qa call failed with status {st}")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    err = qa.qa_get_device_error(h)
+    if err[0]:
+        raise RuntimeError(f"device error after warm-up: {err}")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    stats0 = qa.qa_stats(h)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            step(events[i])
+        torch.cuda.synchronize()
+    barrier(ws)
+    stats1 = qa.qa_stats(h)
+    launches = sum(stats1[n] - stats0[n] for n in stats1)
+    err = qa.qa_get_device_error(h)
+    if err[0]:
+        raise RuntimeError(f"device error in the timed region: {err}")
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in events]
+    pre_ms = [e[1].elapsed_time(e[2]) for e in events]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in events]
+    total_ms = sum(step_ms)
+    total_ms_max = reduce_max(total_ms, ws)
+    ms_per_step = total_ms_max / args.steps
+
+    # algorithmic work
+    flops = w.causal_flops()
+    L0 = w.prompt_lens[0]
+    dec_bytes = sum(w.B * w.Hkv * (L0 + s + 1) * w.D * 2 * 2 for s in range(w.steps))
+    pre_us = statistics.median(pre_ms) * 1e3
+    dec_us_per_step = statistics.median(dec_ms) * 1e3 / w.steps
+    pre_tflops = flops / (pre_us * 1e-6) / 1e12
+    dec_gbs = dec_bytes / w.steps / (dec_us_per_step * 1e-6) / 1e9
+    dec_share = sum(dec_ms) / total_ms
+
+    # e2e through the public API with host buffers (pinned), copies inside the timed region
+    e2e = run_e2e(args, qa, h, w, inp, stream)
+
+    roof_dec = {"bound": "hbm", "kernel": "k3_decode_kernel<128,4>", "achieved": round(dec_gbs, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(dec_gbs / pk["hbm_gbs"], 4),
+                "traffic": traffic_for("k3_decode", dec_bytes / w.steps),
+                "per_launch_bytes": round(dec_bytes / w.steps),
+                "duration": "decode span / 128 launches (includes inter-launch gaps)"}
+    roof_pre = {"bound": "tensor", "kernel": "k1 + k2_prefill_kernel<128>",
+                "achieved": round(pre_tflops, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(pre_tflops / pk["bf16_tflops"], 4),
+                "traffic": traffic_for("k2_prefill", None), "per_launch_flops": flops,
+                "duration": "prefill call (K1 + K2) span"}
+    dominant = roof_dec if dec_share >= 0.5 else roof_pre
+    rev, dirty = git_rev()
+    line = {
+        "metric": METRIC, "value": round(ms_per_step * 1e3 / ws, 2), "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "qwen3_4b_b4_p2048_d128", "step": STEP_DEF, "batch": w.B,
+                   "prompt": w.prompt_lens[0], "decode_steps": w.steps, "layers": 1,
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "components": {
+            "decode_attn_us_per_step": round(dec_us_per_step, 3),
+            "decode_hbm_gbs": round(dec_gbs, 1),
+            "decode_frac_of_measured_hbm": round(dec_gbs / pk["hbm_gbs"], 4),
+            "prefill_attn_us": round(pre_us, 2),
+            "prefill_attn_tflops": round(pre_tflops, 1),
+            "prefill_frac_of_measured_bf16": round(pre_tflops / pk["bf16_tflops"], 4),
+            "decode_time_share": round(dec_share, 4),
+            "step_ms_p50": round(statistics.median(step_ms), 4),
+            "step_ms_spread": round((max(step_ms) - min(step_ms)) / statistics.median(step_ms), 4),
+            "peaks": pk["source"],
+        },
+        "roofline": dominant,
+        "roofline_all": [roof_dec, roof_pre],
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "git": {"rev": rev, "dirty": dirty},
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        model = OracleStepModel(w, inp, frac_rows=64)
+        ests, spent = [], 0.0
+        while spent < args.cpu_budget:
+            est, sp = model.sample()
+            ests.append(est)
+            spent += sp
+        line["cpu_baseline"] = {"value": round(statistics.median(ests) * 1e6, 1), "unit": UNIT,
+                                "cores": 1, "kind": "oracle",
+                                "sample": model.desc + f"; {len(ests)} samples, {spent:.1f} s",
+                                "host_cpus": os.cpu_count()}
+    qa.qa_cache_free(h)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, qa, h, w, inp, stream):
+    """Same step through the public API with HOST buffers: every step copies its
+    inputs (prompt q/k/v, norm weights, the 128 decode tokens' q/k/v) from
+    pinned host memory to the device and reads its results (prefill output and
+    the 128 decode outputs) back, all inside the timed events."""
+    import numpy as np
+    import torch
+    lib = qa.lib
+    sh = stream.cuda_stream
+
+    def flat(*arrays):
+        return np.concatenate([np.ascontiguousarray(a).reshape(-1) for a in arrays])
+
+    host_in = torch.from_numpy(flat(inp.q, inp.k, inp.v, inp.wq, inp.wk, inp.dq, inp.dk,
+                                    inp.dv).view(np.int16)).view(torch.bfloat16).pin_memory()
+    dev_in = torch.empty_like(host_in, device="cuda")
+    sizes = [a.size for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk, inp.dq, inp.dk, inp.dv)]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    ptr = [dev_in.data_ptr() + 2 * int(o) for o in offs[:-1]]
+    q_p, k_p, v_p, wq_p, wk_p, dq_p, dk_p, dv_p = ptr
+    step_q, step_kv = w.B * w.Hq * w.D * 2, w.B * w.Hkv * w.D * 2
+    T = w.T
+    dev_out = torch.empty(T * w.Hq * w.D + w.steps * w.B * w.Hq * w.D, dtype=torch.bfloat16,
+                          device="cuda")
+    host_out = torch.empty(dev_out.shape, dtype=torch.bfloat16).pin_memory()
+    out_p = dev_out.data_ptr()
+    dout_p = out_p + T * w.Hq * w.D * 2
+    lens_arr = qa._i32(w.prompt_lens)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def step():
+        dev_in.copy_(host_in, non_blocking=True)
+        st = lib.qa_cache_reset(h, sh)
+        st |= lib.qa_prefill(h, 0, w.B, lens_arr, q_p, k_p, v_p, wq_p, wk_p, out_p, sh)
+        for s in range(w.steps):
+            st |= lib.qa_decode_step(h, 0, w.B, dq_p + s * step_q, dk_p + s * step_kv,
+                                     dv_p + s * step_kv, wq_p, wk_p, dout_p + s * step_q, sh)
+        host_out.copy_(dev_out, non_blocking=True)
+        if st:
+            raise RuntimeError(f"qa call failed with status {st}")
+
+    for _ in range(3):
+        step()
+    n = max(3, min(args.steps, args.e2e_steps))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / n
+    return {"value": round(ms * 1e3, 2), "unit": UNIT, "h2d_bytes_per_step": host_in.numel() * 2,
+            "d2h_bytes_per_step": host_out.numel() * 2, "steps": n, "host_buffers": "pinned"}
+
+
+def traffic_for(kernel: str, algorithmic_bytes):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else null)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = {"k3_decode": "k3_decode_splitkv.cu", "k2_prefill": "k2_prefill_tcgen05.cu"}[kernel]
+    try:
+        with open(path) as fh:
+            d = json.load(fh)[kernel]
+        with open(os.path.join(ROOT, "gqa_attention_preallocated_qa_gb300", "csrc", src), "rb") as fh:
+            digest = hashlib.sha256(fh.read()).hexdigest()[:16]
+        if d.get("source_sha256_16") != digest:
+            return None
+        return d["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The oracle as it stands, single-threaded on the host, on a bounded sample
+    of the same step per timed step; reports the extrapolated full-step time."""
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    from gqa_attention_preallocated_qa_gb300.configs import QWEN3_4B_B4 as w
+    inp = w.inputs()
+    model = OracleStepModel(w, inp, frac_rows=2048)
+    for _ in range(args.warmup):
+        model.sample()
+    ests, spent = [], 0.0
+    for _ in range(args.steps):
+        est, sp = model.sample()
+        ests.append(est)
+        spent += sp
+    value = statistics.median(ests) * 1e6
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value / 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": "qwen3_4b_b4_p2048_d128", "step": STEP_DEF, "batch": w.B,
+                       "prompt": w.prompt_lens[0], "decode_steps": w.steps, "layers": 1},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": model.desc + f"; {len(ests)} samples, {spent:.1f} s"},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -20,11 +20,16 @@
 
 namespace qa {
 
+// Head rows handled by one row group (LPR lanes): all their loads are issued
+// before any arithmetic, so each lane keeps kRowsPerGroup 16-byte loads in flight.
+constexpr int kRowsPerGroup = 4;
+
 template <int D>
 __global__ void __launch_bounds__(256) k1_norm_rope_append_kernel(const __grid_constant__ K1Params p) {
     constexpr int LPR = D / 8;     // lanes per head row
-    constexpr int RPW = 32 / LPR;  // head rows per warp
+    constexpr int RPW = 32 / LPR;  // row groups per warp
     constexpr int HALF = LPR / 2;  // lane distance of the rotate-half partner
+    constexpr int R = kRowsPerGroup;
     const unsigned FULL = 0xffffffffu;
 
     const int lane = threadIdx.x & 31;
@@ -32,106 +37,111 @@ __global__ void __launch_bounds__(256) k1_norm_rope_append_kernel(const __grid_c
     const int grp = lane / LPR;
     const int H3 = p.Hq + 2 * p.Hkv;
     const int64_t total = static_cast<int64_t>(p.T) * H3;
-    const int64_t row =
-        (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * RPW + grp;
-    const bool valid = row < total;
+    const int64_t row0 =
+        ((static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * RPW + grp) * R;
 
     if (blockIdx.x == 0 && threadIdx.x < p.nseq)
         p.lens[p.seq_slot0 + threadIdx.x] = p.cu[threadIdx.x + 1] - p.cu[threadIdx.x];
 
-    const int64_t t = valid ? row / H3 : 0;
-    const int j = valid ? static_cast<int>(row % H3) : 0;
-    int b = 0;
-    while (b + 1 < p.nseq && t >= p.cu[b + 1]) ++b;
-    const int pos = static_cast<int>(t - p.cu[b]);
+    const uint4 wqv = __ldg(reinterpret_cast<const uint4 *>(p.wq) + sub);
+    const uint4 wkv = __ldg(reinterpret_cast<const uint4 *>(p.wk) + sub);
 
-    const __nv_bfloat16 *src;
-    const __nv_bfloat16 *w;
-    __nv_bfloat16 *dst;
-    bool is_v = false;
-    const int64_t slot = static_cast<int64_t>(p.seq_slot0 + b) * p.seq_stride;
-    if (j < p.Hq) {
-        src = p.q + (t * p.Hq + j) * D;
-        w = p.wq;
-        dst = p.qp + (t * p.Hq + j) * D;
-    } else if (j < p.Hq + p.Hkv) {
-        const int h = j - p.Hq;
-        src = p.k + (t * p.Hkv + h) * D;
-        w = p.wk;
-        dst = p.kc + slot + h * p.head_stride + static_cast<int64_t>(pos) * D;
-    } else {
-        const int h = j - p.Hq - p.Hkv;
-        src = p.v + (t * p.Hkv + h) * D;
-        w = p.wk;
-        dst = p.vc + slot + h * p.head_stride + static_cast<int64_t>(pos) * D;
-        is_v = true;
-    }
-    if (valid && pos >= p.cap) {  // cannot happen after host validation; never write out of bounds
-        set_error(p.err, kErrBounds, kKernK1, 1);
-    }
-    const bool active = valid && pos < p.cap;
-
-    uint4 xv = make_uint4(0, 0, 0, 0);
-    if (active) xv = __ldg(reinterpret_cast<const uint4 *>(src) + sub);
-    const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(w) + sub);
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-    float x[8], wf[8];
+    // Phase 1: addresses and loads of the R rows.
+    uint4 xv[R];
+    __nv_bfloat16 *dst[R];
+    int pos_r[R];
+    uint32_t kind[R];  // 0 = q, 1 = k, 2 = v, 3 = inactive
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        x[2 * e] = bf16lo(xw[e]);
-        x[2 * e + 1] = bf16hi(xw[e]);
-        wf[2 * e] = bf16lo(ww[e]);
-        wf[2 * e + 1] = bf16hi(ww[e]);
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-#pragma unroll
-    for (int o = HALF; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
-    const float r = rsqrtf(ss * (1.0f / D) + p.eps);
-
-    // y = bf16(w * bf16(x * r)), kept packed (exact bf16 values) for the exchange.
-    uint32_t yw[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float a = wf[2 * e] * round_bf16(x[2 * e] * r);
-        const float c = wf[2 * e + 1] * round_bf16(x[2 * e + 1] * r);
-        yw[e] = pack_bf16(a, c);
-    }
-    uint32_t pw[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) pw[e] = __shfl_xor_sync(FULL, yw[e], HALF);
-
-    const bool lower = sub < HALF;
-    const int i0 = 8 * (sub % HALF);
-    const float4 *tab = reinterpret_cast<const float4 *>(p.rope + static_cast<int64_t>(pos) * (D / 2) + i0);
-    uint32_t ow[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float4 cs = make_float4(1.f, 0.f, 1.f, 0.f);  // (cos_a, sin_a, cos_b, sin_b)
-        if (active) cs = __ldg(tab + e);
-        const float y0 = bf16lo(yw[e]), y1 = bf16hi(yw[e]);
-        const float q0 = bf16lo(pw[e]), q1 = bf16hi(pw[e]);
-        float r0, r1;
-        if (lower) {
-            r0 = y0 * cs.x - q0 * cs.y;
-            r1 = y1 * cs.z - q1 * cs.w;
+    for (int r = 0; r < R; ++r) {
+        const int64_t row = row0 + r;
+        const bool valid = row < total;
+        const int64_t t = valid ? row / H3 : 0;
+        const int j = valid ? static_cast<int>(row % H3) : 0;
+        int b = 0;
+        while (b + 1 < p.nseq && t >= p.cu[b + 1]) ++b;
+        const int pos = static_cast<int>(t - p.cu[b]);
+        const int64_t slot = static_cast<int64_t>(p.seq_slot0 + b) * p.seq_stride;
+        const __nv_bfloat16 *src;
+        if (j < p.Hq) {
+            src = p.q + (t * p.Hq + j) * D;
+            dst[r] = p.qp + (t * p.Hq + j) * D;
+            kind[r] = 0;
+        } else if (j < p.Hq + p.Hkv) {
+            const int h = j - p.Hq;
+            src = p.k + (t * p.Hkv + h) * D;
+            dst[r] = p.kc + slot + h * p.head_stride + static_cast<int64_t>(pos) * D;
+            kind[r] = 1;
         } else {
-            r0 = y0 * cs.x + q0 * cs.y;
-            r1 = y1 * cs.z + q1 * cs.w;
+            const int h = j - p.Hq - p.Hkv;
+            src = p.v + (t * p.Hkv + h) * D;
+            dst[r] = p.vc + slot + h * p.head_stride + static_cast<int64_t>(pos) * D;
+            kind[r] = 2;
         }
-        ow[e] = pack_bf16(r0, r1);
+        if (valid && pos >= p.cap) {  // cannot happen after host validation; never write out of bounds
+            set_error(p.err, kErrBounds, kKernK1, 1);
+        }
+        const bool active = valid && pos < p.cap;
+        if (!active) kind[r] = 3;
+        pos_r[r] = active ? pos : 0;
+        xv[r] = active ? __ldg(reinterpret_cast<const uint4 *>(src) + sub) : make_uint4(0, 0, 0, 0);
     }
-    if (active) {
-        uint4 o4 = is_v ? xv : make_uint4(ow[0], ow[1], ow[2], ow[3]);
-        reinterpret_cast<uint4 *>(dst)[sub] = o4;
+
+    // Phase 2: norm, rotate, store.
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint4 wv = kind[r] == 0 ? wqv : wkv;
+        const uint32_t xw[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+        float x[8], wf[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[2 * e] = bf16lo(xw[e]);
+            x[2 * e + 1] = bf16hi(xw[e]);
+            wf[2 * e] = bf16lo(ww[e]);
+            wf[2 * e + 1] = bf16hi(ww[e]);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+        for (int o = HALF; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+        const float rr = rsqrtf(ss * (1.0f / D) + p.eps);
+
+        // y = bf16(w * bf16(x * r)), kept packed (exact bf16 values) for the exchange.
+        uint32_t yw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = wf[2 * e] * round_bf16(x[2 * e] * rr);
+            const float c = wf[2 * e + 1] * round_bf16(x[2 * e + 1] * rr);
+            yw[e] = pack_bf16(a, c);
+        }
+        uint32_t pw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pw[e] = __shfl_xor_sync(FULL, yw[e], HALF);
+
+        const bool lower = sub < HALF;
+        const float4 *tab = reinterpret_cast<const float4 *>(
+            p.rope + static_cast<int64_t>(pos_r[r]) * (D / 2) + 8 * (sub % HALF));
+        uint32_t ow[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 cs = __ldg(tab + e);  // (cos_a, sin_a, cos_b, sin_b)
+            const float y0 = bf16lo(yw[e]), y1 = bf16hi(yw[e]);
+            const float q0 = bf16lo(pw[e]), q1 = bf16hi(pw[e]);
+            const float r0 = lower ? y0 * cs.x - q0 * cs.y : y0 * cs.x + q0 * cs.y;
+            const float r1 = lower ? y1 * cs.z - q1 * cs.w : y1 * cs.z + q1 * cs.w;
+            ow[e] = pack_bf16(r0, r1);
+        }
+        if (kind[r] != 3) {
+            const uint4 o4 = kind[r] == 2 ? xv[r] : make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            reinterpret_cast<uint4 *>(dst[r])[sub] = o4;
+        }
     }
 }
 
 cudaError_t launch_k1(const K1Params &p, int D, cudaStream_t stream) {
     const int64_t rows = static_cast<int64_t>(p.T) * (p.Hq + 2 * p.Hkv);
-    const int rows_per_block = (256 / 32) * (32 / (D / 8));
+    const int rows_per_block = (256 / 32) * (32 / (D / 8)) * kRowsPerGroup;
     const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;

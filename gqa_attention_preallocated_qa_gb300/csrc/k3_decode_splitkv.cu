@@ -57,6 +57,22 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
     f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
 }
 
+// Eight bf16 as four fp32 pairs (element 2i in .x, 2i+1 in .y).
+__device__ __forceinline__ void unpack4x2(const uint4 v, float2 (&f)[4]) {
+    f[0] = make_float2(bf16lo(v.x), bf16hi(v.x));
+    f[1] = make_float2(bf16lo(v.y), bf16hi(v.y));
+    f[2] = make_float2(bf16lo(v.z), bf16hi(v.z));
+    f[3] = make_float2(bf16lo(v.w), bf16hi(v.w));
+}
+
+// One gpu-scope acquire-release increment (publishes this CTA's earlier writes,
+// ordered by a preceding __syncthreads, and sees every earlier incrementer's).
+__device__ __forceinline__ uint32_t atomic_inc_acq_rel(uint32_t *p) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
 // RMSNorm + RoPE of one head row at `pos`, distributed over the LPR lanes of
 // a row group; returns this lane's 8 values rounded to bf16 (as fp32) and the
 // packed words.  Cast placement as in K1.
@@ -103,27 +119,28 @@ __device__ __forceinline__ void norm_rope_row(const __nv_bfloat16 *src, const __
 // and V rows sit at Ks / Vs (row pitch D elements) in shared memory.
 template <int D, int HPC>
 __device__ __forceinline__ void consume_chunk(const __nv_bfloat16 *Ks, const __nv_bfloat16 *Vs,
-                                              int nk, const float (&qf)[HPC][8], float scale_log2,
+                                              int nk, const float2 (&q2)[HPC][4], float scale_log2,
                                               float (&m)[HPC], float (&l)[HPC],
-                                              float (&o)[HPC][8], int sub, int grp) {
+                                              float2 (&o2)[HPC][4], int sub, int grp) {
     using Sh = K3Shape<D, HPC>;
     constexpr int LPR = Sh::LPR, RPW = Sh::RPW, NIT = Sh::NIT;
     const unsigned FULL = 0xffffffffu;
 
+    // Partial dot products over this lane's 8 dims, two at a time (packed fp32x2 FMA).
     float acc[NIT][HPC];
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
         const int key = it * RPW + grp;
         uint4 kv = make_uint4(0, 0, 0, 0);
         if (key < nk) kv = *reinterpret_cast<const uint4 *>(Ks + key * D + 8 * sub);
-        float kf[8];
-        unpack8(kv, kf);
+        float2 k2[4];
+        unpack4x2(kv, k2);
 #pragma unroll
         for (int g = 0; g < HPC; ++g) {
-            float a = 0.f;
+            float2 a = __fmul2_rn(q2[g][0], k2[0]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
-            acc[it][g] = a;
+            for (int e = 1; e < 4; ++e) a = __ffma2_rn(q2[g][e], k2[e], a);
+            acc[it][g] = a.x + a.y;
         }
     }
     // Reduce-scatter over the LPR lanes of the row group: afterwards acc[0][g]
@@ -154,8 +171,9 @@ __device__ __forceinline__ void consume_chunk(const __nv_bfloat16 *Ks, const __n
         const float alpha = (m[g] == -INFINITY) ? 0.f : ex2((m[g] - m_new) * scale_log2);
         pexp[g] = my_valid ? ex2(fmaf(s, scale_log2, -m_new * scale_log2)) : 0.f;
         l[g] = fmaf(l[g], alpha, pexp[g]);
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[g][e] *= alpha;
+        for (int e = 0; e < 4; ++e) o2[g][e] = __fmul2_rn(o2[g][e], a2);
         m[g] = m_new;
     }
 #pragma unroll
@@ -166,18 +184,20 @@ __device__ __forceinline__ void consume_chunk(const __nv_bfloat16 *Ks, const __n
         for (int g = 0; g < HPC; ++g) pk[g] = __shfl_sync(FULL, pexp[g], grp * LPR + it);
         if (key < nk) {
             const uint4 vv = *reinterpret_cast<const uint4 *>(Vs + key * D + 8 * sub);
-            float vf[8];
-            unpack8(vv, vf);
+            float2 v2[4];
+            unpack4x2(vv, v2);
 #pragma unroll
-            for (int g = 0; g < HPC; ++g)
+            for (int g = 0; g < HPC; ++g) {
+                const float2 p2 = make_float2(pk[g], pk[g]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[g][e] = fmaf(pk[g], vf[e], o[g][e]);
+                for (int e = 0; e < 4; ++e) o2[g][e] = __ffma2_rn(p2, v2[e], o2[g][e]);
+            }
         }
     }
 }
 
 template <int D, int HPC>
-__global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
+__global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_kernel(const __grid_constant__ K3Params p) {
     using Sh = K3Shape<D, HPC>;
     constexpr int LPR = Sh::LPR, RPW = Sh::RPW;
@@ -200,6 +220,10 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
     const int kvh = blockIdx.y / p.HG, hg = blockIdx.y % p.HG;
     const int b = blockIdx.z;
     const int S = p.S;
+    // Programmatic dependent launch: this grid may start while the previous
+    // step's grid drains; everything below reads what that grid wrote.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int pos = p.lens[b];
     if (pos < 0 || pos >= p.cap) {
         if (threadIdx.x == 0) set_error(p.err, kErrBounds, kKernK3, 1);
@@ -258,12 +282,15 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
         const int sub = lane % LPR, grp = lane / LPR;
         const float4 *tab = reinterpret_cast<const float4 *>(
             p.rope + static_cast<int64_t>(pos) * (D / 2) + 8 * (sub % (LPR / 2)));
-        float qf[HPC][8];
+        float2 q2[HPC][4];
 #pragma unroll
         for (int g = 0; g < HPC; ++g) {
             uint4 unused;
+            float qf[8];
             norm_rope_row<D>(p.q + (static_cast<int64_t>(b) * p.Hq + h_first + g) * D, p.wq, tab,
-                             p.eps, sub, qf[g], unused);
+                             p.eps, sub, qf, unused);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) q2[g][e] = make_float2(qf[2 * e], qf[2 * e + 1]);
         }
         if (owner && warp == 0) {
             float kf[8];
@@ -286,13 +313,14 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
             __syncwarp();
         }
 
-        float m[HPC], l[HPC], o[HPC][8];
+        float m[HPC], l[HPC];
+        float2 o2[HPC][4];
 #pragma unroll
         for (int g = 0; g < HPC; ++g) {
             m[g] = -INFINITY;
             l[g] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+            for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
         }
         for (int c = c_begin + warp, i = warp; c < c_end; c += NW, i += NW) {
             const int st = i % NS;
@@ -301,13 +329,13 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
             if (!ok) break;
             const int nk = min(kK3Chunk, pos - c * kK3Chunk);
             consume_chunk<D, HPC>(reinterpret_cast<const __nv_bfloat16 *>(ring_k(st)),
-                                  reinterpret_cast<const __nv_bfloat16 *>(ring_v(st)), nk, qf,
-                                  p.scale_log2, m, l, o, sub, grp);
+                                  reinterpret_cast<const __nv_bfloat16 *>(ring_v(st)), nk, q2,
+                                  p.scale_log2, m, l, o2, sub, grp);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_empty[st]));
         }
         if (owner && warp == 0)
-            consume_chunk<D, HPC>(newk, newv, 1, qf, p.scale_log2, m, l, o, sub, grp);
+            consume_chunk<D, HPC>(newk, newv, 1, q2, p.scale_log2, m, l, o2, sub, grp);
 
         // Sum the RPW row groups (same sub, different grp) and the lane sums of l.
 #pragma unroll
@@ -315,7 +343,10 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
 #pragma unroll
             for (int g = 0; g < HPC; ++g)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[g][e] += __shfl_xor_sync(FULL, o[g][e], off);
+                for (int e = 0; e < 4; ++e) {
+                    o2[g][e].x += __shfl_xor_sync(FULL, o2[g][e].x, off);
+                    o2[g][e].y += __shfl_xor_sync(FULL, o2[g][e].y, off);
+                }
 #pragma unroll
         for (int g = 0; g < HPC; ++g)
 #pragma unroll
@@ -326,7 +357,8 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
             float *dst = red + (warp * HPC + g) * (D + 2);
             if (grp == 0) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) dst[8 * sub + e] = o[g][e];
+                for (int e = 0; e < 4; ++e)
+                    reinterpret_cast<float2 *>(dst + 8 * sub)[e] = o2[g][e];
             }
             if (lane == 0) {
                 dst[D] = m[g];
@@ -371,17 +403,15 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
     }
 
     if (!single) {
-        __threadfence();
-        __syncthreads();
+        __syncthreads();  // all partial writes of this CTA precede the release below
         if (threadIdx.x == 0) {
             uint32_t *cnt = p.grp_cnt + static_cast<int64_t>(b) * p.Hkv * p.HG + blockIdx.y;
-            const uint32_t prev = atomicAdd(cnt, 1u);
+            const uint32_t prev = atomic_inc_acq_rel(cnt);
             s_last = (prev == static_cast<uint32_t>(S - 1));
             if (s_last) *cnt = 0u;  // ready for the next launch
         }
         __syncthreads();
         if (!s_last) return;
-        __threadfence();
         // ------------------------------------------------------------ split merge
         // Warp g merges query head g: lanes own splits (m, l) and D/32 dims of o.
         if (warp < HPC) {
@@ -425,9 +455,8 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32)
     // This CTA finished its group; the last group of sequence b advances lens[b].
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
         const uint32_t groups = static_cast<uint32_t>(p.Hkv * p.HG);
-        const uint32_t prev = atomicAdd(p.seq_cnt + b, 1u);
+        const uint32_t prev = atomic_inc_acq_rel(p.seq_cnt + b);
         if (prev == groups - 1) {
             p.lens[b] = pos + 1;
             p.seq_cnt[b] = 0u;
@@ -447,9 +476,17 @@ static cudaError_t launch_k3_t(const K3Params &p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << dev;
     }
-    const dim3 grid(p.S, p.Hkv * p.HG, p.B);
-    k3_decode_kernel<D, HPC><<<grid, (kK3ConsumerWarps + 1) * 32, smem, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.S, p.Hkv * p.HG, p.B);
+    cfg.blockDim = dim3((kK3ConsumerWarps + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k3_decode_kernel<D, HPC>, p);
 }
 
 cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream) {

@@ -142,8 +142,8 @@ bool encode_q_map(CUtensorMap *m, void *base, int D, int Hq, int T) {
 int choose_splits(const qa_cache *c, int batch, int pos_max) {
     const int nchunks = (pos_max + qa::kK3Chunk - 1) / qa::kK3Chunk;
     const int groups = batch * c->cfg.n_kv_heads * c->HG;
-    const int target = 2 * c->num_sms;  // about one wave at two CTAs per SM
-    int S = (target + groups - 1) / groups;
+    const int resident = 2 * c->num_sms;  // the decode kernel fits two CTAs per SM
+    int S = resident / groups;            // one wave: never more CTAs than fit at once
     S = std::min(S, std::max(1, nchunks));
     S = std::min(S, qa::kK3MaxSplits);
     if (S > 1) {  // equal whole-chunk shares; drop splits that would be empty
