@@ -412,6 +412,94 @@ def traffic_for(kernel: str, algorithmic_bytes):
         return None
 
 
+# ---------------------------------------------------------------- decode sweep
+def run_sweep(args):
+    """Decode-only sweep (batch 1 and 4, cache lengths 512 to 16384): the cache
+    holds L raw N(0,1) keys/values per sequence, then `--steps` decode steps
+    run back to back (the length grows by one per step; bytes are counted
+    exactly).  One JSON line per point: mean µs per step and HBM GB/s of the
+    K/V read (events around the whole loop: launch gaps included)."""
+    import numpy as np
+    import torch
+
+    from gqa_attention_preallocated_qa_gb300 import binding as qa
+    from gqa_attention_preallocated_qa_gb300.configs import DECODE_SWEEP
+
+    pk = peaks()
+    for pt in DECODE_SWEEP:
+        inp = pt.inputs()
+        steps = args.steps
+        cap = pt.L + steps + args.warmup
+        h = qa.qa_cache_alloc(1, pt.B, pt.Hq, pt.Hkv, pt.D, cap, pt.theta, pt.eps)
+        K, V, _ = qa.cache_tensors(h, 0, pt.B, pt.Hkv, cap, pt.D)
+
+        def dev(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(
+                torch.bfloat16)
+        K[:, :, :pt.L] = dev(inp.cache_k)
+        V[:, :, :pt.L] = dev(inp.cache_v)
+        q, k, v, wq, wk = (dev(a) for a in (inp.dq[0], inp.dk[0], inp.dv[0], inp.wq, inp.wk))
+        out = torch.empty_like(q)
+        stream = torch.cuda.current_stream()
+        sh = stream.cuda_stream
+        lib = qa.lib
+        args_c = (q.data_ptr(), k.data_ptr(), v.data_ptr(), wq.data_ptr(), wk.data_ptr(),
+                  out.data_ptr())
+        qa.qa_cache_set_lengths(h, 0, [pt.L] * pt.B)
+        for _ in range(args.warmup):
+            lib.qa_decode_step(h, 0, pt.B, *args_c, sh)
+        start = pt.L + args.warmup
+        splits = qa.qa_decode_splits(h, 0, pt.B)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        st = 0
+        for _ in range(steps):
+            st |= lib.qa_decode_step(h, 0, pt.B, *args_c, sh)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if st or qa.qa_get_device_error(h)[0]:
+            raise RuntimeError(f"decode sweep point {pt.name} failed")
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        byts = sum(pt.B * pt.Hkv * (start + s + 1) * pt.D * 4 for s in range(steps)) / steps
+        gbs = byts / (us * 1e-6) / 1e9
+        print(json.dumps({"sweep": pt.name, "B": pt.B, "L": pt.L, "steps": steps,
+                          "splits": splits, "us_per_step": round(us, 3),
+                          "kv_bytes_per_step": round(byts), "hbm_gbs": round(gbs, 1),
+                          "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4)}), flush=True)
+        qa.qa_cache_free(h)
+
+
+def run_profile_case(args):
+    """A short program for ncu: one reset + prefill and four decode steps of the
+    benchmark workload (B=4, prompt 2048), nothing else on the device."""
+    import numpy as np
+    import torch
+
+    from gqa_attention_preallocated_qa_gb300 import binding as qa
+    from gqa_attention_preallocated_qa_gb300.configs import QWEN3_4B_B4 as w
+    inp = w.inputs()
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    q, k, v, wq, wk = (dev(a) for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+    out = torch.empty_like(q)
+    h = qa.qa_cache_alloc(1, w.B, w.Hq, w.Hkv, w.D, w.cap, w.theta, w.eps)
+    for rep in range(2):
+        qa.qa_cache_reset(h)
+        qa.qa_prefill(h, 0, list(w.prompt_lens), q, k, v, wq, wk, out)
+        for s in range(4):
+            dq, dk, dv = dev(inp.dq[s]), dev(inp.dk[s]), dev(inp.dv[s])
+            o = torch.empty_like(dq)
+            qa.qa_decode_step(h, 0, w.B, dq, dk, dv, wq, wk, o)
+    torch.cuda.synchronize()
+    st, word = qa.qa_get_device_error(h)
+    qa.qa_cache_free(h)
+    if st:
+        raise RuntimeError(f"device error {word:#x}")
+    print("profile case done", flush=True)
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args):
     """The oracle as it stands, single-threaded on the host, on a bounded sample
@@ -452,9 +540,17 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="decode-only sweep over batch 1/4 and cache lengths 512..16384")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run one small prefill + 4 decode steps (for ncu) and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
