@@ -36,12 +36,24 @@ __global__ void __launch_bounds__(256) k1_norm_rope_append_kernel(const __grid_c
     const int sub = lane % LPR;
     const int grp = lane / LPR;
     const int H3 = p.Hq + 2 * p.Hkv;
-    const int64_t total = static_cast<int64_t>(p.T) * H3;
-    const int64_t row0 =
-        ((static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * RPW + grp) * R;
+    // A row group owns R consecutive head rows of ONE token: group g is token
+    // g / RG, rows (g % RG) * R ... + R - 1 (one 32-bit division per thread).
+    const int RG = (H3 + R - 1) / R;
+    const int g = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * RPW + grp;
+    const int t0 = g / RG;
+    const int jbase = (g - t0 * RG) * R;
+    const bool tok_valid = t0 < p.T;
+    const int64_t t = tok_valid ? t0 : 0;
+    int b = 0;
+    while (b + 1 < p.nseq && t >= p.cu[b + 1]) ++b;
+    const int pos = static_cast<int>(t - p.cu[b]);
+    const int64_t slot = static_cast<int64_t>(p.seq_slot0 + b) * p.seq_stride;
 
     if (blockIdx.x == 0 && threadIdx.x < p.nseq)
         p.lens[p.seq_slot0 + threadIdx.x] = p.cu[threadIdx.x + 1] - p.cu[threadIdx.x];
+    if (tok_valid && pos >= p.cap)  // cannot happen after host validation; never write out of bounds
+        set_error(p.err, kErrBounds, kKernK1, 1);
+    const bool tok_active = tok_valid && pos < p.cap;
 
     const uint4 wqv = __ldg(reinterpret_cast<const uint4 *>(p.wq) + sub);
     const uint4 wkv = __ldg(reinterpret_cast<const uint4 *>(p.wk) + sub);
@@ -49,18 +61,11 @@ __global__ void __launch_bounds__(256) k1_norm_rope_append_kernel(const __grid_c
     // Phase 1: addresses and loads of the R rows.
     uint4 xv[R];
     __nv_bfloat16 *dst[R];
-    int pos_r[R];
     uint32_t kind[R];  // 0 = q, 1 = k, 2 = v, 3 = inactive
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const int64_t row = row0 + r;
-        const bool valid = row < total;
-        const int64_t t = valid ? row / H3 : 0;
-        const int j = valid ? static_cast<int>(row % H3) : 0;
-        int b = 0;
-        while (b + 1 < p.nseq && t >= p.cu[b + 1]) ++b;
-        const int pos = static_cast<int>(t - p.cu[b]);
-        const int64_t slot = static_cast<int64_t>(p.seq_slot0 + b) * p.seq_stride;
+        const int j = jbase + r;
+        const bool active = tok_active && j < H3;
         const __nv_bfloat16 *src;
         if (j < p.Hq) {
             src = p.q + (t * p.Hq + j) * D;
@@ -77,14 +82,14 @@ __global__ void __launch_bounds__(256) k1_norm_rope_append_kernel(const __grid_c
             dst[r] = p.vc + slot + h * p.head_stride + static_cast<int64_t>(pos) * D;
             kind[r] = 2;
         }
-        if (valid && pos >= p.cap) {  // cannot happen after host validation; never write out of bounds
-            set_error(p.err, kErrBounds, kKernK1, 1);
-        }
-        const bool active = valid && pos < p.cap;
         if (!active) kind[r] = 3;
-        pos_r[r] = active ? pos : 0;
         xv[r] = active ? __ldg(reinterpret_cast<const uint4 *>(src) + sub) : make_uint4(0, 0, 0, 0);
     }
+    const float4 *tab = reinterpret_cast<const float4 *>(
+        p.rope + static_cast<int64_t>(tok_active ? pos : 0) * (D / 2) + 8 * (sub % HALF));
+    float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims, shared by the R rows
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + e);
 
     // Phase 2: norm, rotate, store.
 #pragma unroll
@@ -120,16 +125,13 @@ __global__ void __launch_bounds__(256) k1_norm_rope_append_kernel(const __grid_c
         for (int e = 0; e < 4; ++e) pw[e] = __shfl_xor_sync(FULL, yw[e], HALF);
 
         const bool lower = sub < HALF;
-        const float4 *tab = reinterpret_cast<const float4 *>(
-            p.rope + static_cast<int64_t>(pos_r[r]) * (D / 2) + 8 * (sub % HALF));
         uint32_t ow[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float4 cs = __ldg(tab + e);  // (cos_a, sin_a, cos_b, sin_b)
             const float y0 = bf16lo(yw[e]), y1 = bf16hi(yw[e]);
             const float q0 = bf16lo(pw[e]), q1 = bf16hi(pw[e]);
-            const float r0 = lower ? y0 * cs.x - q0 * cs.y : y0 * cs.x + q0 * cs.y;
-            const float r1 = lower ? y1 * cs.z - q1 * cs.w : y1 * cs.z + q1 * cs.w;
+            const float r0 = lower ? y0 * cs[e].x - q0 * cs[e].y : y0 * cs[e].x + q0 * cs[e].y;
+            const float r1 = lower ? y1 * cs[e].z - q1 * cs[e].w : y1 * cs[e].z + q1 * cs[e].w;
             ow[e] = pack_bf16(r0, r1);
         }
         if (kind[r] != 3) {
@@ -140,9 +142,10 @@ __global__ void __launch_bounds__(256) k1_norm_rope_append_kernel(const __grid_c
 }
 
 cudaError_t launch_k1(const K1Params &p, int D, cudaStream_t stream) {
-    const int64_t rows = static_cast<int64_t>(p.T) * (p.Hq + 2 * p.Hkv);
-    const int rows_per_block = (256 / 32) * (32 / (D / 8)) * kRowsPerGroup;
-    const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+    const int RG = (p.Hq + 2 * p.Hkv + kRowsPerGroup - 1) / kRowsPerGroup;
+    const int64_t groups = static_cast<int64_t>(p.T) * RG;  // < 2^31: T is limited by the caller
+    const int groups_per_block = (256 / 32) * (32 / (D / 8));
+    const int64_t blocks = (groups + groups_per_block - 1) / groups_per_block;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     if (D == 128)

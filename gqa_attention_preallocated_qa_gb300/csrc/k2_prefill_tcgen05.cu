@@ -269,13 +269,20 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                     for (int i = 0; i < 128; ++i)
                         if (i > r) s[i] = -INFINITY;
                 }
-                float mx = s[0];
+                // Row max and row sum with 8 independent partial chains each.
+                float mx8[8];
 #pragma unroll
-                for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+                for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+#pragma unroll
+                for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float m_new = fmaxf(m, mx);
                 const float neg = m_new * c;
                 const float alpha = (m == -INFINITY) ? 0.f : k2_ex2(m * c - neg);
-                float sum = 0.f;
+                float sum8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     uint32_t pk[32];
@@ -283,11 +290,14 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                     for (int i = 0; i < 32; ++i) {
                         const float p0 = k2_ex2(fmaf(s[ch * 64 + 2 * i], c, -neg));
                         const float p1 = k2_ex2(fmaf(s[ch * 64 + 2 * i + 1], c, -neg));
-                        sum += p0 + p1;
+                        sum8[(2 * i) & 7] += p0;
+                        sum8[(2 * i + 1) & 7] += p1;
                         pk[i] = pack_bf16(p0, p1);
                     }
                     tmem_st32(tS + ch * 32, pk);
                 }
+                const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                                  ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
                 l = fmaf(l, alpha, sum);
                 if (j > 0 && __any_sync(FULL, m_new > m)) {
                     // PV_t(j-1) is complete: S_t(j) was issued after it finished.

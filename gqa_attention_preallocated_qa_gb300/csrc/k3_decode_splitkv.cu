@@ -209,6 +209,9 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS];
     __shared__ int s_abort;
     __shared__ int s_last;
+    __shared__ uint32_t s_seq_prev;
+    __shared__ float s_w[HPC][kK3MaxSplits];  // split weights of the merge
+    __shared__ float s_inv[HPC];
 
     uint8_t *ring = smem;
     __nv_bfloat16 *newk = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes);
@@ -412,12 +415,21 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
         }
         __syncthreads();
         if (!s_last) return;
+    }
+    // This CTA is the last of its group, so every CTA of the group has read
+    // lens[b].  Count the group towards sequence b now: the atomic's latency
+    // overlaps the merge below, and the last group advances lens[b] at the end.
+    if (threadIdx.x == 0) s_seq_prev = atomic_inc_acq_rel(p.seq_cnt + b);
+    if (!single) {
         // ------------------------------------------------------------ split merge
-        // Warp g merges query head g: lanes own splits (m, l) and D/32 dims of o.
+        // Warp g turns head g's split maxima into weights 2^((m_s - M) c) (lanes
+        // over splits) and 1 / sum_s w_s l_s; then every thread merges four
+        // output dims of one head over all splits in a fixed order, its loads
+        // unrolled so that they overlap.
         if (warp < HPC) {
             const int g = warp;
             const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h_first + g) * S;
-            float ms[2], ls[2], ws[2];
+            float ms[2], ls[2];
 #pragma unroll
             for (int k2 = 0; k2 < 2; ++k2) {
                 const int s = lane + 32 * k2;
@@ -430,37 +442,43 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
             float Lsum = 0.f;
 #pragma unroll
             for (int k2 = 0; k2 < 2; ++k2) {
-                ws[k2] = ms[k2] == -INFINITY ? 0.f : ex2((ms[k2] - M) * p.scale_log2);
-                Lsum = fmaf(ws[k2], ls[k2], Lsum);
+                const int s = lane + 32 * k2;
+                const float w = ms[k2] == -INFINITY ? 0.f : ex2((ms[k2] - M) * p.scale_log2);
+                if (s < S) s_w[g][s] = w;
+                Lsum = fmaf(w, ls[k2], Lsum);
             }
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) Lsum += __shfl_xor_sync(FULL, Lsum, off);
-            constexpr int DPL = D / 32;
-            float acc[DPL];
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+            if (lane == 0) s_inv[g] = 1.f / Lsum;
+        }
+        __syncthreads();
+        constexpr int D4 = D / 4;
+        for (int idx = threadIdx.x; idx < HPC * D4; idx += blockDim.x) {
+            const int g = idx / D4, d4 = idx % D4;
+            const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h_first + g) * S;
+            const float4 *po = reinterpret_cast<const float4 *>(p.part_o + row0 * D) + d4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
             for (int s = 0; s < S; ++s) {
-                const float wsv = __shfl_sync(FULL, s < 32 ? ws[0] : ws[1], s & 31);
-                const float *po = p.part_o + (row0 + s) * D + lane * DPL;
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wsv, __ldcg(po + e), acc[e]);
+                const float4 v = __ldcg(po + static_cast<int64_t>(s) * D4);
+                const float w = s_w[g][s];
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
             }
-            const float inv = 1.f / Lsum;
-            __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(b) * p.Hq + h_first + g) * D + lane * DPL;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
+            const float inv = s_inv[g];
+            uint2 o;
+            o.x = pack_bf16(acc.x * inv, acc.y * inv);
+            o.y = pack_bf16(acc.z * inv, acc.w * inv);
+            reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(b) * p.Hq + h_first + g) * D)[d4] = o;
         }
     }
     // ---------------------------------------------------------------- length update
-    // This CTA finished its group; the last group of sequence b advances lens[b].
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t groups = static_cast<uint32_t>(p.Hkv * p.HG);
-        const uint32_t prev = atomic_inc_acq_rel(p.seq_cnt + b);
-        if (prev == groups - 1) {
-            p.lens[b] = pos + 1;
-            p.seq_cnt[b] = 0u;
-        }
+    if (threadIdx.x == 0 && s_seq_prev == static_cast<uint32_t>(p.Hkv * p.HG) - 1u) {
+        p.lens[b] = pos + 1;
+        p.seq_cnt[b] = 0u;
     }
 }
 

@@ -173,7 +173,7 @@ qa_status check_prefill(const qa_cache *c, int layer, int batch, const int32_t *
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(wq) || !aligned16(wk) ||
             !aligned16(dst))
             return QA_ERR_ALIGNMENT;
-        if (T > (int64_t(1) << 30)) return QA_ERR_INVALID_ARG;
+        if (T > (int64_t(1) << 26)) return QA_ERR_INVALID_ARG;  // keeps K1's 32-bit row-group index
     }
     *T_out = T;
     return QA_OK;
