@@ -60,6 +60,8 @@ SIGNATURES = {
     "qa_stats": (ctypes.c_int, [_vp, _u64p]),
     "qa_memory_info": (ctypes.c_int, [_vp, _u64p, _u64p]),
     "qa_decode_splits": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int]),
+    "qa_decode_step_noalloc": (ctypes.c_int, [ctypes.POINTER(qa_config), ctypes.c_int, _i32p, _vp,
+                                              _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "qa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "qa_abi_version": (ctypes.c_int, []),
 }
@@ -150,6 +152,15 @@ def qa_decode_step(cache, layer, batch, q, k, v, q_norm_w, k_norm_w, out, stream
     _check(lib.qa_decode_step(cache, layer, batch, _ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w),
                               _ptr(k_norm_w), _ptr(out), _stream(stream)),
            "qa_decode_step")
+
+
+def qa_decode_step_noalloc(cfg: qa_config, positions, k_cache, v_cache, q, k, v, q_norm_w,
+                           k_norm_w, out, stream=None) -> None:
+    """Allocation-free decode step on caller-owned cache memory (see include/qa.h)."""
+    _check(lib.qa_decode_step_noalloc(ctypes.byref(cfg), len(positions), _i32(positions),
+                                      _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(k), _ptr(v),
+                                      _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out), _stream(stream)),
+           "qa_decode_step_noalloc")
 
 
 def qa_cache_view(cache, layer):

@@ -24,6 +24,11 @@
 // instruction; a 32-key chunk is LPR iterations.  Partial dot products are
 // reduce-scattered over the LPR lanes so that each lane ends with the full
 // score of one key for every head.
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "qa.h"
 #include "qa_device.cuh"
 
 namespace qa {
@@ -78,8 +83,8 @@ __device__ __forceinline__ uint32_t atomic_inc_acq_rel(uint32_t *p) {
 // packed words.  Cast placement as in K1.
 template <int D>
 __device__ __forceinline__ void norm_rope_row(const __nv_bfloat16 *src, const __nv_bfloat16 *w,
-                                              const float4 *tab, float eps, int sub, float (&out)[8],
-                                              uint4 &packed) {
+                                              const float4 (&cs)[4], float eps, int sub,
+                                              float (&out)[8], uint4 &packed) {
     constexpr int LPR = D / 8, HALF = LPR / 2;
     const unsigned FULL = 0xffffffffu;
     const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(src) + sub);
@@ -103,11 +108,10 @@ __device__ __forceinline__ void norm_rope_row(const __nv_bfloat16 *src, const __
     const bool lower = sub < HALF;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float4 cs = __ldg(tab + e);
         const float y0 = bf16lo(yw[e]), y1 = bf16hi(yw[e]);
         const float q0 = bf16lo(pw[e]), q1 = bf16hi(pw[e]);
-        const float r0 = lower ? y0 * cs.x - q0 * cs.y : y0 * cs.x + q0 * cs.y;
-        const float r1 = lower ? y1 * cs.z - q1 * cs.w : y1 * cs.z + q1 * cs.w;
+        const float r0 = lower ? y0 * cs[e].x - q0 * cs[e].y : y0 * cs[e].x + q0 * cs[e].y;
+        const float r1 = lower ? y1 * cs[e].z - q1 * cs[e].w : y1 * cs[e].z + q1 * cs[e].w;
         ow[e] = pack_bf16(r0, r1);
         out[2 * e] = bf16lo(ow[e]);
         out[2 * e + 1] = bf16hi(ow[e]);
@@ -196,9 +200,15 @@ __device__ __forceinline__ void consume_chunk(const __nv_bfloat16 *Ks, const __n
     }
 }
 
-template <int D, int HPC>
-__global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
-    k3_decode_kernel(const __grid_constant__ K3Params p) {
+// The kernel body.  kHostPositions = false is the decode step of the cache
+// object: positions come from the device lengths, (cos, sin) from the
+// library's table, and the last group of each sequence advances its length.
+// kHostPositions = true is the allocation-free variant: positions and the
+// (cos, sin) of each sequence's position come in the kernel parameters
+// (pos_arr[b], cs_arr[b * D/2 + i]) and the caller keeps the lengths.
+template <int D, int HPC, bool kHostPositions>
+__device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
+                                        const float2 *cs_arr) {
     using Sh = K3Shape<D, HPC>;
     constexpr int LPR = Sh::LPR, RPW = Sh::RPW;
     constexpr int NW = kK3ConsumerWarps;
@@ -227,7 +237,7 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     // step's grid drains; everything below reads what that grid wrote.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int pos = p.lens[b];
+    const int pos = kHostPositions ? pos_arr[b] : p.lens[b];
     if (pos < 0 || pos >= p.cap) {
         if (threadIdx.x == 0) set_error(p.err, kErrBounds, kKernK3, 1);
         return;
@@ -283,14 +293,24 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     } else {
         // ------------------------------------------------------------ consumers
         const int sub = lane % LPR, grp = lane / LPR;
-        const float4 *tab = reinterpret_cast<const float4 *>(
-            p.rope + static_cast<int64_t>(pos) * (D / 2) + 8 * (sub % (LPR / 2)));
+        float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims at pos
+        if constexpr (kHostPositions) {
+            const float4 *src = reinterpret_cast<const float4 *>(cs_arr + b * (D / 2) +
+                                                                 8 * (sub % (LPR / 2)));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cs[e] = src[e];
+        } else {
+            const float4 *tab = reinterpret_cast<const float4 *>(
+                p.rope + static_cast<int64_t>(pos) * (D / 2) + 8 * (sub % (LPR / 2)));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + e);
+        }
         float2 q2[HPC][4];
 #pragma unroll
         for (int g = 0; g < HPC; ++g) {
             uint4 unused;
             float qf[8];
-            norm_rope_row<D>(p.q + (static_cast<int64_t>(b) * p.Hq + h_first + g) * D, p.wq, tab,
+            norm_rope_row<D>(p.q + (static_cast<int64_t>(b) * p.Hq + h_first + g) * D, p.wq, cs,
                              p.eps, sub, qf, unused);
 #pragma unroll
             for (int e = 0; e < 4; ++e) q2[g][e] = make_float2(qf[2 * e], qf[2 * e + 1]);
@@ -298,7 +318,7 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
         if (owner && warp == 0) {
             float kf[8];
             uint4 kp;
-            norm_rope_row<D>(p.k + (static_cast<int64_t>(b) * p.Hkv + kvh) * D, p.wk, tab, p.eps,
+            norm_rope_row<D>(p.k + (static_cast<int64_t>(b) * p.Hkv + kvh) * D, p.wk, cs, p.eps,
                              sub, kf, kp);
             const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(
                                        p.v + (static_cast<int64_t>(b) * p.Hkv + kvh) * D) +
@@ -419,7 +439,7 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     // This CTA is the last of its group, so every CTA of the group has read
     // lens[b].  Count the group towards sequence b now: the atomic's latency
     // overlaps the merge below, and the last group advances lens[b] at the end.
-    if (threadIdx.x == 0) s_seq_prev = atomic_inc_acq_rel(p.seq_cnt + b);
+    if (!kHostPositions && threadIdx.x == 0) s_seq_prev = atomic_inc_acq_rel(p.seq_cnt + b);
     if (!single) {
         // ------------------------------------------------------------ split merge
         // Warp g turns head g's split maxima into weights 2^((m_s - M) c) (lanes
@@ -475,11 +495,19 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
         }
     }
     // ---------------------------------------------------------------- length update
-    __syncthreads();
-    if (threadIdx.x == 0 && s_seq_prev == static_cast<uint32_t>(p.Hkv * p.HG) - 1u) {
-        p.lens[b] = pos + 1;
-        p.seq_cnt[b] = 0u;
+    if constexpr (!kHostPositions) {
+        __syncthreads();
+        if (threadIdx.x == 0 && s_seq_prev == static_cast<uint32_t>(p.Hkv * p.HG) - 1u) {
+            p.lens[b] = pos + 1;
+            p.seq_cnt[b] = 0u;
+        }
     }
+}
+
+template <int D, int HPC>
+__global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
+    k3_decode_kernel(const __grid_constant__ K3Params p) {
+    k3_body<D, HPC, false>(p, nullptr, nullptr);
 }
 
 template <int D, int HPC>
@@ -521,3 +549,192 @@ cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream) {
 }
 
 }  // namespace qa
+
+// ==================================================================== allocation-free decode step
+// qa_decode_step_noalloc runs the same decode kernel body for callers that may
+// not allocate device memory.  Its scratch (split partials, counters, error
+// word) lives in a fixed array of this module: the CUDA driver creates it when
+// the library's device code loads on a GPU, and it stays until the process
+// exits.  Host code never dereferences the symbol; it asks the runtime for the
+// array's device address once per device.
+namespace qa {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per GPU
+constexpr int kNoAllocMaxGroups = 4096;                   // batch * Hkv * head groups
+constexpr int kNoAllocMaxBatch = 16;
+constexpr size_t kNoAllocErrOffset = kNoAllocMaxGroups * sizeof(uint32_t);
+constexpr size_t kNoAllocClearBytes = kNoAllocErrOffset + 256;  // counters + error word
+constexpr size_t kNoAllocPartOffset = 32768;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct __align__(16) K3NoAllocParams {
+    float2 cs[kNoAllocMaxBatch * 64];  // (cos, sin) at pos[b] of the D/2 frequencies, [b][i]
+    int pos[kNoAllocMaxBatch];         // slot of each sequence's new token
+    K3Params base;
+};
+
+template <int D, int HPC>
+__global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
+    k3_decode_noalloc_kernel(const __grid_constant__ K3NoAllocParams p) {
+    k3_body<D, HPC, true>(p.base, p.pos, p.cs);
+}
+
+template <int D, int HPC>
+static cudaError_t launch_noalloc_t(const K3NoAllocParams &p, cudaStream_t stream) {
+    constexpr int smem = K3Shape<D, HPC>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(k3_decode_noalloc_kernel<D, HPC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(p.base.S, p.base.Hkv * p.base.HG, p.base.B);
+    k3_decode_noalloc_kernel<D, HPC><<<grid, (kK3ConsumerWarps + 1) * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+static cudaError_t launch_noalloc(const K3NoAllocParams &p, int D, int HPC, cudaStream_t stream) {
+    if (D == 128) {
+        if (HPC == 4) return launch_noalloc_t<128, 4>(p, stream);
+        if (HPC == 2) return launch_noalloc_t<128, 2>(p, stream);
+        if (HPC == 1) return launch_noalloc_t<128, 1>(p, stream);
+    } else if (D == 64) {
+        if (HPC == 4) return launch_noalloc_t<64, 4>(p, stream);
+        if (HPC == 2) return launch_noalloc_t<64, 2>(p, stream);
+        if (HPC == 1) return launch_noalloc_t<64, 1>(p, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+namespace {
+struct NoAllocDevice {
+    unsigned char *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int num_sms = 0;
+};
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
+
+// Once per device, with that device current: the device address of the
+// scratch array and the SM count.  Neither call allocates.
+qa_status noalloc_setup(NoAllocDevice *&out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+        return QA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice &d = g_noalloc_devices[dev];
+    if (!d.scratch) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return QA_ERR_CUDA;
+        }
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return QA_ERR_CUDA;
+        d.num_sms = sms;
+        d.scratch = static_cast<unsigned char *>(ptr);
+    }
+    out = &d;
+    return QA_OK;
+}
+
+bool aligned16_na(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+}  // namespace qa
+
+extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noalloc(
+    const qa_config *cfg, int batch, const int32_t *positions, void *k_cache, void *v_cache,
+    const void *q, const void *k, const void *v, const void *q_norm_w, const void *k_norm_w,
+    void *out, void *stream) {
+    using namespace qa;
+    if (!cfg || !positions) return QA_ERR_INVALID_ARG;
+    const qa_config g = *cfg;
+    if (g.max_batch <= 0 || g.capacity <= 0 || !(g.rope_theta > 0.f) || !(g.rms_eps >= 0.f))
+        return QA_ERR_INVALID_ARG;
+    if ((g.head_dim != 64 && g.head_dim != 128) || g.n_kv_heads <= 0 || g.n_q_heads <= 0 ||
+        g.n_q_heads % g.n_kv_heads)
+        return QA_ERR_UNSUPPORTED_SHAPE;
+    const int G = g.n_q_heads / g.n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return QA_ERR_UNSUPPORTED_SHAPE;
+    if (batch < 1 || batch > g.max_batch) return QA_ERR_INVALID_ARG;
+    if (batch > kNoAllocMaxBatch) return QA_ERR_UNSUPPORTED_SHAPE;  // above the parameter block
+    if (!k_cache || !v_cache || !q || !k || !v || !q_norm_w || !k_norm_w || !out)
+        return QA_ERR_INVALID_ARG;
+    if (!aligned16_na(k_cache) || !aligned16_na(v_cache) || !aligned16_na(q) ||
+        !aligned16_na(k) || !aligned16_na(v) || !aligned16_na(q_norm_w) ||
+        !aligned16_na(k_norm_w) || !aligned16_na(out))
+        return QA_ERR_ALIGNMENT;
+    int pos_max = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (positions[b] < 0) return QA_ERR_INVALID_ARG;
+        if (positions[b] >= g.capacity) return QA_ERR_CAPACITY;  // no slot left: never evict
+        pos_max = std::max(pos_max, static_cast<int>(positions[b]));
+    }
+    const int HPC = std::min(G, 4), HG = G / HPC, D = g.head_dim;
+    const int groups = batch * g.n_kv_heads * HG;
+    if (groups > kNoAllocMaxGroups) return QA_ERR_UNSUPPORTED_SHAPE;  // above the counters
+    NoAllocDevice *dev = nullptr;
+    qa_status st = noalloc_setup(dev);
+    if (st != QA_OK) return st;
+
+    // Split plan as in qa_decode_step, further capped by the partials the
+    // scratch array can hold (one split needs no partials at all).
+    const int nchunks = (pos_max + kK3Chunk - 1) / kK3Chunk;
+    int S = std::max(1, (2 * dev->num_sms) / groups);
+    S = std::min(S, std::max(1, nchunks));
+    S = std::min(S, kK3MaxSplits);
+    const size_t per_split = static_cast<size_t>(batch) * g.n_q_heads * (D + 2) * sizeof(float);
+    const size_t room = kNoAllocScratchBytes - kNoAllocPartOffset - 256;
+    S = std::min<size_t>(S, std::max<size_t>(1, room / per_split));
+    if (S > 1) {
+        const int cps = (nchunks + S - 1) / S;
+        S = (nchunks + cps - 1) / cps;
+    }
+
+    K3NoAllocParams p{};
+    for (int b = 0; b < batch; ++b) {
+        p.pos[b] = positions[b];
+        for (int i = 0; i < D / 2; ++i) {  // same fp64 formula as the cache's table
+            const double a = static_cast<double>(positions[b]) *
+                             std::pow(static_cast<double>(g.rope_theta), -2.0 * i / D);
+            p.cs[b * (D / 2) + i] =
+                make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+        }
+    }
+    unsigned char *scr = dev->scratch;
+    const size_t nrows = static_cast<size_t>(batch) * g.n_q_heads * S;
+    K3Params &bp = p.base;
+    bp.q = static_cast<const __nv_bfloat16 *>(q);
+    bp.k = static_cast<const __nv_bfloat16 *>(k);
+    bp.v = static_cast<const __nv_bfloat16 *>(v);
+    bp.wq = static_cast<const __nv_bfloat16 *>(q_norm_w);
+    bp.wk = static_cast<const __nv_bfloat16 *>(k_norm_w);
+    bp.kc = static_cast<__nv_bfloat16 *>(k_cache);
+    bp.vc = static_cast<__nv_bfloat16 *>(v_cache);
+    bp.lens = nullptr;
+    bp.rope = nullptr;
+    bp.grp_cnt = reinterpret_cast<uint32_t *>(scr);
+    bp.seq_cnt = nullptr;
+    bp.err = reinterpret_cast<uint32_t *>(scr + kNoAllocErrOffset);
+    bp.part_m = reinterpret_cast<float *>(scr + kNoAllocPartOffset);
+    bp.part_l = bp.part_m + nrows;
+    const size_t o_off = (kNoAllocPartOffset + 2 * nrows * sizeof(float) + 255) & ~size_t(255);
+    bp.part_o = reinterpret_cast<float *>(scr + o_off);
+    bp.out = static_cast<__nv_bfloat16 *>(out);
+    bp.head_stride = static_cast<int64_t>(g.capacity) * D;
+    bp.seq_stride = bp.head_stride * g.n_kv_heads;
+    bp.B = batch;
+    bp.Hq = g.n_q_heads;
+    bp.Hkv = g.n_kv_heads;
+    bp.G = G;
+    bp.HG = HG;
+    bp.cap = g.capacity;
+    bp.S = S;
+    bp.eps = g.rms_eps;
+    bp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents: counters and error word start at zero.
+    if (cudaMemsetAsync(scr, 0, kNoAllocClearBytes, s) != cudaSuccess) return QA_ERR_CUDA;
+    if (launch_noalloc(p, D, HPC, s) != cudaSuccess) return QA_ERR_CUDA;
+    return QA_OK;
+}

@@ -169,6 +169,43 @@ qa_status qa_memory_info(qa_cache *cache, uint64_t *kv_bytes, uint64_t *scratch_
  * lengths of `layer` and `batch` sequences (a pure host computation). */
 int qa_decode_splits(qa_cache *cache, int layer, int batch);
 
+/* ---- allocation-free decode step ----------------------------------------
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that must not allocate device memory at all: code that runs while a CUDA
+ * graph is being captured (an allocation there is illegal or breaks the
+ * capture), engines that hand out every byte of the GPU from their own arena
+ * and forbid any other allocation, and plug-ins embedded in a host framework
+ * that owns the device allocator.  Such a caller owns the cache memory and the
+ * lengths itself and passes them in.
+ *
+ * One decode step of one layer, computed by the same kernel as
+ * qa_decode_step: for each of sequences 0..batch-1 the new token's q and k are
+ * RMS-normed and rotated at position positions[b], k' and v are written to
+ * cache slot positions[b], and every query head attends over slots
+ * 0..positions[b] (inclusive).
+ *   cfg         geometry (num_layers is ignored; one layer is passed).
+ *   positions   HOST int32 [batch]: current length of each sequence, which is
+ *               the slot of its new token; each must be < capacity.  The
+ *               caller advances its own lengths after the call.
+ *   k_cache, v_cache  DEVICE bf16 [max_batch][n_kv_heads][capacity][head_dim]
+ *               of this layer, caller-owned, read and appended to.
+ *   q, k, v, q_norm_w, k_norm_w, out: as in qa_decode_step.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ * The kernel's scratch (split partials and counters) is a fixed 4 MiB array
+ * in the library's device code, created on every GPU that loads the library
+ * and held until the process exits.  The first call on a device looks up
+ * that array's address (no allocation); make that first call before any
+ * stream capture.  Every call shares the array: calls that may overlap on the
+ * GPU (different streams without ordering) race and give wrong results.
+ * Limits: batch <= 16 and batch * n_kv_heads * (heads-per-CTA groups) <=
+ * 4096, else QA_ERR_UNSUPPORTED_SHAPE; the split count is reduced to what the
+ * array can hold.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ALIGNMENT,
+ * CAPACITY (a position >= capacity), CUDA. */
+qa_status qa_decode_step_noalloc(const qa_config *cfg, int batch, const int32_t *positions,
+                                 void *k_cache, void *v_cache, const void *q, const void *k,
+                                 const void *v, const void *q_norm_w, const void *k_norm_w,
+                                 void *out, void *stream);
+
 /* Static description of a status code. */
 const char *qa_status_str(qa_status status);
 
