@@ -2,28 +2,27 @@
 //
 // For every (sequence b, kv head, head group, split) CTA:
 //   1. read pos = lens[b] (device lengths; the host never passes positions),
-//   2. RMSNorm + RoPE the HPC query heads of the group at pos (kept in
-//      registers, rounded to bf16 like the prefill path),
+//   2. RMSNorm + RoPE the HPC (<= 4) query heads of the group at pos, rounded
+//      to bf16 like the prefill path, staged in shared memory,
 //   3. the CTA owning the last split also norms + rotates k, appends k' and v
 //      to cache slot pos and attends to that new key from shared memory,
-//   4. stream its share of cache keys [0, pos) through a ring of shared-memory
-//      stages filled by bulk TMA copies (one contiguous copy for K and one
-//      for V per 32-key chunk; the K/V rows of one (sequence, kv head) are
-//      contiguous in the cache), all HPC query heads sharing every load,
-//   5. online softmax in fp32 per warp, CTA combine through shared memory,
-//   6. partial (m, l, o) to scratch; the last CTA of the group (atomic
-//      counter, no spinning) merges the splits with a warp-level log-sum-exp
-//      reduction in a fixed order, writes out[b][h] in bf16, and the last
-//      group of the sequence advances lens[b].
+//   4. stream its share of cache keys [0, pos) in 32-key chunks through a ring
+//      of shared-memory stages filled by TMA tensor copies (128-byte swizzle,
+//      evict-first L2 policy); all query heads of the group share every load,
+//   5. per chunk and warp: S = q' K^T and O += P V as warp-level bf16 MMAs
+//      (m16n8k16, fp32 accumulate; the 4 heads of a group fill rows 0-3 of the
+//      16-row tile, so the tile's unused rows cost tensor time, not memory),
+//      online softmax in fp32 on the score fragments, P reused in registers as
+//      the A operand of P V,
+//   6. CTA combine through shared memory, partial (m, l, o) to scratch; the
+//      last CTA of the group (acquire-release counter, no spinning) merges the
+//      splits in a fixed order, writes out[b][h] in bf16, and the last group of
+//      the sequence advances lens[b].
 // This serves the decode step of the dryft-flash-infer agent guide ("Where the
 // wins are": per-step overhead is the largest cost at batch 1 and 4, so the
 // step is one launch) against the preallocated cache of the same section.
-//
-// Lane mapping inside a consumer warp: a key row of D bf16 is read by
-// LPR = D/8 lanes (16 bytes each); RPW = 32/LPR rows are read per
-// instruction; a 32-key chunk is LPR iterations.  Partial dot products are
-// reduce-scattered over the LPR lanes so that each lane ends with the full
-// score of one key for every head.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -33,41 +32,24 @@
 
 namespace qa {
 
-constexpr int kK3Stages = 6;
+constexpr int kK3Stages = 4;
 
 template <int D, int HPC>
 struct K3Shape {
-    static constexpr int LPR = D / 8;
-    static constexpr int RPW = 32 / LPR;
-    static constexpr int NIT = kK3Chunk / RPW;
-    static_assert(NIT == LPR, "a chunk must give one key per lane");
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kChunkBytes = kK3Chunk * kRowBytes;
-    static constexpr int kRingBytes = kK3Stages * 2 * kChunkBytes;
-    static constexpr int kNewKVBytes = 2 * kRowBytes;
+    static constexpr int kBoxBytes = kK3Chunk * 128;         // 32 rows x 64 bf16, swizzled
+    static constexpr int kTileBytes = (D / 64) * kBoxBytes;  // K (or V) of one chunk
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRingBytes = kK3Stages * kStageBytes;
+    static constexpr int kNewBytes = kStageBytes;            // the new key as a one-key chunk
+    static constexpr int kQBytes = (HPC * D * 2 + 15) & ~15;
     static constexpr int kRedFloats = kK3ConsumerWarps * HPC * (D + 2);
-    static constexpr int kSmemBytes = kRingBytes + kNewKVBytes + kRedFloats * 4;
+    static constexpr int kSmemBytes = 1024 + kRingBytes + kNewBytes + kQBytes + kRedFloats * 4;
 };
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
-    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
-    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
-    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
-}
-
-// Eight bf16 as four fp32 pairs (element 2i in .x, 2i+1 in .y).
-__device__ __forceinline__ void unpack4x2(const uint4 v, float2 (&f)[4]) {
-    f[0] = make_float2(bf16lo(v.x), bf16hi(v.x));
-    f[1] = make_float2(bf16lo(v.y), bf16hi(v.y));
-    f[2] = make_float2(bf16lo(v.z), bf16hi(v.z));
-    f[3] = make_float2(bf16lo(v.w), bf16hi(v.w));
 }
 
 // One gpu-scope acquire-release increment (publishes this CTA's earlier writes,
@@ -78,13 +60,20 @@ __device__ __forceinline__ uint32_t atomic_inc_acq_rel(uint32_t *p) {
     return old;
 }
 
-// RMSNorm + RoPE of one head row at `pos`, distributed over the LPR lanes of
-// a row group; returns this lane's 8 values rounded to bf16 (as fp32) and the
-// packed words.  Cast placement as in K1.
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+// RMSNorm + RoPE of one head row at one position, distributed over the D/8
+// lanes of a row group (16 bytes each); cs holds (cos_a, sin_a, cos_b, sin_b)
+// for this lane's 8 dims.  Returns the lane's 8 values as packed bf16.  Cast
+// placement as in K1.
 template <int D>
-__device__ __forceinline__ void norm_rope_row(const __nv_bfloat16 *src, const __nv_bfloat16 *w,
-                                              const float4 (&cs)[4], float eps, int sub,
-                                              float (&out)[8], uint4 &packed) {
+__device__ __forceinline__ uint4 norm_rope_row(const __nv_bfloat16 *src, const __nv_bfloat16 *w,
+                                               const float4 (&cs)[4], float eps, int sub) {
     constexpr int LPR = D / 8, HALF = LPR / 2;
     const unsigned FULL = 0xffffffffu;
     const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(src) + sub);
@@ -105,7 +94,7 @@ __device__ __forceinline__ void norm_rope_row(const __nv_bfloat16 *src, const __
                           wf[2 * e + 1] * round_bf16(x[2 * e + 1] * r));
 #pragma unroll
     for (int e = 0; e < 4; ++e) pw[e] = __shfl_xor_sync(FULL, yw[e], HALF);
-    const bool lower = sub < HALF;
+    const bool lower = (sub % LPR) < HALF;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const float y0 = bf16lo(yw[e]), y1 = bf16hi(yw[e]);
@@ -113,89 +102,94 @@ __device__ __forceinline__ void norm_rope_row(const __nv_bfloat16 *src, const __
         const float r0 = lower ? y0 * cs[e].x - q0 * cs[e].y : y0 * cs[e].x + q0 * cs[e].y;
         const float r1 = lower ? y1 * cs[e].z - q1 * cs[e].w : y1 * cs[e].z + q1 * cs[e].w;
         ow[e] = pack_bf16(r0, r1);
-        out[2 * e] = bf16lo(ow[e]);
-        out[2 * e + 1] = bf16hi(ow[e]);
     }
-    packed = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    return make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
 
-// Online-softmax update of one warp with a chunk of nk (1..32) keys whose K
-// and V rows sit at Ks / Vs (row pitch D elements) in shared memory.
-template <int D, int HPC>
-__device__ __forceinline__ void consume_chunk(const __nv_bfloat16 *Ks, const __nv_bfloat16 *Vs,
-                                              int nk, const float2 (&q2)[HPC][4], float scale_log2,
-                                              float (&m)[HPC], float (&l)[HPC],
-                                              float2 (&o2)[HPC][4], int sub, int grp) {
-    using Sh = K3Shape<D, HPC>;
-    constexpr int LPR = Sh::LPR, RPW = Sh::RPW, NIT = Sh::NIT;
-    const unsigned FULL = 0xffffffffu;
+// Byte offset of the 16-byte block db (8 bf16) of row `row` in a chunk tile:
+// 64-column boxes of 32 rows x 128 bytes, 16-byte blocks XOR-swizzled by row.
+__device__ __forceinline__ uint32_t swz(int row, int db) {
+    return static_cast<uint32_t>((db >> 3) * (kK3Chunk * 128) + row * 128 +
+                                 (((db & 7) ^ (row & 7)) << 4));
+}
 
-    // Partial dot products over this lane's 8 dims, two at a time (packed fp32x2 FMA).
-    float acc[NIT][HPC];
+__device__ __forceinline__ uint32_t keep_pair(uint32_t x, bool lo, bool hi) {
+    return (lo ? (x & 0x0000ffffu) : 0u) | (hi ? (x & 0xffff0000u) : 0u);
+}
+
+// One warp consumes one chunk of nk (1..32) keys whose K and V tiles start at
+// shared addresses sK, sV.  Lane L < 16 owns query head L/4 (rows 4..15 of the
+// MMA tile are padding); its score fragment covers keys nt*8 + 2(L%4) + {0,1}.
+template <int D>
+__device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk,
+                                              const uint32_t (&qa0)[D / 16],
+                                              const uint32_t (&qa2)[D / 16], float c, float &m,
+                                              float &l, float2 (&o)[D / 8], float &z0, float &z1,
+                                              int lane) {
+    const unsigned FULL = 0xffffffffu;
+    const int mat = lane >> 3, r = lane & 7, q4 = lane & 3;
+    float2 s[4];
 #pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-        const int key = it * RPW + grp;
-        uint4 kv = make_uint4(0, 0, 0, 0);
-        if (key < nk) kv = *reinterpret_cast<const uint4 *>(Ks + key * D + 8 * sub);
-        float2 k2[4];
-        unpack4x2(kv, k2);
+    for (int nt = 0; nt < 4; ++nt) s[nt] = make_float2(0.f, 0.f);
+    // S = q' K^T: B fragments straight from the K rows (row = key, 8 dims per matrix row).
 #pragma unroll
-        for (int g = 0; g < HPC; ++g) {
-            float2 a = __fmul2_rn(q2[g][0], k2[0]);
+    for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
-            for (int e = 1; e < 4; ++e) a = __ffma2_rn(q2[g][e], k2[e], a);
-            acc[it][g] = a.x + a.y;
+        for (int ntp = 0; ntp < 2; ++ntp) {
+            const int key = (2 * ntp + (mat >> 1)) * 8 + r;
+            uint32_t b[4];
+            ldmatrix_x4(b, sK + swz(key, 2 * kk + (mat & 1)));
+            mma_bf16_16816(s[2 * ntp], z0, z1, qa0[kk], qa2[kk], b[0], b[1]);
+            mma_bf16_16816(s[2 * ntp + 1], z0, z1, qa0[kk], qa2[kk], b[2], b[3]);
         }
     }
-    // Reduce-scatter over the LPR lanes of the row group: afterwards acc[0][g]
-    // holds the full dot product of key (sub * RPW + grp).
+    // Online softmax on the fragment (keys past nk are masked out).
+    float mx = -INFINITY;
 #pragma unroll
-    for (int mk = LPR / 2; mk >= 1; mk >>= 1) {
-        const bool upper = (sub & mk) != 0;
-#pragma unroll
-        for (int i = 0; i < mk; ++i) {
-#pragma unroll
-            for (int g = 0; g < HPC; ++g) {
-                const float keep = upper ? acc[i + mk][g] : acc[i][g];
-                const float send = upper ? acc[i][g] : acc[i + mk][g];
-                acc[i][g] = keep + __shfl_xor_sync(FULL, send, mk);
-            }
-        }
+    for (int nt = 0; nt < 4; ++nt) {
+        if (nt * 8 + 2 * q4 >= nk) s[nt].x = -INFINITY;
+        if (nt * 8 + 2 * q4 + 1 >= nk) s[nt].y = -INFINITY;
+        mx = fmaxf(mx, fmaxf(s[nt].x, s[nt].y));
     }
-    const int my_key = sub * RPW + grp;
-    const bool my_valid = my_key < nk;
-    float pexp[HPC];
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+    const float m_new = fmaxf(m, mx);
+    const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * c);
+    const float neg = m_new * c;
+    float ps = 0.f;
+    uint32_t pa[2][2];  // P as A fragments: [k-step][a0 | a2]
 #pragma unroll
-    for (int g = 0; g < HPC; ++g) {
-        const float s = my_valid ? acc[0][g] : -INFINITY;
-        float mx = s;
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
-        const float m_new = fmaxf(m[g], mx);
-        const float alpha = (m[g] == -INFINITY) ? 0.f : ex2((m[g] - m_new) * scale_log2);
-        pexp[g] = my_valid ? ex2(fmaf(s, scale_log2, -m_new * scale_log2)) : 0.f;
-        l[g] = fmaf(l[g], alpha, pexp[g]);
-        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o2[g][e] = __fmul2_rn(o2[g][e], a2);
-        m[g] = m_new;
+    for (int nt = 0; nt < 4; ++nt) {
+        const float p0 = ex2(fmaf(s[nt].x, c, -neg));
+        const float p1 = ex2(fmaf(s[nt].y, c, -neg));
+        ps += p0 + p1;
+        pa[nt >> 1][nt & 1] = pack_bf16(p0, p1);
     }
+    l = fmaf(l, alpha, ps);
+    m = m_new;
 #pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-        const int key = it * RPW + grp;
-        float pk[HPC];
+    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int g = 0; g < HPC; ++g) pk[g] = __shfl_sync(FULL, pexp[g], grp * LPR + it);
-        if (key < nk) {
-            const uint4 vv = *reinterpret_cast<const uint4 *>(Vs + key * D + 8 * sub);
-            float2 v2[4];
-            unpack4x2(vv, v2);
+    for (int nt = 0; nt < D / 8; ++nt) o[nt] = __fmul2_rn(o[nt], a2);
+    // O += P V: B fragments from the V rows by transposing loads.  In a partial
+    // chunk the rows past nk may hold anything (stale or poisoned): drop them.
+    const bool partial = nk < kK3Chunk;
 #pragma unroll
-            for (int g = 0; g < HPC; ++g) {
-                const float2 p2 = make_float2(pk[g], pk[g]);
+    for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) o2[g][e] = __ffma2_rn(p2, v2[e], o2[g][e]);
+        for (int ndp = 0; ndp < D / 16; ++ndp) {
+            const int key = ks * 16 + (mat & 1) * 8 + r;
+            uint32_t b[4];
+            ldmatrix_x4_trans(b, sV + swz(key, 2 * ndp + (mat >> 1)));
+            if (partial) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int k0 = ks * 16 + (i & 1) * 8 + 2 * q4;
+                    b[i] = keep_pair(b[i], k0 < nk, k0 + 1 < nk);
+                }
             }
+            mma_bf16_16816(o[2 * ndp], z0, z1, pa[ks][0], pa[ks][1], b[0], b[1]);
+            mma_bf16_16816(o[2 * ndp + 1], z0, z1, pa[ks][0], pa[ks][1], b[2], b[3]);
         }
     }
 }
@@ -206,16 +200,18 @@ __device__ __forceinline__ void consume_chunk(const __nv_bfloat16 *Ks, const __n
 // kHostPositions = true is the allocation-free variant: positions and the
 // (cos, sin) of each sequence's position come in the kernel parameters
 // (pos_arr[b], cs_arr[b * D/2 + i]) and the caller keeps the lengths.
+// tmk / tmv: tensor maps (D, capacity, max_batch * Hkv) over this layer's K / V.
 template <int D, int HPC, bool kHostPositions>
 __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
-                                        const float2 *cs_arr) {
+                                        const float2 *cs_arr, const CUtensorMap *tmk,
+                                        const CUtensorMap *tmv) {
     using Sh = K3Shape<D, HPC>;
-    constexpr int LPR = Sh::LPR, RPW = Sh::RPW;
+    constexpr int LPR = D / 8;
     constexpr int NW = kK3ConsumerWarps;
     constexpr int NS = kK3Stages;
     const unsigned FULL = 0xffffffffu;
 
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS];
     __shared__ int s_abort;
     __shared__ int s_last;
@@ -223,10 +219,12 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
     __shared__ float s_w[HPC][kK3MaxSplits];  // split weights of the merge
     __shared__ float s_inv[HPC];
 
-    uint8_t *ring = smem;
-    __nv_bfloat16 *newk = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes);
-    __nv_bfloat16 *newv = newk + D;
-    float *red = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kNewKVBytes);
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sRing = smem_u32(smem);
+    const uint32_t sNew = sRing + Sh::kRingBytes;
+    __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes + Sh::kNewBytes);
+    float *red = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kNewBytes + Sh::kQBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x;
@@ -248,12 +246,8 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
     const int c_end = min(c_begin + cps, nchunks);
     const bool owner = split == S - 1;
     const int64_t kv_base = static_cast<int64_t>(b) * p.seq_stride + kvh * p.head_stride;
-    const __nv_bfloat16 *Kg = p.kc + kv_base;
-    const __nv_bfloat16 *Vg = p.vc + kv_base;
     const int h_first = kvh * p.G + hg * HPC;  // first query head of this CTA
-
-    auto ring_k = [&](int st) { return ring + st * 2 * Sh::kChunkBytes; };
-    auto ring_v = [&](int st) { return ring + st * 2 * Sh::kChunkBytes + Sh::kChunkBytes; };
+    const int tm_z = b * p.Hkv + kvh;          // (sequence, kv head) index in the tensor maps
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -268,6 +262,8 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
     if (warp == NW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            prefetch_tmap(tmk);
+            prefetch_tmap(tmv);
             const uint64_t policy = policy_evict_first();
             int issued = 0;
             for (int c = c_begin; c < c_end; ++c, ++issued) {
@@ -276,13 +272,16 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
                     !mbar_wait(smem_u32(&bar_empty[st]), ((issued / NS) - 1) & 1, &s_abort, p.err,
                                kKernK3, 2))
                     break;
-                const int nk = min(kK3Chunk, pos - c * kK3Chunk);
-                const uint32_t bytes = static_cast<uint32_t>(nk) * Sh::kRowBytes;
                 const uint32_t fb = smem_u32(&bar_full[st]);
-                mbar_expect_tx(fb, 2 * bytes);
-                const int64_t off = static_cast<int64_t>(c) * kK3Chunk * D;
-                bulk_g2s_evict_first(smem_u32(ring_k(st)), Kg + off, bytes, fb, policy);
-                bulk_g2s_evict_first(smem_u32(ring_v(st)), Vg + off, bytes, fb, policy);
+                mbar_expect_tx(fb, Sh::kStageBytes);
+                const uint32_t dk = sRing + st * Sh::kStageBytes;
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x) {
+                    tma_load_3d_hint(dk + x * Sh::kBoxBytes, tmk, x * 64, c * kK3Chunk, tm_z, fb,
+                                     policy);
+                    tma_load_3d_hint(dk + Sh::kTileBytes + x * Sh::kBoxBytes, tmv, x * 64,
+                                     c * kK3Chunk, tm_z, fb, policy);
+                }
             }
             // No copy may land after the CTA exits: wait (bounded) for the last ones.
             for (int i = max(0, issued - NS); i < issued; ++i) {
@@ -292,7 +291,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
         }
     } else {
         // ------------------------------------------------------------ consumers
-        const int sub = lane % LPR, grp = lane / LPR;
+        const int sub = lane % LPR;
         float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims at pos
         if constexpr (kHostPositions) {
             const float4 *src = reinterpret_cast<const float4 *>(cs_arr + b * (D / 2) +
@@ -305,87 +304,77 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
 #pragma unroll
             for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + e);
         }
-        float2 q2[HPC][4];
-#pragma unroll
-        for (int g = 0; g < HPC; ++g) {
-            uint4 unused;
-            float qf[8];
-            norm_rope_row<D>(p.q + (static_cast<int64_t>(b) * p.Hq + h_first + g) * D, p.wq, cs,
-                             p.eps, sub, qf, unused);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) q2[g][e] = make_float2(qf[2 * e], qf[2 * e + 1]);
+        // Warp w norms and rotates query head w of the CTA into shared memory.
+        if (warp < HPC) {
+            const uint4 qp = norm_rope_row<D>(
+                p.q + (static_cast<int64_t>(b) * p.Hq + h_first + warp) * D, p.wq, cs, p.eps, sub);
+            if (lane < LPR) reinterpret_cast<uint4 *>(qs + warp * D)[sub] = qp;
         }
-        if (owner && warp == 0) {
-            float kf[8];
-            uint4 kp;
-            norm_rope_row<D>(p.k + (static_cast<int64_t>(b) * p.Hkv + kvh) * D, p.wk, cs, p.eps,
-                             sub, kf, kp);
+        if (owner && warp == NW - 1) {
+            // The new token: k' and v as row 0 of a one-key chunk (rows 1-31 zero),
+            // and into cache slot pos for later steps.
+            const uint4 kp = norm_rope_row<D>(p.k + (static_cast<int64_t>(b) * p.Hkv + kvh) * D,
+                                              p.wk, cs, p.eps, sub);
             const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(
                                        p.v + (static_cast<int64_t>(b) * p.Hkv + kvh) * D) +
                                    sub);
-            if (grp == 0) {
-                reinterpret_cast<uint4 *>(newk)[sub] = kp;
-                reinterpret_cast<uint4 *>(newv)[sub] = vv;
-                // Slot pos is read only by later launches.  With several head
-                // groups the first one writes.
-                if (hg == 0) {
+            uint4 *nz = reinterpret_cast<uint4 *>(smem + Sh::kRingBytes);
+            for (int i = lane; i < Sh::kNewBytes / 16; i += 32) nz[i] = make_uint4(0, 0, 0, 0);
+            __syncwarp();
+            if (lane < LPR) {
+                *reinterpret_cast<uint4 *>(smem + Sh::kRingBytes + swz(0, sub)) = kp;
+                *reinterpret_cast<uint4 *>(smem + Sh::kRingBytes + Sh::kTileBytes + swz(0, sub)) = vv;
+                if (hg == 0) {  // slot pos is read only by later launches
                     reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[sub] = kp;
                     reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[sub] = vv;
                 }
             }
-            __syncwarp();
         }
+        asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");  // q' and the new key ready
 
-        float m[HPC], l[HPC];
-        float2 o2[HPC][4];
+        // A fragments of q' (rows = heads 0..3 of the 16-row tile; padding rows zero).
+        const int hrow = lane >> 2, q4 = lane & 3;
+        const bool real = lane < 16 && hrow < HPC;
+        uint32_t qa0[D / 16], qa2[D / 16];
 #pragma unroll
-        for (int g = 0; g < HPC; ++g) {
-            m[g] = -INFINITY;
-            l[g] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qs + hrow * D + 16 * kk);
+            qa0[kk] = real ? qrow[q4] : 0u;
+            qa2[kk] = real ? qrow[4 + q4] : 0u;
         }
+        float m = -INFINITY, l = 0.f;
+        float2 o[D / 8];
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) o[nt] = make_float2(0.f, 0.f);
+        float z0 = 0.f, z1 = 0.f;  // rows 8-15 of every MMA tile (all zero, never read)
+
         for (int c = c_begin + warp, i = warp; c < c_end; c += NW, i += NW) {
             const int st = i % NS;
             bool ok = mbar_wait(smem_u32(&bar_full[st]), (i / NS) & 1, &s_abort, p.err, kKernK3, 4);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             const int nk = min(kK3Chunk, pos - c * kK3Chunk);
-            consume_chunk<D, HPC>(reinterpret_cast<const __nv_bfloat16 *>(ring_k(st)),
-                                  reinterpret_cast<const __nv_bfloat16 *>(ring_v(st)), nk, q2,
-                                  p.scale_log2, m, l, o2, sub, grp);
+            const uint32_t sk = sRing + st * Sh::kStageBytes;
+            consume_chunk<D>(sk, sk + Sh::kTileBytes, nk, qa0, qa2, p.scale_log2, m, l, o, z0, z1,
+                             lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_empty[st]));
         }
-        if (owner && warp == 0)
-            consume_chunk<D, HPC>(newk, newv, 1, q2, p.scale_log2, m, l, o2, sub, grp);
+        if (owner && warp == NW - 1)
+            consume_chunk<D>(sNew, sNew + Sh::kTileBytes, 1, qa0, qa2, p.scale_log2, m, l, o, z0,
+                             z1, lane);
 
-        // Sum the RPW row groups (same sub, different grp) and the lane sums of l.
-#pragma unroll
-        for (int off = LPR; off < 32; off <<= 1)
-#pragma unroll
-            for (int g = 0; g < HPC; ++g)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    o2[g][e].x += __shfl_xor_sync(FULL, o2[g][e].x, off);
-                    o2[g][e].y += __shfl_xor_sync(FULL, o2[g][e].y, off);
-                }
-#pragma unroll
-        for (int g = 0; g < HPC; ++g)
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) l[g] += __shfl_xor_sync(FULL, l[g], off);
         // Warp results -> shared memory: red[w][g][0..D) = o, [D] = m, [D+1] = l.
+        l += __shfl_xor_sync(FULL, l, 1);
+        l += __shfl_xor_sync(FULL, l, 2);
+        if (real) {
+            float *dst = red + (warp * HPC + hrow) * (D + 2);
 #pragma unroll
-        for (int g = 0; g < HPC; ++g) {
-            float *dst = red + (warp * HPC + g) * (D + 2);
-            if (grp == 0) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    reinterpret_cast<float2 *>(dst + 8 * sub)[e] = o2[g][e];
-            }
-            if (lane == 0) {
-                dst[D] = m[g];
-                dst[D + 1] = l[g];
+            for (int nt = 0; nt < D / 8; ++nt)
+                *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * q4) = o[nt];
+            if (q4 == 0) {
+                dst[D] = m;
+                dst[D + 1] = l;
             }
         }
     }
@@ -507,7 +496,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
 template <int D, int HPC>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_kernel(const __grid_constant__ K3Params p) {
-    k3_body<D, HPC, false>(p, nullptr, nullptr);
+    k3_body<D, HPC, false>(p, nullptr, nullptr, p.tm_k, p.tm_v);
 }
 
 template <int D, int HPC>
@@ -568,7 +557,8 @@ constexpr size_t kNoAllocPartOffset = 32768;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-struct __align__(16) K3NoAllocParams {
+struct alignas(64) K3NoAllocParams {
+    CUtensorMap tmk, tmv;              // over the caller's K / V of this layer
     float2 cs[kNoAllocMaxBatch * 64];  // (cos, sin) at pos[b] of the D/2 frequencies, [b][i]
     int pos[kNoAllocMaxBatch];         // slot of each sequence's new token
     K3Params base;
@@ -577,7 +567,7 @@ struct __align__(16) K3NoAllocParams {
 template <int D, int HPC>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_noalloc_kernel(const __grid_constant__ K3NoAllocParams p) {
-    k3_body<D, HPC, true>(p.base, p.pos, p.cs);
+    k3_body<D, HPC, true>(p.base, p.pos, p.cs, &p.tmk, &p.tmv);
 }
 
 template <int D, int HPC>
@@ -691,6 +681,9 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     }
 
     K3NoAllocParams p{};
+    if (!encode_decode_map(&p.tmk, k_cache, D, g.capacity, g.max_batch * g.n_kv_heads) ||
+        !encode_decode_map(&p.tmv, v_cache, D, g.capacity, g.max_batch * g.n_kv_heads))
+        return QA_ERR_CUDA;
     for (int b = 0; b < batch; ++b) {
         p.pos[b] = positions[b];
         for (int i = 0; i < D / 2; ++i) {  // same fp64 formula as the cache's table
@@ -703,6 +696,8 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     unsigned char *scr = dev->scratch;
     const size_t nrows = static_cast<size_t>(batch) * g.n_q_heads * S;
     K3Params &bp = p.base;
+    bp.tm_k = nullptr;  // the kernel takes the maps from the parameter block
+    bp.tm_v = nullptr;
     bp.q = static_cast<const __nv_bfloat16 *>(q);
     bp.k = static_cast<const __nv_bfloat16 *>(k);
     bp.v = static_cast<const __nv_bfloat16 *>(v);

@@ -36,6 +36,7 @@ struct qa_cache {
     float *part_m = nullptr, *part_l = nullptr, *part_o = nullptr;
     uint32_t *grp_cnt = nullptr, *seq_cnt = nullptr;
     uint32_t *err = nullptr;
+    CUtensorMap *dmaps = nullptr;  // device: [layer][K, V] decode tensor maps
     std::vector<int32_t> lens_host;
     uint64_t kv_bytes = 0, scratch_bytes = 0;
     std::atomic<uint64_t> launches[QA_NUM_KERNELS];
@@ -87,6 +88,7 @@ void free_all(qa_cache *c) {
     cudaFree(c->grp_cnt);
     cudaFree(c->seq_cnt);
     cudaFree(c->err);
+    cudaFree(c->dmaps);
 }
 
 template <typename T>
@@ -138,6 +140,24 @@ bool encode_q_map(CUtensorMap *m, void *base, int D, int Hq, int T) {
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+}  // namespace
+
+bool qa::encode_decode_map(CUtensorMap *m, void *base, int D, int capacity, int rows_z) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(capacity),
+                                static_cast<cuuint64_t>(rows_z)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(capacity) * D * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(qa::kK3Chunk), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 
 int choose_splits(const qa_cache *c, int batch, int pos_max) {
     const int nchunks = (pos_max + qa::kK3Chunk - 1) / qa::kK3Chunk;
@@ -298,7 +318,19 @@ QA_API qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out) {
                     make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
             }
         ok = cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) ==
-                 cudaSuccess &&
+                 cudaSuccess;
+    }
+    if (ok) {
+        // Decode tensor maps, two per layer, kept in device memory.
+        std::vector<CUtensorMap> maps(static_cast<size_t>(2) * g.num_layers);
+        for (int l = 0; ok && l < g.num_layers; ++l)
+            ok = qa::encode_decode_map(&maps[2 * l], c->K + l * c->layer_elems, D, g.capacity,
+                                       g.max_batch * g.n_kv_heads) &&
+                 qa::encode_decode_map(&maps[2 * l + 1], c->V + l * c->layer_elems, D, g.capacity,
+                                       g.max_batch * g.n_kv_heads);
+        ok = ok && dev_alloc(&c->dmaps, maps.size(), scr) &&
+             cudaMemcpy(c->dmaps, maps.data(), maps.size() * sizeof(CUtensorMap),
+                        cudaMemcpyHostToDevice) == cudaSuccess &&
              cudaDeviceSynchronize() == cudaSuccess;
     }
     if (!ok) {
@@ -445,6 +477,8 @@ QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q
         pos_max = std::max(pos_max, mirror[b]);
     }
     K3Params p{};
+    p.tm_k = c->dmaps + 2 * layer;
+    p.tm_v = c->dmaps + 2 * layer + 1;
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.k = static_cast<const __nv_bfloat16 *>(k);
     p.v = static_cast<const __nv_bfloat16 *>(v);

@@ -61,6 +61,7 @@ constexpr int kK3Chunk = 32;        // keys per pipeline chunk
 constexpr int kK3MaxSplits = 64;
 
 struct K3Params {
+    const CUtensorMap *tm_k, *tm_v;  // (D, capacity, max_batch * Hkv) over this layer's K / V
     const __nv_bfloat16 *q, *k, *v;  // [B][Hq][D], [B][Hkv][D]
     const __nv_bfloat16 *wq, *wk;
     __nv_bfloat16 *kc, *vc;          // layer base
@@ -81,6 +82,9 @@ struct K3Params {
 #include <cuda_runtime.h>
 
 namespace qa {
+// Tensor map of the decode kernel over one layer's K or V: (D, capacity,
+// max_batch * Hkv), 64 x 32 x 1 boxes, 128-byte swizzle.  Host-only encode.
+bool encode_decode_map(CUtensorMap *m, void *base, int D, int capacity, int rows_z);
 // Host launchers, one per kernel file.
 cudaError_t launch_k1(const K1Params &p, int D, cudaStream_t stream);
 cudaError_t launch_k2(const K2Params &p, int D, int nitems, cudaStream_t stream);

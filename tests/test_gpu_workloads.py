@@ -83,9 +83,9 @@ def test_b4_prompt2048_128_steps_with_reset_reruns(qa, oracle_mod):
                 qa.qa_decode_step(c.h, 0, w.B, dq[s], dk[s], dv[s], wq, wk, douts[s])
             torch.cuda.synchronize()
             runs.append((bits(out), bits(douts)))
-        for a, b in runs[1:]:  # reset state is clean: reruns are bit-identical
-            np.testing.assert_array_equal(a[0], runs[0][0])
-            np.testing.assert_array_equal(b[1], runs[0][1])
+        for pre, dec in runs[1:]:  # reset state is clean: reruns are bit-identical
+            np.testing.assert_array_equal(pre, runs[0][0])
+            np.testing.assert_array_equal(dec, runs[0][1])
         got_pre = F(runs[0][0])
         got_dec = F(runs[0][1])
         lay = oracle_mod.OracleLayer(oracle_mod.Geometry(w.B, w.Hq, w.Hkv, w.D, w.cap))
