@@ -43,7 +43,9 @@ struct K3Shape {
     static constexpr int kNewBytes = kStageBytes;            // the new key as a one-key chunk
     static constexpr int kQBytes = (HPC * D * 2 + 15) & ~15;
     static constexpr int kRedFloats = kK3ConsumerWarps * HPC * (D + 2);
-    static constexpr int kSmemBytes = 1024 + kRingBytes + kNewBytes + kQBytes + kRedFloats * 4;
+    static constexpr int kPartFloats = HPC * (D + 2);  // this CTA's split partial
+    static constexpr int kSmemBytes =
+        1024 + kRingBytes + kNewBytes + kQBytes + (kRedFloats + kPartFloats) * 4;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -214,10 +216,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS];
     __shared__ int s_abort;
-    __shared__ int s_last;
     __shared__ uint32_t s_seq_prev;
-    __shared__ float s_w[HPC][kK3MaxSplits];  // split weights of the merge
-    __shared__ float s_inv[HPC];
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -225,6 +224,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
     const uint32_t sNew = sRing + Sh::kRingBytes;
     __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes + Sh::kNewBytes);
     float *red = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kNewBytes + Sh::kQBytes);
+    float *part = red + Sh::kRedFloats;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x;
@@ -249,48 +249,36 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
     const int h_first = kvh * p.G + hg * HPC;  // first query head of this CTA
     const int tm_z = b * p.Hkv + kvh;          // (sequence, kv head) index in the tensor maps
 
-    if (threadIdx.x == 0) {
+    const int my_chunks = c_end - c_begin;
+    uint64_t policy = 0;
+    // Stage `st` receives chunk c: K then V, each D/64 boxes of 32 rows.
+    auto issue = [&](int c, int st) {
+        const uint32_t fb = smem_u32(&bar_full[st]);
+        mbar_expect_tx(fb, Sh::kStageBytes);
+        const uint32_t dk = sRing + st * Sh::kStageBytes;
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x) {
+            tma_load_3d_hint(dk + x * Sh::kBoxBytes, tmk, x * 64, c * kK3Chunk, tm_z, fb, policy);
+            tma_load_3d_hint(dk + Sh::kTileBytes + x * Sh::kBoxBytes, tmv, x * 64, c * kK3Chunk,
+                             tm_z, fb, policy);
+        }
+    };
+    if (warp == NW && lane == 0) {
+        // The TMA thread sets up the ring and starts the first loads at once; the
+        // consumers' prologue below overlaps their latency.
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&bar_full[s]), 1);
             mbar_init(smem_u32(&bar_empty[s]), 1);
         }
         s_abort = 0;
         fence_mbar_init();
+        prefetch_tmap(tmk);
+        prefetch_tmap(tmv);
+        policy = policy_evict_first();
+        for (int i = 0; i < min(NS, my_chunks); ++i) issue(c_begin + i, i);
     }
-    __syncthreads();
-
-    if (warp == NW) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tmap(tmk);
-            prefetch_tmap(tmv);
-            const uint64_t policy = policy_evict_first();
-            int issued = 0;
-            for (int c = c_begin; c < c_end; ++c, ++issued) {
-                const int st = issued % NS;
-                if (issued >= NS &&
-                    !mbar_wait(smem_u32(&bar_empty[st]), ((issued / NS) - 1) & 1, &s_abort, p.err,
-                               kKernK3, 2))
-                    break;
-                const uint32_t fb = smem_u32(&bar_full[st]);
-                mbar_expect_tx(fb, Sh::kStageBytes);
-                const uint32_t dk = sRing + st * Sh::kStageBytes;
-#pragma unroll
-                for (int x = 0; x < D / 64; ++x) {
-                    tma_load_3d_hint(dk + x * Sh::kBoxBytes, tmk, x * 64, c * kK3Chunk, tm_z, fb,
-                                     policy);
-                    tma_load_3d_hint(dk + Sh::kTileBytes + x * Sh::kBoxBytes, tmv, x * 64,
-                                     c * kK3Chunk, tm_z, fb, policy);
-                }
-            }
-            // No copy may land after the CTA exits: wait (bounded) for the last ones.
-            for (int i = max(0, issued - NS); i < issued; ++i) {
-                int dummy = 0;
-                mbar_wait(smem_u32(&bar_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK3, 3);
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ consumers
+    if (warp < NW) {
+        // ------------------------------------------------------------ consumer prologue
         const int sub = lane % LPR;
         float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims at pos
         if constexpr (kHostPositions) {
@@ -330,8 +318,28 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
                 }
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");  // q' and the new key ready
+    }
+    __syncthreads();  // ring initialised, q' and the new key in shared memory
 
+    if (warp == NW) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued = min(NS, my_chunks);
+            for (; issued < my_chunks; ++issued) {
+                const int st = issued % NS;
+                if (!mbar_wait(smem_u32(&bar_empty[st]), ((issued / NS) - 1) & 1, &s_abort, p.err,
+                               kKernK3, 2))
+                    break;
+                issue(c_begin + issued, st);
+            }
+            // No copy may land after the CTA exits: wait (bounded) for the last ones.
+            for (int i = max(0, issued - NS); i < issued; ++i) {
+                int dummy = 0;
+                mbar_wait(smem_u32(&bar_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK3, 3);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
         // A fragments of q' (rows = heads 0..3 of the 16-row tile; padding rows zero).
         const int hrow = lane >> 2, q4 = lane & 3;
         const bool real = lane < 16 && hrow < HPC;
@@ -381,9 +389,8 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
     __syncthreads();
 
     // ---------------------------------------------------------------- CTA combine
-    // Thread t (of the 160) combines elements (g, d) of the CTA's HPC x D partial.
-    const bool single = (S == 1);
-    const int64_t part_row = (static_cast<int64_t>(b) * p.Hq + h_first) * S + split;  // head g at + g*S
+    // Thread t (of the 160) combines elements (g, d) of the CTA's HPC x D
+    // partial: part[g][0..D) = o, part[g][D] = m, part[g][D+1] = l.
     for (int idx = threadIdx.x; idx < HPC * D; idx += blockDim.x) {
         const int g = idx / D, d = idx % D;
         float M = -INFINITY;
@@ -401,96 +408,61 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
                 O = fmaf(sc, src[d], O);
             }
         }
-        if (single) {
-            p.out[(static_cast<int64_t>(b) * p.Hq + h_first + g) * D + d] =
-                __float2bfloat16_rn(O / Lsum);
-        } else {
-            const int64_t prow = part_row + static_cast<int64_t>(g) * S;
-            p.part_o[prow * D + d] = O;
-            if (d == 0) {
-                p.part_m[prow] = M;
-                p.part_l[prow] = Lsum;
-            }
+        part[g * (D + 2) + d] = O;
+        if (d == 0) {
+            part[g * (D + 2) + D] = M;
+            part[g * (D + 2) + D + 1] = Lsum;
         }
     }
 
-    if (!single) {
-        __syncthreads();  // all partial writes of this CTA precede the release below
-        if (threadIdx.x == 0) {
-            uint32_t *cnt = p.grp_cnt + static_cast<int64_t>(b) * p.Hkv * p.HG + blockIdx.y;
-            const uint32_t prev = atomic_inc_acq_rel(cnt);
-            s_last = (prev == static_cast<uint32_t>(S - 1));
-            if (s_last) *cnt = 0u;  // ready for the next launch
-        }
-        __syncthreads();
-        if (!s_last) return;
+    // ---------------------------------------------------------------- split merge
+    // The S CTAs of this (sequence, kv head, head group) form one cluster.  After
+    // the barrier every CTA's partial is visible; CTA `split` merges its share of
+    // the HPC x D outputs by reading all S partials through distributed shared
+    // memory, in split order (deterministic for a given length).
+    cluster_sync();
+    if (!kHostPositions && split == 0 && threadIdx.x == 0) {
+        // Every CTA of this group has read lens[b]: count the group towards
+        // sequence b; the last group advances lens[b] below.
+        s_seq_prev = atomic_inc_acq_rel(p.seq_cnt + b);
     }
-    // This CTA is the last of its group, so every CTA of the group has read
-    // lens[b].  Count the group towards sequence b now: the atomic's latency
-    // overlaps the merge below, and the last group advances lens[b] at the end.
-    if (!kHostPositions && threadIdx.x == 0) s_seq_prev = atomic_inc_acq_rel(p.seq_cnt + b);
-    if (!single) {
-        // ------------------------------------------------------------ split merge
-        // Warp g turns head g's split maxima into weights 2^((m_s - M) c) (lanes
-        // over splits) and 1 / sum_s w_s l_s; then every thread merges four
-        // output dims of one head over all splits in a fixed order, its loads
-        // unrolled so that they overlap.
-        if (warp < HPC) {
-            const int g = warp;
-            const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h_first + g) * S;
-            float ms[2], ls[2];
+    {
+        const int total = HPC * D;
+        const int E = (total + S - 1) / S;
+        const int hi = min((split + 1) * E, total);
+        for (int idx = split * E + threadIdx.x; idx < hi; idx += blockDim.x) {
+            const int g = idx / D, d = idx % D;
+            const uint32_t a_m = smem_u32(part + g * (D + 2) + D);
+            const uint32_t a_o = smem_u32(part + g * (D + 2) + d);
+            float ms[kK3MaxSplits];
+            float M = -INFINITY;
 #pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int s = lane + 32 * k2;
-                ms[k2] = s < S ? __ldcg(p.part_m + row0 + s) : -INFINITY;
-                ls[k2] = s < S ? __ldcg(p.part_l + row0 + s) : 0.f;
+            for (int s = 0; s < kK3MaxSplits; ++s) {
+                ms[s] = s < S ? ld_cluster_f32(map_rank(a_m, s)) : -INFINITY;
+                M = fmaxf(M, ms[s]);
             }
-            float M = fmaxf(ms[0], ms[1]);
+            float Lsum = 0.f, O = 0.f;
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
-            float Lsum = 0.f;
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int s = lane + 32 * k2;
-                const float w = ms[k2] == -INFINITY ? 0.f : ex2((ms[k2] - M) * p.scale_log2);
-                if (s < S) s_w[g][s] = w;
-                Lsum = fmaf(w, ls[k2], Lsum);
+            for (int s = 0; s < kK3MaxSplits; ++s) {
+                if (s < S && ms[s] != -INFINITY) {
+                    const float w = ex2((ms[s] - M) * p.scale_log2);
+                    Lsum = fmaf(w, ld_cluster_f32(map_rank(a_m + 4, s)), Lsum);
+                    O = fmaf(w, ld_cluster_f32(map_rank(a_o, s)), O);
+                }
             }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) Lsum += __shfl_xor_sync(FULL, Lsum, off);
-            if (lane == 0) s_inv[g] = 1.f / Lsum;
-        }
-        __syncthreads();
-        constexpr int D4 = D / 4;
-        for (int idx = threadIdx.x; idx < HPC * D4; idx += blockDim.x) {
-            const int g = idx / D4, d4 = idx % D4;
-            const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h_first + g) * S;
-            const float4 *po = reinterpret_cast<const float4 *>(p.part_o + row0 * D) + d4;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int s = 0; s < S; ++s) {
-                const float4 v = __ldcg(po + static_cast<int64_t>(s) * D4);
-                const float w = s_w[g][s];
-                acc.x = fmaf(w, v.x, acc.x);
-                acc.y = fmaf(w, v.y, acc.y);
-                acc.z = fmaf(w, v.z, acc.z);
-                acc.w = fmaf(w, v.w, acc.w);
-            }
-            const float inv = s_inv[g];
-            uint2 o;
-            o.x = pack_bf16(acc.x * inv, acc.y * inv);
-            o.y = pack_bf16(acc.z * inv, acc.w * inv);
-            reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(b) * p.Hq + h_first + g) * D)[d4] = o;
+            p.out[(static_cast<int64_t>(b) * p.Hq + h_first + g) * D + d] =
+                __float2bfloat16_rn(O / Lsum);
         }
     }
-    // ---------------------------------------------------------------- length update
     if constexpr (!kHostPositions) {
         __syncthreads();
-        if (threadIdx.x == 0 && s_seq_prev == static_cast<uint32_t>(p.Hkv * p.HG) - 1u) {
+        if (split == 0 && threadIdx.x == 0 &&
+            s_seq_prev == static_cast<uint32_t>(p.Hkv * p.HG) - 1u) {
             p.lens[b] = pos + 1;
             p.seq_cnt[b] = 0u;
         }
     }
+    cluster_sync();  // peers may still be reading this CTA's partial
 }
 
 template <int D, int HPC>
@@ -508,6 +480,9 @@ static cudaError_t launch_k3_t(const K3Params &p, cudaStream_t stream) {
     if (dev < 31 && !(configured_mask & (1 << dev))) {
         cudaError_t e = cudaFuncSetAttribute(k3_decode_kernel<D, HPC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k3_decode_kernel<D, HPC>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << dev;
     }
@@ -516,12 +491,81 @@ static cudaError_t launch_k3_t(const K3Params &p, cudaStream_t stream) {
     cfg.blockDim = dim3((kK3ConsumerWarps + 1) * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;  // one cluster = the splits of a group
+    attr[0].val.clusterDim.x = p.S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k3_decode_kernel<D, HPC>, p);
+}
+
+template <int D, int HPC>
+static int cluster_capacity_t(int S) {
+    constexpr int smem = K3Shape<D, HPC>::kSmemBytes;
+    auto kern = k3_decode_kernel<D, HPC>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S, 1, 1);
+    cfg.blockDim = dim3((kK3ConsumerWarps + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k3_decode_kernel<D, HPC>, p);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int k3_cluster_capacity(int D, int HPC, int S) {
+    constexpr int kDev = 16;
+    // [device][D == 128][HPC 1/2/4][S]: 0 = not queried yet, -1 = query failed
+    static int cache[kDev][2][3][kK3MaxSplits + 1] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (S < 1 || S > kK3MaxSplits || cudaGetDevice(&dev) != cudaSuccess || dev >= kDev) return 0;
+    const int di = D == 128 ? 1 : 0, hi = HPC == 4 ? 2 : (HPC == 2 ? 1 : 0);
+    std::lock_guard<std::mutex> lock(mu);
+    int &slot = cache[dev][di][hi][S];
+    if (slot == 0) {
+        int n = 0;
+        if (D == 128)
+            n = HPC == 4 ? cluster_capacity_t<128, 4>(S)
+                         : (HPC == 2 ? cluster_capacity_t<128, 2>(S) : cluster_capacity_t<128, 1>(S));
+        else
+            n = HPC == 4 ? cluster_capacity_t<64, 4>(S)
+                         : (HPC == 2 ? cluster_capacity_t<64, 2>(S) : cluster_capacity_t<64, 1>(S));
+        slot = n > 0 ? n : -1;
+    }
+    return slot > 0 ? slot : 0;
+}
+
+int k3_choose_splits(int D, int HPC, int groups, int pos_max) {
+    const int nchunks = (pos_max + kK3Chunk - 1) / kK3Chunk;
+    int best = 1;
+    for (int S = 2; S <= std::min(kK3MaxSplits, std::max(1, nchunks)); ++S)
+        if (k3_cluster_capacity(D, HPC, S) >= groups) best = S;
+    if (best > 1) {  // equal whole-chunk shares; drop splits that would be empty
+        const int cps = (nchunks + best - 1) / best;
+        best = (nchunks + cps - 1) / cps;
+    }
+    return best;
 }
 
 cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream) {
@@ -541,19 +585,16 @@ cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream) {
 
 // ==================================================================== allocation-free decode step
 // qa_decode_step_noalloc runs the same decode kernel body for callers that may
-// not allocate device memory.  Its scratch (split partials, counters, error
-// word) lives in a fixed array of this module: the CUDA driver creates it when
-// the library's device code loads on a GPU, and it stays until the process
-// exits.  Host code never dereferences the symbol; it asks the runtime for the
-// array's device address once per device.
+// not allocate device memory.  The kernel's global scratch lives in a fixed
+// array of this module: the CUDA driver creates it when the library's device
+// code loads on a GPU, and it stays until the process exits.  Host code never
+// dereferences the symbol; it asks the runtime for the array's device address
+// once per device.  (The splits are merged in distributed shared memory, so
+// the array holds the error word only.)
 namespace qa {
 
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per GPU
-constexpr int kNoAllocMaxGroups = 4096;                   // batch * Hkv * head groups
+constexpr size_t kNoAllocScratchBytes = 256;
 constexpr int kNoAllocMaxBatch = 16;
-constexpr size_t kNoAllocErrOffset = kNoAllocMaxGroups * sizeof(uint32_t);
-constexpr size_t kNoAllocClearBytes = kNoAllocErrOffset + 256;  // counters + error word
-constexpr size_t kNoAllocPartOffset = 32768;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -575,10 +616,23 @@ static cudaError_t launch_noalloc_t(const K3NoAllocParams &p, cudaStream_t strea
     constexpr int smem = K3Shape<D, HPC>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(k3_decode_noalloc_kernel<D, HPC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k3_decode_noalloc_kernel<D, HPC>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    const dim3 grid(p.base.S, p.base.Hkv * p.base.HG, p.base.B);
-    k3_decode_noalloc_kernel<D, HPC><<<grid, (kK3ConsumerWarps + 1) * 32, smem, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.base.S, p.base.Hkv * p.base.HG, p.base.B);
+    cfg.blockDim = dim3((kK3ConsumerWarps + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.base.S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k3_decode_noalloc_kernel<D, HPC>, p);
 }
 
 static cudaError_t launch_noalloc(const K3NoAllocParams &p, int D, int HPC, cudaStream_t stream) {
@@ -661,24 +715,13 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     }
     const int HPC = std::min(G, 4), HG = G / HPC, D = g.head_dim;
     const int groups = batch * g.n_kv_heads * HG;
-    if (groups > kNoAllocMaxGroups) return QA_ERR_UNSUPPORTED_SHAPE;  // above the counters
+    if (g.n_kv_heads * HG > 65535) return QA_ERR_UNSUPPORTED_SHAPE;
     NoAllocDevice *dev = nullptr;
     qa_status st = noalloc_setup(dev);
     if (st != QA_OK) return st;
 
-    // Split plan as in qa_decode_step, further capped by the partials the
-    // scratch array can hold (one split needs no partials at all).
-    const int nchunks = (pos_max + kK3Chunk - 1) / kK3Chunk;
-    int S = std::max(1, (2 * dev->num_sms) / groups);
-    S = std::min(S, std::max(1, nchunks));
-    S = std::min(S, kK3MaxSplits);
-    const size_t per_split = static_cast<size_t>(batch) * g.n_q_heads * (D + 2) * sizeof(float);
-    const size_t room = kNoAllocScratchBytes - kNoAllocPartOffset - 256;
-    S = std::min<size_t>(S, std::max<size_t>(1, room / per_split));
-    if (S > 1) {
-        const int cps = (nchunks + S - 1) / S;
-        S = (nchunks + cps - 1) / cps;
-    }
+    // Split plan as in qa_decode_step (the variant has the same resources).
+    const int S = k3_choose_splits(D, HPC, groups, pos_max);
 
     K3NoAllocParams p{};
     if (!encode_decode_map(&p.tmk, k_cache, D, g.capacity, g.max_batch * g.n_kv_heads) ||
@@ -694,7 +737,6 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
         }
     }
     unsigned char *scr = dev->scratch;
-    const size_t nrows = static_cast<size_t>(batch) * g.n_q_heads * S;
     K3Params &bp = p.base;
     bp.tm_k = nullptr;  // the kernel takes the maps from the parameter block
     bp.tm_v = nullptr;
@@ -707,13 +749,8 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     bp.vc = static_cast<__nv_bfloat16 *>(v_cache);
     bp.lens = nullptr;
     bp.rope = nullptr;
-    bp.grp_cnt = reinterpret_cast<uint32_t *>(scr);
     bp.seq_cnt = nullptr;
-    bp.err = reinterpret_cast<uint32_t *>(scr + kNoAllocErrOffset);
-    bp.part_m = reinterpret_cast<float *>(scr + kNoAllocPartOffset);
-    bp.part_l = bp.part_m + nrows;
-    const size_t o_off = (kNoAllocPartOffset + 2 * nrows * sizeof(float) + 255) & ~size_t(255);
-    bp.part_o = reinterpret_cast<float *>(scr + o_off);
+    bp.err = reinterpret_cast<uint32_t *>(scr);
     bp.out = static_cast<__nv_bfloat16 *>(out);
     bp.head_stride = static_cast<int64_t>(g.capacity) * D;
     bp.seq_stride = bp.head_stride * g.n_kv_heads;
@@ -728,8 +765,8 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     bp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: counters and error word start at zero.
-    if (cudaMemsetAsync(scr, 0, kNoAllocClearBytes, s) != cudaSuccess) return QA_ERR_CUDA;
+    // The array keeps the previous call's contents: the error word starts at zero.
+    if (cudaMemsetAsync(scr, 0, kNoAllocScratchBytes, s) != cudaSuccess) return QA_ERR_CUDA;
     if (launch_noalloc(p, D, HPC, s) != cudaSuccess) return QA_ERR_CUDA;
     return QA_OK;
 }

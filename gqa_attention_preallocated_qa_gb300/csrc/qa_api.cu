@@ -33,8 +33,7 @@ struct qa_cache {
     __nv_bfloat16 *K = nullptr, *V = nullptr;
     int32_t *lens_dev = nullptr;
     float2 *rope = nullptr;
-    float *part_m = nullptr, *part_l = nullptr, *part_o = nullptr;
-    uint32_t *grp_cnt = nullptr, *seq_cnt = nullptr;
+    uint32_t *seq_cnt = nullptr;
     uint32_t *err = nullptr;
     CUtensorMap *dmaps = nullptr;  // device: [layer][K, V] decode tensor maps
     std::vector<int32_t> lens_host;
@@ -44,12 +43,9 @@ struct qa_cache {
 
 namespace {
 
-__global__ void qa_reset_kernel(int32_t *lens, int n_lens, uint32_t *grp_cnt, int n_grp,
-                                uint32_t *seq_cnt, int n_seq) {
+__global__ void qa_reset_kernel(int32_t *lens, int n_lens, uint32_t *seq_cnt, int n_seq) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_lens; i += gridDim.x * blockDim.x)
         lens[i] = 0;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_grp; i += gridDim.x * blockDim.x)
-        grp_cnt[i] = 0;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_seq; i += gridDim.x * blockDim.x)
         seq_cnt[i] = 0;
 }
@@ -82,10 +78,6 @@ void free_all(qa_cache *c) {
     cudaFree(c->V);
     cudaFree(c->lens_dev);
     cudaFree(c->rope);
-    cudaFree(c->part_m);
-    cudaFree(c->part_l);
-    cudaFree(c->part_o);
-    cudaFree(c->grp_cnt);
     cudaFree(c->seq_cnt);
     cudaFree(c->err);
     cudaFree(c->dmaps);
@@ -160,17 +152,8 @@ bool qa::encode_decode_map(CUtensorMap *m, void *base, int D, int capacity, int 
 namespace {
 
 int choose_splits(const qa_cache *c, int batch, int pos_max) {
-    const int nchunks = (pos_max + qa::kK3Chunk - 1) / qa::kK3Chunk;
-    const int groups = batch * c->cfg.n_kv_heads * c->HG;
-    const int resident = 2 * c->num_sms;  // the decode kernel fits two CTAs per SM
-    int S = resident / groups;            // one wave: never more CTAs than fit at once
-    S = std::min(S, std::max(1, nchunks));
-    S = std::min(S, qa::kK3MaxSplits);
-    if (S > 1) {  // equal whole-chunk shares; drop splits that would be empty
-        const int cps = (nchunks + S - 1) / S;
-        S = (nchunks + cps - 1) / cps;
-    }
-    return std::max(S, 1);
+    return qa::k3_choose_splits(c->cfg.head_dim, c->HPC, batch * c->cfg.n_kv_heads * c->HG,
+                                pos_max);
 }
 
 // Validation shared by qa_prefill and qa_prefill_transform.
@@ -297,14 +280,10 @@ QA_API qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out) {
     const int D = g.head_dim;
     c->layer_elems = static_cast<int64_t>(g.max_batch) * g.n_kv_heads * g.capacity * D;
     const size_t kv = static_cast<size_t>(c->layer_elems) * g.num_layers;
-    const size_t parts = static_cast<size_t>(g.max_batch) * g.n_q_heads * qa::kK3MaxSplits;
     uint64_t kvb = 0, scr = 0;
     bool ok = dev_alloc(&c->K, kv, kvb) && dev_alloc(&c->V, kv, kvb) &&
               dev_alloc(&c->lens_dev, static_cast<size_t>(g.num_layers) * g.max_batch, scr) &&
               dev_alloc(&c->rope, static_cast<size_t>(g.capacity) * (D / 2), scr) &&
-              dev_alloc(&c->part_m, parts, scr) && dev_alloc(&c->part_l, parts, scr) &&
-              dev_alloc(&c->part_o, parts * D, scr) &&
-              dev_alloc(&c->grp_cnt, static_cast<size_t>(g.max_batch) * g.n_kv_heads * c->HG, scr) &&
               dev_alloc(&c->seq_cnt, static_cast<size_t>(g.max_batch), scr) &&
               dev_alloc(&c->err, 1, scr);
     if (ok) {
@@ -358,9 +337,8 @@ QA_API qa_status qa_cache_reset(qa_cache *c, void *stream) {
     if (!c) return QA_ERR_INVALID_ARG;
     const qa_config &g = c->cfg;
     const int n_lens = g.num_layers * g.max_batch;
-    const int n_grp = g.max_batch * g.n_kv_heads * c->HG;
-    qa_reset_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        c->lens_dev, n_lens, c->grp_cnt, n_grp, c->seq_cnt, g.max_batch);
+    qa_reset_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(c->lens_dev, n_lens,
+                                                                       c->seq_cnt, g.max_batch);
     if (cudaGetLastError() != cudaSuccess) return QA_ERR_CUDA;
     c->launches[QA_KERNEL_RESET]++;
     std::fill(c->lens_host.begin(), c->lens_host.end(), 0);
@@ -488,10 +466,6 @@ QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q
     p.vc = c->V + layer * c->layer_elems;
     p.lens = c->lens_dev + static_cast<int64_t>(layer) * g.max_batch;
     p.rope = c->rope;
-    p.part_m = c->part_m;
-    p.part_l = c->part_l;
-    p.part_o = c->part_o;
-    p.grp_cnt = c->grp_cnt;
     p.seq_cnt = c->seq_cnt;
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.err = c->err;

@@ -58,7 +58,7 @@ struct alignas(64) K2Params {
 // ---------------------------------------------------------------- K3
 constexpr int kK3ConsumerWarps = 4;
 constexpr int kK3Chunk = 32;        // keys per pipeline chunk
-constexpr int kK3MaxSplits = 64;
+constexpr int kK3MaxSplits = 16;   // splits of one (sequence, kv head) = CTAs of one cluster
 
 struct K3Params {
     const CUtensorMap *tm_k, *tm_v;  // (D, capacity, max_batch * Hkv) over this layer's K / V
@@ -67,9 +67,7 @@ struct K3Params {
     __nv_bfloat16 *kc, *vc;          // layer base
     int32_t *lens;                   // layer base [max_batch]
     const float2 *rope;              // [cap][D/2]
-    float *part_m, *part_l, *part_o; // [B][Hq][S] / [B][Hq][S][D]
-    uint32_t *grp_cnt;               // [B][Hkv * HG]
-    uint32_t *seq_cnt;               // [B]
+    uint32_t *seq_cnt;               // [B] groups done per sequence (length update)
     __nv_bfloat16 *out;              // [B][Hq][D]
     uint32_t *err;
     int64_t seq_stride, head_stride;
@@ -89,4 +87,10 @@ bool encode_decode_map(CUtensorMap *m, void *base, int D, int capacity, int rows
 cudaError_t launch_k1(const K1Params &p, int D, cudaStream_t stream);
 cudaError_t launch_k2(const K2Params &p, int D, int nitems, cudaStream_t stream);
 cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream);
+// Number of clusters of S decode CTAs that can be resident at once on the
+// current device (cached per device, head_dim, heads per CTA and S); 0 on error.
+int k3_cluster_capacity(int D, int HPC, int S);
+// Largest split count (<= kK3MaxSplits, <= chunks) whose `groups` clusters all
+// fit on the device at once.
+int k3_choose_splits(int D, int HPC, int groups, int pos_max);
 }  // namespace qa

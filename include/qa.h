@@ -81,8 +81,9 @@ typedef struct qa_cache qa_cache; /* opaque */
 /* Allocate a cache on the current CUDA device: K and V as bf16
  * [num_layers][max_batch][n_kv_heads][capacity][head_dim] (zero-filled),
  * int32 lengths [num_layers][max_batch] (all zero), an fp32 rotary table
- * [capacity][head_dim/2] of (cos, sin) built on the host in fp64, the
- * split-KV partials of the decode kernel and an error word.  Synchronous.
+ * [capacity][head_dim/2] of (cos, sin) built on the host in fp64, the decode
+ * kernel's TMA tensor maps (two per layer) and per-sequence counters, and an
+ * error word.  Synchronous.
  * Errors: INVALID_ARG (cfg or out null, non-positive sizes),
  * UNSUPPORTED_SHAPE, CUDA (allocation failed; nothing is leaked). */
 qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out);
@@ -118,9 +119,10 @@ qa_status qa_prefill(qa_cache *cache, int layer, int batch, const int32_t *promp
  * q: [batch][Hq][D], k, v: [batch][Hkv][D], weights [D], out: [batch][Hq][D].
  * One fused launch: RMSNorm + RoPE of q and k at pos_b, append of k' and v to
  * slot pos_b, attention of every q head over slots 0..pos_b (the new token
- * attends to itself) split over the key range, log-sum-exp merge of the
- * splits, length += 1.  Positions are read from the device lengths, so the
- * step is position-agnostic on the host side.
+ * attends to itself) split over the key range (the splits of one sequence and
+ * kv head form one thread-block cluster), log-sum-exp merge of the splits in
+ * distributed shared memory, length += 1.  Positions are read from the device
+ * lengths, so the step is position-agnostic on the host side.
  * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (a sequence already holds
  * `capacity` tokens; nothing is evicted or wrapped). */
 qa_status qa_decode_step(qa_cache *cache, int layer, int batch,
@@ -191,16 +193,17 @@ int qa_decode_splits(qa_cache *cache, int layer, int batch);
  *               of this layer, caller-owned, read and appended to.
  *   q, k, v, q_norm_w, k_norm_w, out: as in qa_decode_step.
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
- * The kernel's scratch (split partials and counters) is a fixed 4 MiB array
- * in the library's device code, created on every GPU that loads the library
- * and held until the process exits.  The first call on a device looks up
- * that array's address (no allocation); make that first call before any
- * stream capture.  Every call shares the array: calls that may overlap on the
- * GPU (different streams without ordering) race and give wrong results.
- * Limits: batch <= 16 and batch * n_kv_heads * (heads-per-CTA groups) <=
- * 4096, else QA_ERR_UNSUPPORTED_SHAPE; the split count is reduced to what the
- * array can hold.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ALIGNMENT,
- * CAPACITY (a position >= capacity), CUDA. */
+ * The kernel's global scratch (its error word; the key-range splits are
+ * merged in distributed shared memory) is a fixed 256-byte array in the
+ * library's device code, created on every GPU that loads the library and held
+ * until the process exits; each call clears it first.  The first call on a
+ * device looks up that array's address (no allocation); make that first call
+ * before any stream capture.  Every call shares the array: calls that may
+ * overlap on the GPU (different streams without ordering) race on it.
+ * Limits: batch <= 16 (the per-sequence positions and rotary values travel in
+ * the kernel parameters), else QA_ERR_UNSUPPORTED_SHAPE.  Errors:
+ * INVALID_ARG, UNSUPPORTED_SHAPE, ALIGNMENT, CAPACITY (a position >=
+ * capacity), CUDA. */
 qa_status qa_decode_step_noalloc(const qa_config *cfg, int batch, const int32_t *positions,
                                  void *k_cache, void *v_cache, const void *q, const void *k,
                                  const void *v, const void *q_norm_w, const void *k_norm_w,
