@@ -49,6 +49,10 @@ __device__ __forceinline__ float k2_ex2(float x) {
     return y;
 }
 
+// The softmax rescales O only when a row's max grows by more than this many
+// powers of two (in the exp2 domain).
+constexpr float kRescaleLog2 = 8.f;
+
 // Heaviest-first work order: query blocks with more key tiles start first.
 __device__ __forceinline__ bool k2_decode_item(const K2Params &p, int idx, int &b, int &kvh,
                                                int &pair, int &qb) {
@@ -205,34 +209,39 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 mma_commit(smem_u32(&bar_kv_empty[0]));
             }
             int committed = ok ? 1 : 0;  // ring slots handed back (for the final drain)
+            // Per KV tile j and query tile t, as soon as softmax t has written P_t(j):
+            // O_t += P_t(j) V_j, then (once that has consumed P_t, which shares the
+            // S_t columns) S_t(j+1) = Q_t K_{j+1}^T.  Tile t+1 never waits for tile t's
+            // next S, so the two softmax warpgroups and the tensor pipe overlap.
             for (int j = 0; ok && j < nkv; ++j) {
                 const int iv = 2 * j + 1, sv = iv % NS;
+                const int ik = 2 * (j + 1), sk = ik % NS;
+                const bool more = j + 1 < nkv;
                 ok = mbar_wait(smem_u32(&bar_kv_full[sv]), (iv / NS) & 1, &s_abort, p.err, kKernK2, 6);
+                if (ok && more)
+                    ok = mbar_wait(smem_u32(&bar_kv_full[sk]), (ik / NS) & 1, &s_abort, p.err,
+                                   kKernK2, 8);
                 for (int t = 0; ok && t < ntiles; ++t) {
                     ok = mbar_wait(smem_u32(&bar_p[t]), j & 1, &s_abort, p.err, kKernK2, 7);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(t, sv, j > 0);
                     mma_commit(smem_u32(&bar_pv[t]));
-                }
-                if (!ok) break;
-                mma_commit(smem_u32(&bar_kv_empty[sv]));
-                ++committed;
-                if (j + 1 < nkv) {
-                    const int ik = 2 * (j + 1), sk = ik % NS;
-                    ok = mbar_wait(smem_u32(&bar_kv_full[sk]), (ik / NS) & 1, &s_abort, p.err,
-                                   kKernK2, 8);
-                    for (int t = 0; ok && t < ntiles; ++t) {
-                        // P_t(j) lives in the S_t columns: PV_t(j) must be done first.
+                    if (t == ntiles - 1) {
+                        mma_commit(smem_u32(&bar_kv_empty[sv]));
+                        ++committed;
+                    }
+                    if (more) {
                         ok = mbar_wait(smem_u32(&bar_pv[t]), j & 1, &s_abort, p.err, kKernK2, 9);
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(t, sk);
                         mma_commit(smem_u32(&bar_s[t]));
+                        if (t == ntiles - 1) {
+                            mma_commit(smem_u32(&bar_kv_empty[sk]));
+                            ++committed;
+                        }
                     }
-                    if (!ok) break;
-                    mma_commit(smem_u32(&bar_kv_empty[sk]));
-                    ++committed;
                 }
             }
             // Drain: every commit above must have arrived before the CTA exits.
@@ -249,69 +258,100 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             const uint32_t tS = tmem + (t ? Lay::kColS1 : Lay::kColS0) + lane_off;
             const uint32_t tO = tmem + (t ? Lay::kColO1 : Lay::kColO0) + lane_off;
             const float c = p.scale_log2;
-            float m = -INFINITY, l = 0.f;
+            // mref: the reference max of this row in the exp2 domain's units (raw
+            // scores).  It only moves when the row max exceeds it by more than
+            // kRescaleLog2 / c, so O is rescaled rarely; p = 2^(s*c - mref*c) then
+            // stays below 2^kRescaleLog2, and out = O / l is exact for any mref.
+            float mref = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j < nkv; ++j) {
                 ok = mbar_wait(smem_u32(&bar_s[t]), j & 1, &s_abort, p.err, kKernK2, 11);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 tc_fence_after();
-                float s[128];
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t u[32];
-                    tmem_ld32(tS + ch * 32, u);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(u[i]);
+                const bool diag = j == nkv - 1;
+                // The row of S: 4 TMEM loads in flight, one wait.
+                uint32_t sr[128];
+                {
+                    uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr);
+                    uint32_t(&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 32);
+                    uint32_t(&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 64);
+                    uint32_t(&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 96);
+                    tmem_ld32_async(tS, s0);
+                    tmem_ld32_async(tS + 32, s1);
+                    tmem_ld32_async(tS + 64, s2);
+                    tmem_ld32_async(tS + 96, s3);
+                    tmem_wait_ld4(s0, s1, s2, s3);
                 }
-                if (j == nkv - 1) {
+                if (diag) {  // keys after the row's own position are masked
 #pragma unroll
                     for (int i = 0; i < 128; ++i)
-                        if (i > r) s[i] = -INFINITY;
+                        if (i > r) sr[i] = __float_as_uint(-INFINITY);
                 }
-                // Row max and row sum with 8 independent partial chains each.
+                // Row max with 8 independent partial chains.
                 float mx8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+                for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(sr[k]);
 #pragma unroll
-                for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+                for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
                 const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-                const float m_new = fmaxf(m, mx);
-                const float neg = m_new * c;
-                const float alpha = (m == -INFINITY) ? 0.f : k2_ex2(m * c - neg);
-                float sum8[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
-#pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float p0 = k2_ex2(fmaf(s[ch * 64 + 2 * i], c, -neg));
-                        const float p1 = k2_ex2(fmaf(s[ch * 64 + 2 * i + 1], c, -neg));
-                        sum8[(2 * i) & 7] += p0;
-                        sum8[(2 * i + 1) & 7] += p1;
-                        pk[i] = pack_bf16(p0, p1);
+                // The first P.V overwrites O, so tile 0 just sets mref; later tiles move
+                // it (and rescale O by alpha, after P is written) only when it grew.
+                bool rescale = false;
+                float alpha = 1.f;
+                if (j == 0) {
+                    mref = mx;
+                } else {
+                    const bool grow = (mx - mref) * c > kRescaleLog2;
+                    rescale = __any_sync(FULL, grow);
+                    if (grow) {
+                        alpha = k2_ex2((mref - mx) * c);
+                        mref = mx;
+                        l *= alpha;
                     }
-                    tmem_st32(tS + ch * 32, pk);
                 }
-                const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                                  ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-                l = fmaf(l, alpha, sum);
-                if (j > 0 && __any_sync(FULL, m_new > m)) {
+                // p = 2^(s*c - mref*c): packed fp32x2 scale-and-subtract, then the exp
+                // unit; P is stored 32 columns at a time over the first 64 columns of S_t
+                // (all of S is already in registers).
+                const float2 c2 = make_float2(c, c);
+                const float2 n2 = make_float2(-mref * c, -mref * c);
+                float2 sum4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sum4[k] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int col = ch * 32 + 2 * i;
+                        const float2 x = __ffma2_rn(
+                            make_float2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2, n2);
+                        const float2 pv = make_float2(k2_ex2(x.x), k2_ex2(x.y));
+                        pk[i] = pack_bf16(pv.x, pv.y);
+                        sum4[i & 3] = __fadd2_rn(sum4[i & 3], pv);
+                    }
+                    tmem_st16(tS + ch * 16, pk);
+                }
+                const float2 sp = __fadd2_rn(__fadd2_rn(sum4[0], sum4[1]), __fadd2_rn(sum4[2], sum4[3]));
+                l += sp.x + sp.y;
+                if (rescale) {
                     // PV_t(j-1) is complete: S_t(j) was issued after it finished.
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
                     for (int ch = 0; ch < D / 32; ++ch) {
                         uint32_t u[32];
                         tmem_ld32(tO + ch * 32, u);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 v = __fmul2_rn(
+                                make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), a2);
+                            u[2 * i] = __float_as_uint(v.x);
+                            u[2 * i + 1] = __float_as_uint(v.y);
+                        }
                         tmem_st32(tO + ch * 32, u);
                     }
                 }
-                m = m_new;
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bar_p[t]));
