@@ -394,18 +394,28 @@ def run_e2e(args, qa, h, w, inp, stream):
             "d2h_bytes_per_step": host_out.numel() * 2, "steps": n, "host_buffers": "pinned"}
 
 
+def kernel_source_digest(kernel: str) -> str:
+    """sha256 (first 16 hex digits) over the kernel's source file and the
+    device headers it includes."""
+    import hashlib
+    csrc = os.path.join(ROOT, "gqa_attention_preallocated_qa_gb300", "csrc")
+    src = {"k3_decode": "k3_decode_splitkv.cu", "k2_prefill": "k2_prefill_tcgen05.cu",
+           "k1_norm": "k1_norm_rope_append.cu"}[kernel]
+    h = hashlib.sha256()
+    for name in (src, "qa_device.cuh", "qa_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel: str, algorithmic_bytes):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (else null)."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = {"k3_decode": "k3_decode_splitkv.cu", "k2_prefill": "k2_prefill_tcgen05.cu"}[kernel]
     try:
         with open(path) as fh:
             d = json.load(fh)[kernel]
-        with open(os.path.join(ROOT, "gqa_attention_preallocated_qa_gb300", "csrc", src), "rb") as fh:
-            digest = hashlib.sha256(fh.read()).hexdigest()[:16]
-        if d.get("source_sha256_16") != digest:
+        if d.get("source_sha256_16") != kernel_source_digest(kernel):
             return None
         return d["dram_bytes_per_launch"]
     except (OSError, KeyError, ValueError):

@@ -53,6 +53,7 @@ __device__ __forceinline__ float k2_ex2(float x) {
 // powers of two (in the exp2 domain).
 constexpr float kRescaleLog2 = 8.f;
 
+
 // Heaviest-first work order: query blocks with more key tiles start first.
 __device__ __forceinline__ bool k2_decode_item(const K2Params &p, int idx, int &b, int &kvh,
                                                int &pair, int &qb) {
@@ -210,9 +211,12 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             }
             int committed = ok ? 1 : 0;  // ring slots handed back (for the final drain)
             // Per KV tile j and query tile t, as soon as softmax t has written P_t(j):
-            // O_t += P_t(j) V_j, then (once that has consumed P_t, which shares the
-            // S_t columns) S_t(j+1) = Q_t K_{j+1}^T.  Tile t+1 never waits for tile t's
-            // next S, so the two softmax warpgroups and the tensor pipe overlap.
+            // O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T right behind it.  S_t(j+1)
+            // overwrites the TMEM columns P_t(j) sits in; tcgen05.mma operations issued
+            // by one thread execute in issue order, so P.V_t(j) has read P_t(j) before
+            // S_t(j+1) writes there, and no wait is needed between the two.  Tile t+1
+            // never waits for tile t's next S, so the two softmax warpgroups and the
+            // tensor pipe overlap.
             for (int j = 0; ok && j < nkv; ++j) {
                 const int iv = 2 * j + 1, sv = iv % NS;
                 const int ik = 2 * (j + 1), sk = ik % NS;
@@ -226,15 +230,12 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(t, sv, j > 0);
-                    mma_commit(smem_u32(&bar_pv[t]));
+                    if (!more) mma_commit(smem_u32(&bar_pv[t]));  // O_t final
                     if (t == ntiles - 1) {
                         mma_commit(smem_u32(&bar_kv_empty[sv]));
                         ++committed;
                     }
                     if (more) {
-                        ok = mbar_wait(smem_u32(&bar_pv[t]), j & 1, &s_abort, p.err, kKernK2, 9);
-                        if (!ok) break;
-                        tc_fence_after();
                         issue_s(t, sk);
                         mma_commit(smem_u32(&bar_s[t]));
                         if (t == ntiles - 1) {
@@ -336,7 +337,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 const float2 sp = __fadd2_rn(__fadd2_rn(sum4[0], sum4[1]), __fadd2_rn(sum4[2], sum4[3]));
                 l += sp.x + sp.y;
                 if (rescale) {
-                    // PV_t(j-1) is complete: S_t(j) was issued after it finished.
+                    // P.V_t(j-1) is complete: the commit that signalled S_t(j) tracks
+                    // every tcgen05 operation issued before it.
                     const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
                     for (int ch = 0; ch < D / 32; ++ch) {
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 mbar_arrive(smem_u32(&bar_p[t]));
             }
             if (ok) {
-                ok = mbar_wait(smem_u32(&bar_pv[t]), (nkv - 1) & 1, &s_abort, p.err, kKernK2, 12);
+                ok = mbar_wait(smem_u32(&bar_pv[t]), 0, &s_abort, p.err, kKernK2, 12);
                 ok = __all_sync(FULL, ok);
             }
             if (ok) {
