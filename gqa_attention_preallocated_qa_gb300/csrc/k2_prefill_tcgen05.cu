@@ -19,8 +19,8 @@
 // threads read their row of S_t with tcgen05.ld, compute p = 2^(s*c - m*c) in
 // fp32, write P as bf16 over the first 64 columns of S_t, rescale O_t when the
 // running max grew, and signal; O_t += P_t V_j reads P from TMEM and V
-// (MN-major) from smem.  The issuer waits for PV_t(j) to finish before the
-// next S_t overwrites P_t.
+// (MN-major) from smem.  S_t(j+1) is issued right behind PV_t(j) by the same
+// thread, so it overwrites P_t only after PV_t(j) has read it.
 //
 // K and V come straight out of the cache through one 3-D tensor map per
 // sequence, (D, L_b, Hkv), so rows at or past the sequence's length read as

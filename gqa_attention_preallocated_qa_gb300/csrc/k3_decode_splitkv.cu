@@ -14,10 +14,12 @@
 //      16-row tile, so the tile's unused rows cost tensor time, not memory),
 //      online softmax in fp32 on the score fragments, P reused in registers as
 //      the A operand of P V,
-//   6. CTA combine through shared memory, partial (m, l, o) to scratch; the
-//      last CTA of the group (acquire-release counter, no spinning) merges the
-//      splits in a fixed order, writes out[b][h] in bf16, and the last group of
-//      the sequence advances lens[b].
+//   6. the S split CTAs of a group form one thread-block cluster: every
+//      consumer warp pushes its partial (m, l, o) with st.async straight into
+//      the shared memory of the CTA that owns each run of outputs, counted on
+//      that CTA's receive mbarrier; each owner merges the S x 4 partials of its
+//      run in a fixed order (deterministic), writes out[b][h] in bf16, and the
+//      last group of the sequence advances lens[b] (acquire-release counter).
 // This serves the decode step of the dryft-flash-infer agent guide ("Where the
 // wins are": per-step overhead is the largest cost at batch 1 and 4, so the
 // step is one launch) against the preallocated cache of the same section.
@@ -42,24 +44,17 @@ struct K3Shape {
     static constexpr int kRingBytes = kK3Stages * kStageBytes;
     static constexpr int kNewBytes = kStageBytes;            // the new key as a one-key chunk
     static constexpr int kQBytes = (HPC * D * 2 + 15) & ~15;
-    static constexpr int kRedFloats = kK3ConsumerWarps * HPC * (D + 2);
-    static constexpr int kPartFloats = HPC * (D + 2);  // this CTA's split partial
-    static constexpr int kSmemBytes =
-        1024 + kRingBytes + kNewBytes + kQBytes + (kRedFloats + kPartFloats) * 4;
+    // Partials received from the cluster: o runs of at most ceil(HPC*D/S)+7
+    // elements and (m, l) per head, from S x kK3ConsumerWarps source warps.
+    static constexpr int kRecvFloats =
+        kK3ConsumerWarps * (HPC * D + 8 * kK3MaxSplits) + kK3ConsumerWarps * kK3MaxSplits * HPC * 2;
+    static constexpr int kSmemBytes = 1024 + kRingBytes + kNewBytes + kQBytes + kRecvFloats * 4;
 };
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// One gpu-scope acquire-release increment (publishes this CTA's earlier writes,
-// ordered by a preceding __syncthreads, and sees every earlier incrementer's).
-__device__ __forceinline__ uint32_t atomic_inc_acq_rel(uint32_t *p) {
-    uint32_t old;
-    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
-    return old;
 }
 
 __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
@@ -169,7 +164,6 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk,
     }
     l = fmaf(l, alpha, ps);
     m = m_new;
-#pragma unroll
     const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
     for (int nt = 0; nt < D / 8; ++nt) o[nt] = __fmul2_rn(o[nt], a2);
@@ -196,17 +190,24 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk,
     }
 }
 
-// The kernel body.  kHostPositions = false is the decode step of the cache
-// object: positions come from the device lengths, (cos, sin) from the
-// library's table, and the last group of each sequence advances its length.
-// kHostPositions = true is the allocation-free variant: positions and the
-// (cos, sin) of each sequence's position come in the kernel parameters
-// (pos_arr[b], cs_arr[b * D/2 + i]) and the caller keeps the lengths.
+// The kernel body.  Sequence b = b0 + blockIdx.z takes its new token at slot
+// pos[blockIdx.z] (launch parameters).  kTableRope = true is the decode step
+// of the cache object: (cos, sin) at pos from the library's table, and the
+// device length of b set to pos + 1.  kTableRope = false is the
+// allocation-free variant: (cos, sin) of each sequence's position in cs_arr
+// (cs_arr[blockIdx.z * D/2 + i]) and the caller keeps the lengths.
 // tmk / tmv: tensor maps (D, capacity, max_batch * Hkv) over this layer's K / V.
-template <int D, int HPC, bool kHostPositions>
-__device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
-                                        const float2 *cs_arr, const CUtensorMap *tmk,
-                                        const CUtensorMap *tmv) {
+//
+// Launches may overlap the tail of the previous kernel on the stream
+// (programmatic dependent launch).  Before griddepcontrol.wait the body only
+// reads what that kernel cannot be writing: its inputs (q, k, v, weights,
+// rotary table) and the cache rows below pos - 1.  A decode step writes one
+// row per sequence, its own pos, which for the next step of the same layer is
+// row pos - 1; the chunk holding it is loaded after the wait.  Every write
+// (cache slot, lengths, out) also comes after the wait.
+template <int D, int HPC, bool kTableRope>
+__device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
+                                        const CUtensorMap *tmk, const CUtensorMap *tmv) {
     using Sh = K3Shape<D, HPC>;
     constexpr int LPR = D / 8;
     constexpr int NW = kK3ConsumerWarps;
@@ -214,42 +215,53 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
     const unsigned FULL = 0xffffffffu;
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS];
+    __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_recv;
     __shared__ int s_abort;
-    __shared__ uint32_t s_seq_prev;
+    __shared__ float s_w[HPC * NW * kK3MaxSplits], s_linv[HPC];
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sRing = smem_u32(smem);
     const uint32_t sNew = sRing + Sh::kRingBytes;
     __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes + Sh::kNewBytes);
-    float *red = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kNewBytes + Sh::kQBytes);
-    float *part = red + Sh::kRedFloats;
+    float *recv = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kNewBytes + Sh::kQBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x;
     const int kvh = blockIdx.y / p.HG, hg = blockIdx.y % p.HG;
-    const int b = blockIdx.z;
+    const int bl = blockIdx.z, b = p.b0 + bl;
+    const int pos = p.pos[bl];
     const int S = p.S;
-    // Programmatic dependent launch: this grid may start while the previous
-    // step's grid drains; everything below reads what that grid wrote.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int pos = kHostPositions ? pos_arr[b] : p.lens[b];
-    if (pos < 0 || pos >= p.cap) {
-        if (threadIdx.x == 0) set_error(p.err, kErrBounds, kKernK3, 1);
-        return;
-    }
-    const int nchunks = (pos + kK3Chunk - 1) / kK3Chunk;
-    const int cps = (nchunks + S - 1) / S;
-    const int c_begin = min(split * cps, nchunks);
-    const int c_end = min(c_begin + cps, nchunks);
+
+    // Merge geometry.  The group's HPC x D outputs are dealt to the S CTAs of
+    // the cluster in runs of E (a multiple of 8); every consumer warp of every
+    // CTA (NSRC sources) sends the owner of each run its partial o for the run
+    // and (m, l) of the heads the run touches.
+    const int total = HPC * D;
+    const int NSRC = S * NW;
+    const int E = ((total + S - 1) / S + 7) & ~7;
+    const int e_lo = split * E;
+    const int E_me = max(0, min(E, total - e_lo));
+    const int g_lo = e_lo / D;
+    const int nh_me = E_me > 0 ? (e_lo + E_me - 1) / D - g_lo + 1 : 0;
+    float *rcv_o = recv;               // [NSRC][E]
+    float *rcv_ml = recv + NSRC * E;   // [NSRC][HPC][2]
+
+    // The cache chunks plus the new key (one unit, the last) are dealt to the
+    // splits in shares that differ by one at most: split `split` streams chunks
+    // [c_begin, c_end) and the last split also attends to the new key.
+    const bool pos_ok = pos >= 0 && pos < p.cap;
+    const int nchunks = pos_ok ? (pos + kK3Chunk - 1) / kK3Chunk : 0;
+    const int64_t units = nchunks + 1;
+    const int c_begin = static_cast<int>(split * units / S);
+    const int c_end = static_cast<int>(min((split + 1) * units / S, static_cast<int64_t>(nchunks)));
+    const int my_chunks = max(0, c_end - c_begin);
+    const int c_safe = pos > 0 ? (pos - 1) / kK3Chunk : 0;  // chunks below row pos - 1
     const bool owner = split == S - 1;
     const int64_t kv_base = static_cast<int64_t>(b) * p.seq_stride + kvh * p.head_stride;
     const int h_first = kvh * p.G + hg * HPC;  // first query head of this CTA
     const int tm_z = b * p.Hkv + kvh;          // (sequence, kv head) index in the tensor maps
 
-    const int my_chunks = c_end - c_begin;
     uint64_t policy = 0;
     // Stage `st` receives chunk c: K then V, each D/64 boxes of 32 rows.
     auto issue = [&](int c, int st) {
@@ -263,26 +275,34 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
                              tm_z, fb, policy);
         }
     };
+    const int first_round = min(NS, my_chunks);
+    int issued_early = 0;
     if (warp == NW && lane == 0) {
-        // The TMA thread sets up the ring and starts the first loads at once; the
-        // consumers' prologue below overlaps their latency.
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&bar_full[s]), 1);
             mbar_init(smem_u32(&bar_empty[s]), 1);
         }
+        mbar_init(smem_u32(&bar_recv), 1);
         s_abort = 0;
+        if (E_me > 0) mbar_expect_tx(smem_u32(&bar_recv), NSRC * (E_me * 4 + nh_me * 8));
         fence_mbar_init();
-        prefetch_tmap(tmk);
-        prefetch_tmap(tmv);
         policy = policy_evict_first();
-        for (int i = 0; i < min(NS, my_chunks); ++i) issue(c_begin + i, i);
+        // First loads at once, for the chunks no running kernel can be writing.
+        while (issued_early < first_round && c_begin + issued_early < c_safe) {
+            issue(c_begin + issued_early, issued_early);
+            ++issued_early;
+        }
     }
-    if (warp < NW) {
-        // ------------------------------------------------------------ consumer prologue
+    cluster_arrive();  // peers may push into this CTA once they have waited on this
+
+    // ---------------------------------------------------------------- prologue
+    // q' on the consumer warps, the new key on the producer warp of the last
+    // split; the first loads are in flight meanwhile.
+    if (pos_ok && (warp < NW || owner)) {
         const int sub = lane % LPR;
         float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims at pos
-        if constexpr (kHostPositions) {
-            const float4 *src = reinterpret_cast<const float4 *>(cs_arr + b * (D / 2) +
+        if constexpr (!kTableRope) {
+            const float4 *src = reinterpret_cast<const float4 *>(cs_arr + bl * (D / 2) +
                                                                  8 * (sub % (LPR / 2)));
 #pragma unroll
             for (int e = 0; e < 4; ++e) cs[e] = src[e];
@@ -293,31 +313,49 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
             for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + e);
         }
         // Warp w norms and rotates query head w of the CTA into shared memory.
-        if (warp < HPC) {
+        if (warp < HPC && warp < NW) {
             const uint4 qp = norm_rope_row<D>(
                 p.q + (static_cast<int64_t>(b) * p.Hq + h_first + warp) * D, p.wq, cs, p.eps, sub);
             if (lane < LPR) reinterpret_cast<uint4 *>(qs + warp * D)[sub] = qp;
         }
-        if (owner && warp == NW - 1) {
-            // The new token: k' and v as row 0 of a one-key chunk (rows 1-31 zero),
-            // and into cache slot pos for later steps.
+        if (owner && warp == NW) {
+            // The new token: k' and v as row 0 of a one-key chunk (its other rows are
+            // never read: the chunk is consumed with one key, which masks them); the
+            // copy into cache slot pos waits for the previous kernel below.
             const uint4 kp = norm_rope_row<D>(p.k + (static_cast<int64_t>(b) * p.Hkv + kvh) * D,
                                               p.wk, cs, p.eps, sub);
             const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(
                                        p.v + (static_cast<int64_t>(b) * p.Hkv + kvh) * D) +
                                    sub);
-            uint4 *nz = reinterpret_cast<uint4 *>(smem + Sh::kRingBytes);
-            for (int i = lane; i < Sh::kNewBytes / 16; i += 32) nz[i] = make_uint4(0, 0, 0, 0);
-            __syncwarp();
             if (lane < LPR) {
                 *reinterpret_cast<uint4 *>(smem + Sh::kRingBytes + swz(0, sub)) = kp;
                 *reinterpret_cast<uint4 *>(smem + Sh::kRingBytes + Sh::kTileBytes + swz(0, sub)) = vv;
-                if (hg == 0) {  // slot pos is read only by later launches
-                    reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[sub] = kp;
-                    reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[sub] = vv;
-                }
             }
         }
+    }
+
+    // Programmatic dependent launch: what follows may read or overwrite what the
+    // previous kernel on the stream wrote.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!pos_ok) {
+        if (threadIdx.x == 0) set_error(p.err, kErrBounds, kKernK3, 1);
+        return;
+    }
+    if (warp == NW && lane == 0)
+        for (int i = issued_early; i < first_round; ++i) issue(c_begin + i, i);
+    if (owner && warp == NW && hg == 0 && lane < LPR) {
+        // Slot pos of the cache, read only by later launches.
+        const uint32_t *kr = reinterpret_cast<const uint32_t *>(smem + Sh::kRingBytes + swz(0, lane));
+        const uint32_t *vr =
+            reinterpret_cast<const uint32_t *>(smem + Sh::kRingBytes + Sh::kTileBytes + swz(0, lane));
+        reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
+            make_uint4(kr[0], kr[1], kr[2], kr[3]);
+        reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
+            make_uint4(vr[0], vr[1], vr[2], vr[3]);
+    }
+    if constexpr (kTableRope) {
+        if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + 1;
     }
     __syncthreads();  // ring initialised, q' and the new key in shared memory
 
@@ -368,107 +406,89 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const int *pos_arr,
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_empty[st]));
         }
-        if (owner && warp == NW - 1)
+        if (owner && warp == my_chunks % NW)  // the new key: the warp whose turn is next
             consume_chunk<D>(sNew, sNew + Sh::kTileBytes, 1, qa0, qa2, p.scale_log2, m, l, o, z0,
                              z1, lane);
-
-        // Warp results -> shared memory: red[w][g][0..D) = o, [D] = m, [D+1] = l.
         l += __shfl_xor_sync(FULL, l, 1);
         l += __shfl_xor_sync(FULL, l, 2);
+
+        // ------------------------------------------------------------ push the partial
+        // Lane (hrow, q4) holds o[hrow][nt*8 + 2*q4 + {0,1}]; each pair goes to the
+        // CTA owning that output run, (m, l) of head hrow to every owner it touches.
+        cluster_wait();  // every peer's receive barrier is initialised
         if (real) {
-            float *dst = red + (warp * HPC + hrow) * (D + 2);
+            const int src = split * NW + warp;
+            const uint32_t a_o = smem_u32(rcv_o + src * E);
+            const uint32_t a_bar = smem_u32(&bar_recv);
 #pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt)
-                *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * q4) = o[nt];
+            for (int nt = 0; nt < D / 8; ++nt) {
+                const int e = hrow * D + nt * 8 + 2 * q4;
+                const int dst = e / E;
+                st_async_f32x2(map_rank(a_o + 4u * (e - dst * E), dst), o[nt].x, o[nt].y,
+                               map_rank(a_bar, dst));
+            }
             if (q4 == 0) {
-                dst[D] = m;
-                dst[D + 1] = l;
+                const uint32_t a_ml = smem_u32(rcv_ml + (src * HPC + hrow) * 2);
+                for (int dst = hrow * D / E; dst <= (hrow * D + D - 1) / E; ++dst)
+                    st_async_f32x2(map_rank(a_ml, dst), m, l, map_rank(a_bar, dst));
             }
-        }
-    }
-    __syncthreads();
-
-    // ---------------------------------------------------------------- CTA combine
-    // Thread t (of the 160) combines elements (g, d) of the CTA's HPC x D
-    // partial: part[g][0..D) = o, part[g][D] = m, part[g][D+1] = l.
-    for (int idx = threadIdx.x; idx < HPC * D; idx += blockDim.x) {
-        const int g = idx / D, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, red[(w * HPC + g) * (D + 2) + D]);
-        float Lsum = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float *src = red + (w * HPC + g) * (D + 2);
-                const float mw = src[D];
-                if (mw == -INFINITY) continue;
-                const float sc = ex2((mw - M) * p.scale_log2);
-                Lsum = fmaf(sc, src[D + 1], Lsum);
-                O = fmaf(sc, src[d], O);
-            }
-        }
-        part[g * (D + 2) + d] = O;
-        if (d == 0) {
-            part[g * (D + 2) + D] = M;
-            part[g * (D + 2) + D + 1] = Lsum;
         }
     }
 
-    // ---------------------------------------------------------------- split merge
-    // The S CTAs of this (sequence, kv head, head group) form one cluster.  After
-    // the barrier every CTA's partial is visible; CTA `split` merges its share of
-    // the HPC x D outputs by reading all S partials through distributed shared
-    // memory, in split order (deterministic for a given length).
-    cluster_sync();
-    if (!kHostPositions && split == 0 && threadIdx.x == 0) {
-        // Every CTA of this group has read lens[b]: count the group towards
-        // sequence b; the last group advances lens[b] below.
-        s_seq_prev = atomic_inc_acq_rel(p.seq_cnt + b);
-    }
-    {
-        const int total = HPC * D;
-        const int E = (total + S - 1) / S;
-        const int hi = min((split + 1) * E, total);
-        for (int idx = split * E + threadIdx.x; idx < hi; idx += blockDim.x) {
-            const int g = idx / D, d = idx % D;
-            const uint32_t a_m = smem_u32(part + g * (D + 2) + D);
-            const uint32_t a_o = smem_u32(part + g * (D + 2) + d);
-            float ms[kK3MaxSplits];
-            float M = -INFINITY;
+    // ---------------------------------------------------------------- merge
+    // Once every source's bytes have landed: per head, weights 2^((m_i - M) c)
+    // and 1 / sum_i w_i l_i (one warp per head); then each output of the run is
+    // the weighted sum over the sources in a fixed order (deterministic).
+    if (E_me > 0) {
+        bool ok = mbar_wait_cluster(smem_u32(&bar_recv), 0, &s_abort, p.err, kKernK3, 5);
+        ok = __syncthreads_and(ok);
+        if (!ok) return;
+        for (int hl = warp; hl < nh_me; hl += NW + 1) {
+            const int g = g_lo + hl;
+            float mi[2 * kK3MaxSplits * NW / 32], M = -INFINITY;
 #pragma unroll
-            for (int s = 0; s < kK3MaxSplits; ++s) {
-                ms[s] = s < S ? ld_cluster_f32(map_rank(a_m, s)) : -INFINITY;
-                M = fmaxf(M, ms[s]);
+            for (int k = 0; k < 2 * kK3MaxSplits * NW / 32; ++k) {
+                const int i = lane + 32 * k;
+                mi[k] = i < NSRC ? rcv_ml[(i * HPC + g) * 2] : -INFINITY;
+                M = fmaxf(M, mi[k]);
             }
-            float Lsum = 0.f, O = 0.f;
 #pragma unroll
-            for (int s = 0; s < kK3MaxSplits; ++s) {
-                if (s < S && ms[s] != -INFINITY) {
-                    const float w = ex2((ms[s] - M) * p.scale_log2);
-                    Lsum = fmaf(w, ld_cluster_f32(map_rank(a_m + 4, s)), Lsum);
-                    O = fmaf(w, ld_cluster_f32(map_rank(a_o, s)), O);
+            for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o2));
+            float Ls = 0.f;
+#pragma unroll
+            for (int k = 0; k < 2 * kK3MaxSplits * NW / 32; ++k) {
+                const int i = lane + 32 * k;
+                if (i < NSRC) {
+                    const float w = mi[k] == -INFINITY ? 0.f : ex2((mi[k] - M) * p.scale_log2);
+                    s_w[hl * NSRC + i] = w;
+                    Ls = fmaf(w, rcv_ml[(i * HPC + g) * 2 + 1], Ls);
                 }
             }
-            p.out[(static_cast<int64_t>(b) * p.Hq + h_first + g) * D + d] =
-                __float2bfloat16_rn(O / Lsum);
+#pragma unroll
+            for (int o2 = 16; o2 >= 1; o2 >>= 1) Ls += __shfl_xor_sync(FULL, Ls, o2);
+            if (lane == 0) s_linv[hl] = 1.f / Ls;
         }
-    }
-    if constexpr (!kHostPositions) {
         __syncthreads();
-        if (split == 0 && threadIdx.x == 0 &&
-            s_seq_prev == static_cast<uint32_t>(p.Hkv * p.HG) - 1u) {
-            p.lens[b] = pos + 1;
-            p.seq_cnt[b] = 0u;
+        for (int k = threadIdx.x; k < E_me; k += blockDim.x) {
+            const int e = e_lo + k, g = e / D, d = e % D, hl = g - g_lo;
+            const float *w = s_w + hl * NSRC;
+            // NSRC is a multiple of 4: four running sums, added in a fixed order.
+            float O4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i = 0; i < NSRC; i += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) O4[u] = fmaf(w[i + u], rcv_o[(i + u) * E + k], O4[u]);
+            }
+            const float O = (O4[0] + O4[1]) + (O4[2] + O4[3]);
+            p.out[(static_cast<int64_t>(b) * p.Hq + h_first + g) * D + d] =
+                __float2bfloat16_rn(O * s_linv[hl]);
         }
     }
-    cluster_sync();  // peers may still be reading this CTA's partial
 }
 
 template <int D, int HPC>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_kernel(const __grid_constant__ K3Params p) {
-    k3_body<D, HPC, false>(p, nullptr, nullptr, p.tm_k, p.tm_v);
+    k3_body<D, HPC, true>(p, nullptr, p.tm_k, p.tm_v);
 }
 
 template <int D, int HPC>
@@ -561,10 +581,6 @@ int k3_choose_splits(int D, int HPC, int groups, int pos_max) {
     int best = 1;
     for (int S = 2; S <= std::min(kK3MaxSplits, std::max(1, nchunks)); ++S)
         if (k3_cluster_capacity(D, HPC, S) >= groups) best = S;
-    if (best > 1) {  // equal whole-chunk shares; drop splits that would be empty
-        const int cps = (nchunks + best - 1) / best;
-        best = (nchunks + cps - 1) / cps;
-    }
     return best;
 }
 
@@ -595,20 +611,20 @@ namespace qa {
 
 constexpr size_t kNoAllocScratchBytes = 256;
 constexpr int kNoAllocMaxBatch = 16;
+static_assert(kNoAllocMaxBatch <= kK3MaxSeqPerLaunch, "positions travel in K3Params::pos");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 struct alignas(64) K3NoAllocParams {
     CUtensorMap tmk, tmv;              // over the caller's K / V of this layer
     float2 cs[kNoAllocMaxBatch * 64];  // (cos, sin) at pos[b] of the D/2 frequencies, [b][i]
-    int pos[kNoAllocMaxBatch];         // slot of each sequence's new token
-    K3Params base;
+    K3Params base;                     // base.pos[b]: slot of each sequence's new token
 };
 
 template <int D, int HPC>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_noalloc_kernel(const __grid_constant__ K3NoAllocParams p) {
-    k3_body<D, HPC, true>(p.base, p.pos, p.cs, &p.tmk, &p.tmv);
+    k3_body<D, HPC, false>(p.base, p.cs, &p.tmk, &p.tmv);
 }
 
 template <int D, int HPC>
@@ -728,7 +744,7 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
         !encode_decode_map(&p.tmv, v_cache, D, g.capacity, g.max_batch * g.n_kv_heads))
         return QA_ERR_CUDA;
     for (int b = 0; b < batch; ++b) {
-        p.pos[b] = positions[b];
+        p.base.pos[b] = positions[b];
         for (int i = 0; i < D / 2; ++i) {  // same fp64 formula as the cache's table
             const double a = static_cast<double>(positions[b]) *
                              std::pow(static_cast<double>(g.rope_theta), -2.0 * i / D);
@@ -749,11 +765,11 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     bp.vc = static_cast<__nv_bfloat16 *>(v_cache);
     bp.lens = nullptr;
     bp.rope = nullptr;
-    bp.seq_cnt = nullptr;
     bp.err = reinterpret_cast<uint32_t *>(scr);
     bp.out = static_cast<__nv_bfloat16 *>(out);
     bp.head_stride = static_cast<int64_t>(g.capacity) * D;
     bp.seq_stride = bp.head_stride * g.n_kv_heads;
+    bp.b0 = 0;
     bp.B = batch;
     bp.Hq = g.n_q_heads;
     bp.Hkv = g.n_kv_heads;

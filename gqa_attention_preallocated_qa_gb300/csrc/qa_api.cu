@@ -33,7 +33,6 @@ struct qa_cache {
     __nv_bfloat16 *K = nullptr, *V = nullptr;
     int32_t *lens_dev = nullptr;
     float2 *rope = nullptr;
-    uint32_t *seq_cnt = nullptr;
     uint32_t *err = nullptr;
     CUtensorMap *dmaps = nullptr;  // device: [layer][K, V] decode tensor maps
     std::vector<int32_t> lens_host;
@@ -43,11 +42,9 @@ struct qa_cache {
 
 namespace {
 
-__global__ void qa_reset_kernel(int32_t *lens, int n_lens, uint32_t *seq_cnt, int n_seq) {
+__global__ void qa_reset_kernel(int32_t *lens, int n_lens) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_lens; i += gridDim.x * blockDim.x)
         lens[i] = 0;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_seq; i += gridDim.x * blockDim.x)
-        seq_cnt[i] = 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -78,7 +75,6 @@ void free_all(qa_cache *c) {
     cudaFree(c->V);
     cudaFree(c->lens_dev);
     cudaFree(c->rope);
-    cudaFree(c->seq_cnt);
     cudaFree(c->err);
     cudaFree(c->dmaps);
 }
@@ -284,7 +280,6 @@ QA_API qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out) {
     bool ok = dev_alloc(&c->K, kv, kvb) && dev_alloc(&c->V, kv, kvb) &&
               dev_alloc(&c->lens_dev, static_cast<size_t>(g.num_layers) * g.max_batch, scr) &&
               dev_alloc(&c->rope, static_cast<size_t>(g.capacity) * (D / 2), scr) &&
-              dev_alloc(&c->seq_cnt, static_cast<size_t>(g.max_batch), scr) &&
               dev_alloc(&c->err, 1, scr);
     if (ok) {
         // Rotary table in fp64, stored as fp32 (cos, sin): angle = pos * theta^(-2i/D).
@@ -337,8 +332,7 @@ QA_API qa_status qa_cache_reset(qa_cache *c, void *stream) {
     if (!c) return QA_ERR_INVALID_ARG;
     const qa_config &g = c->cfg;
     const int n_lens = g.num_layers * g.max_batch;
-    qa_reset_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(c->lens_dev, n_lens,
-                                                                       c->seq_cnt, g.max_batch);
+    qa_reset_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(c->lens_dev, n_lens);
     if (cudaGetLastError() != cudaSuccess) return QA_ERR_CUDA;
     c->launches[QA_KERNEL_RESET]++;
     std::fill(c->lens_host.begin(), c->lens_host.end(), 0);
@@ -432,6 +426,7 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
 
 QA_API int qa_decode_splits(qa_cache *c, int layer, int batch) {
     if (check_layer(c, layer, batch) != QA_OK) return 0;
+    batch = std::min(batch, qa::kK3MaxSeqPerLaunch);  // the first launch of the step
     int pos_max = 0;
     for (int b = 0; b < batch; ++b)
         pos_max = std::max(pos_max, c->lens_host[static_cast<size_t>(layer) * c->cfg.max_batch + b]);
@@ -448,12 +443,12 @@ QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q
         !aligned16(k_norm_w) || !aligned16(out))
         return QA_ERR_ALIGNMENT;
     const qa_config &g = c->cfg;
+    // The host copy of the lengths is exact (every change goes through this
+    // library), so the positions travel in the launch parameters and the kernel
+    // never waits on reading them; the kernel still sets the device lengths.
     int32_t *mirror = c->lens_host.data() + static_cast<size_t>(layer) * g.max_batch;
-    int pos_max = 0;
-    for (int b = 0; b < batch; ++b) {
+    for (int b = 0; b < batch; ++b)
         if (mirror[b] + 1 > g.capacity) return QA_ERR_CAPACITY;
-        pos_max = std::max(pos_max, mirror[b]);
-    }
     K3Params p{};
     p.tm_k = c->dmaps + 2 * layer;
     p.tm_v = c->dmaps + 2 * layer + 1;
@@ -466,23 +461,31 @@ QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q
     p.vc = c->V + layer * c->layer_elems;
     p.lens = c->lens_dev + static_cast<int64_t>(layer) * g.max_batch;
     p.rope = c->rope;
-    p.seq_cnt = c->seq_cnt;
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.err = c->err;
     p.head_stride = static_cast<int64_t>(g.capacity) * g.head_dim;
     p.seq_stride = p.head_stride * g.n_kv_heads;
-    p.B = batch;
     p.Hq = g.n_q_heads;
     p.Hkv = g.n_kv_heads;
     p.G = c->G;
     p.HG = c->HG;
     p.cap = g.capacity;
-    p.S = choose_splits(c, batch, pos_max);
     p.eps = g.rms_eps;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.head_dim)));
-    if (qa::launch_k3(p, g.head_dim, c->HPC, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return QA_ERR_CUDA;
-    c->launches[QA_KERNEL_DECODE_ATTN]++;
+    for (int b0 = 0; b0 < batch; b0 += qa::kK3MaxSeqPerLaunch) {
+        const int nb = std::min(qa::kK3MaxSeqPerLaunch, batch - b0);
+        int pos_max = 0;
+        for (int i = 0; i < nb; ++i) {
+            p.pos[i] = mirror[b0 + i];
+            pos_max = std::max(pos_max, mirror[b0 + i]);
+        }
+        p.b0 = b0;
+        p.B = nb;
+        p.S = choose_splits(c, nb, pos_max);
+        if (qa::launch_k3(p, g.head_dim, c->HPC, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return QA_ERR_CUDA;
+        c->launches[QA_KERNEL_DECODE_ATTN]++;
+    }
     for (int b = 0; b < batch; ++b) mirror[b] += 1;
     return QA_OK;
 }

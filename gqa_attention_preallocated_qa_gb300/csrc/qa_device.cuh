@@ -86,6 +86,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Bounded wait with cluster-scope acquire: for data that other CTAs of the
+// cluster wrote into this CTA's shared memory with st.async.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                  uint32_t *err, uint32_t kernel, uint32_t site) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t spin = 0;; ++spin) {
+        uint32_t ok;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            "selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((spin & 63u) == 63u) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitTimeoutNs) {
+                *abort = 1;
+                set_error(err, kErrTimeout, kernel, site);
+                return false;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 // Contiguous global -> shared copy completing on an mbarrier (16-byte aligned,
 // size a multiple of 16).
@@ -163,21 +188,29 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // ------------------------------------------------------------------ clusters
 // Every thread of every CTA of the cluster arrives; shared-memory writes made
 // before it are visible to all CTAs of the cluster after it.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile(
-        "barrier.cluster.arrive.release.aligned;\n"
-        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Split cluster barrier: arrive (releasing this thread's earlier writes, e.g.
+// mbarrier initialisation) and, later, wait for every thread of the cluster.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 // The shared::cluster address of the same variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_rank(uint32_t smem_addr, uint32_t rank) {
     uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+// Asynchronous 8-byte store into another CTA's shared memory (both addresses
+// from map_rank); its bytes count towards the transaction count of `bar`,
+// an mbarrier in the destination CTA.
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+            addr),
+        "f"(a), "f"(b), "r"(bar)
+        : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05

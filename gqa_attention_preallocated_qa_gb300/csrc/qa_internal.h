@@ -59,20 +59,22 @@ struct alignas(64) K2Params {
 constexpr int kK3ConsumerWarps = 4;
 constexpr int kK3Chunk = 32;        // keys per pipeline chunk
 constexpr int kK3MaxSplits = 16;   // splits of one (sequence, kv head) = CTAs of one cluster
+constexpr int kK3MaxSeqPerLaunch = 64;  // positions carried in one launch's parameters
 
 struct K3Params {
     const CUtensorMap *tm_k, *tm_v;  // (D, capacity, max_batch * Hkv) over this layer's K / V
-    const __nv_bfloat16 *q, *k, *v;  // [B][Hq][D], [B][Hkv][D]
+    const __nv_bfloat16 *q, *k, *v;  // [batch][Hq][D], [batch][Hkv][D] (whole call)
     const __nv_bfloat16 *wq, *wk;
     __nv_bfloat16 *kc, *vc;          // layer base
-    int32_t *lens;                   // layer base [max_batch]
+    int32_t *lens;                   // layer base [max_batch]: set to pos + 1 (null: not kept)
     const float2 *rope;              // [cap][D/2]
-    uint32_t *seq_cnt;               // [B] groups done per sequence (length update)
-    __nv_bfloat16 *out;              // [B][Hq][D]
+    __nv_bfloat16 *out;              // [batch][Hq][D]
     uint32_t *err;
     int64_t seq_stride, head_stride;
     int B, Hq, Hkv, G, HG, cap, S;
     float eps, scale_log2;
+    int b0;                          // first sequence of this launch (blockIdx.z = b - b0)
+    int pos[kK3MaxSeqPerLaunch];     // slot of each launched sequence's new token
 };
 
 }  // namespace qa

@@ -121,8 +121,13 @@ qa_status qa_prefill(qa_cache *cache, int layer, int batch, const int32_t *promp
  * slot pos_b, attention of every q head over slots 0..pos_b (the new token
  * attends to itself) split over the key range (the splits of one sequence and
  * kv head form one thread-block cluster), log-sum-exp merge of the splits in
- * distributed shared memory, length += 1.  Positions are read from the device
- * lengths, so the step is position-agnostic on the host side.
+ * distributed shared memory, length += 1 (host copy and device lengths).
+ * Positions come from the cache's host copy of the lengths and travel in the
+ * launch parameters (one launch per 64 sequences).  Launches may overlap the
+ * previous kernel on the stream (programmatic dependent launch): the step
+ * reads q, k, v and the weights before that kernel has finished, so they must
+ * not be written by the immediately preceding decode step (its out buffer in
+ * particular must not be this step's q, k or v).
  * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (a sequence already holds
  * `capacity` tokens; nothing is evicted or wrapped). */
 qa_status qa_decode_step(qa_cache *cache, int layer, int batch,
@@ -163,12 +168,13 @@ qa_status qa_get_device_error(qa_cache *cache, uint32_t *detail);
  * kernels ran (the launch-counter check of the pegainfer PR #862 review). */
 qa_status qa_stats(qa_cache *cache, uint64_t launches[QA_NUM_KERNELS]);
 
-/* Bytes of device memory the cache owns: K+V, and scratch (decode partials,
- * counters, rotary table). */
+/* Bytes of device memory the cache owns: K+V, and scratch (device lengths,
+ * rotary table, error word). */
 qa_status qa_memory_info(qa_cache *cache, uint64_t *kv_bytes, uint64_t *scratch_bytes);
 
 /* Number of key-range splits the decode kernel will use for the current
- * lengths of `layer` and `batch` sequences (a pure host computation). */
+ * lengths of `layer` and `batch` sequences (a pure host computation; a step
+ * launches one kernel per 64 sequences, and this is the first one's count). */
 int qa_decode_splits(qa_cache *cache, int layer, int batch);
 
 /* ---- allocation-free decode step ----------------------------------------
