@@ -34,7 +34,20 @@
 
 namespace qa {
 
-constexpr int kK3Stages = 4;
+constexpr int kK3Stages = kK3ConsumerWarps;  // one stage per consumer warp
+
+// Floats a CTA receives in the split merge, maximised over the split count S:
+// from each of S x kK3ConsumerWarps source warps, an o run of E elements (E a
+// multiple of 8) and (m, l) of every head.
+constexpr int k3_recv_floats(int total, int hpc) {
+    int best = 0;
+    for (int S = 1; S <= kK3MaxSplits; ++S) {
+        const int E = ((total + S - 1) / S + 7) & ~7;
+        const int f = S * kK3ConsumerWarps * (E + 2 * hpc);
+        best = f > best ? f : best;
+    }
+    return best;
+}
 
 template <int D, int HPC>
 struct K3Shape {
@@ -42,13 +55,9 @@ struct K3Shape {
     static constexpr int kTileBytes = (D / 64) * kBoxBytes;  // K (or V) of one chunk
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kK3Stages * kStageBytes;
-    static constexpr int kNewBytes = kStageBytes;            // the new key as a one-key chunk
     static constexpr int kQBytes = (HPC * D * 2 + 15) & ~15;
-    // Partials received from the cluster: o runs of at most ceil(HPC*D/S)+7
-    // elements and (m, l) per head, from S x kK3ConsumerWarps source warps.
-    static constexpr int kRecvFloats =
-        kK3ConsumerWarps * (HPC * D + 8 * kK3MaxSplits) + kK3ConsumerWarps * kK3MaxSplits * HPC * 2;
-    static constexpr int kSmemBytes = 1024 + kRingBytes + kNewBytes + kQBytes + kRecvFloats * 4;
+    static constexpr int kRecvFloats = k3_recv_floats(HPC * D, HPC);
+    static constexpr int kSmemBytes = 1024 + kRingBytes + kQBytes + kRecvFloats * 4;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -217,14 +226,14 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_recv;
     __shared__ int s_abort;
-    __shared__ float s_w[HPC * NW * kK3MaxSplits], s_linv[HPC];
+    __shared__ __align__(16) __nv_bfloat16 s_newk[D], s_newv[D];  // k', v of the new token
+    __shared__ float s_w[HPC * kK3MaxSplits * NW], s_linv[HPC];     // merge weights
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sRing = smem_u32(smem);
-    const uint32_t sNew = sRing + Sh::kRingBytes;
-    __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes + Sh::kNewBytes);
-    float *recv = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kNewBytes + Sh::kQBytes);
+    __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes);
+    float *recv = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kQBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x;
@@ -319,17 +328,16 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             if (lane < LPR) reinterpret_cast<uint4 *>(qs + warp * D)[sub] = qp;
         }
         if (owner && warp == NW) {
-            // The new token: k' and v as row 0 of a one-key chunk (its other rows are
-            // never read: the chunk is consumed with one key, which masks them); the
-            // copy into cache slot pos waits for the previous kernel below.
+            // The new token: k' and v into shared memory; the copy into cache slot
+            // pos waits for the previous kernel below.
             const uint4 kp = norm_rope_row<D>(p.k + (static_cast<int64_t>(b) * p.Hkv + kvh) * D,
                                               p.wk, cs, p.eps, sub);
             const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(
                                        p.v + (static_cast<int64_t>(b) * p.Hkv + kvh) * D) +
                                    sub);
             if (lane < LPR) {
-                *reinterpret_cast<uint4 *>(smem + Sh::kRingBytes + swz(0, sub)) = kp;
-                *reinterpret_cast<uint4 *>(smem + Sh::kRingBytes + Sh::kTileBytes + swz(0, sub)) = vv;
+                reinterpret_cast<uint4 *>(s_newk)[sub] = kp;
+                reinterpret_cast<uint4 *>(s_newv)[sub] = vv;
             }
         }
     }
@@ -346,13 +354,10 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         for (int i = issued_early; i < first_round; ++i) issue(c_begin + i, i);
     if (owner && warp == NW && hg == 0 && lane < LPR) {
         // Slot pos of the cache, read only by later launches.
-        const uint32_t *kr = reinterpret_cast<const uint32_t *>(smem + Sh::kRingBytes + swz(0, lane));
-        const uint32_t *vr =
-            reinterpret_cast<const uint32_t *>(smem + Sh::kRingBytes + Sh::kTileBytes + swz(0, lane));
         reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
-            make_uint4(kr[0], kr[1], kr[2], kr[3]);
+            reinterpret_cast<const uint4 *>(s_newk)[lane];
         reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
-            make_uint4(vr[0], vr[1], vr[2], vr[3]);
+            reinterpret_cast<const uint4 *>(s_newv)[lane];
     }
     if constexpr (kTableRope) {
         if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + 1;
@@ -406,9 +411,35 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_empty[st]));
         }
-        if (owner && warp == my_chunks % NW)  // the new key: the warp whose turn is next
-            consume_chunk<D>(sNew, sNew + Sh::kTileBytes, 1, qa0, qa2, p.scale_log2, m, l, o, z0,
-                             z1, lane);
+        if (owner && warp == my_chunks % NW) {
+            // The new key, on the warp whose turn is next: s = q'.k' (the 4 lanes of a
+            // head split the dims), then the online-softmax update of the lane's o.
+            const float c = p.scale_log2;
+            float sd = 0.f;
+            if (real) {
+                const __nv_bfloat162 *qh =
+                    reinterpret_cast<const __nv_bfloat162 *>(qs + hrow * D) + q4 * (D / 8);
+                const __nv_bfloat162 *kh = reinterpret_cast<const __nv_bfloat162 *>(s_newk) + q4 * (D / 8);
+#pragma unroll
+                for (int i = 0; i < D / 8; ++i) {
+                    const float2 a = __bfloat1622float2(qh[i]), kk = __bfloat1622float2(kh[i]);
+                    sd = fmaf(a.x, kk.x, fmaf(a.y, kk.y, sd));
+                }
+            }
+            sd += __shfl_xor_sync(FULL, sd, 1);
+            sd += __shfl_xor_sync(FULL, sd, 2);
+            const float m_new = fmaxf(m, sd);
+            const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * c);
+            const float pn = ex2((sd - m_new) * c);
+            l = fmaf(l, alpha, q4 == 0 ? pn : 0.f);  // l is summed over the quad below
+            m = m_new;
+            const __nv_bfloat162 *vh = reinterpret_cast<const __nv_bfloat162 *>(s_newv);
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                const float2 vv = __bfloat1622float2(vh[nt * 4 + q4]);
+                o[nt] = make_float2(fmaf(pn, vv.x, o[nt].x * alpha), fmaf(pn, vv.y, o[nt].y * alpha));
+            }
+        }
         l += __shfl_xor_sync(FULL, l, 1);
         l += __shfl_xor_sync(FULL, l, 2);
 
@@ -436,32 +467,35 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     }
 
     // ---------------------------------------------------------------- merge
-    // Once every source's bytes have landed: per head, weights 2^((m_i - M) c)
-    // and 1 / sum_i w_i l_i (one warp per head); then each output of the run is
-    // the weighted sum over the sources in a fixed order (deterministic).
+    // Once every source's bytes have landed: per head of the run (one warp
+    // each), w_i = 2^((m_i - M) c) with M = max_i m_i and 1 / sum_i w_i l_i;
+    // then each output of the run is sum_i w_i o_i times that, over the sources
+    // in a fixed order (deterministic).
     if (E_me > 0) {
         bool ok = mbar_wait_cluster(smem_u32(&bar_recv), 0, &s_abort, p.err, kKernK3, 5);
         ok = __syncthreads_and(ok);
         if (!ok) return;
+        const float c = p.scale_log2;
+        constexpr int kPerLane = (kK3MaxSplits * NW + 31) / 32;
         for (int hl = warp; hl < nh_me; hl += NW + 1) {
-            const int g = g_lo + hl;
-            float mi[2 * kK3MaxSplits * NW / 32], M = -INFINITY;
+            const float *ml = rcv_ml + 2 * (g_lo + hl);  // source i: ml[2 * HPC * i], l after it
+            float mi[kPerLane], M = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < 2 * kK3MaxSplits * NW / 32; ++k) {
+            for (int k = 0; k < kPerLane; ++k) {
                 const int i = lane + 32 * k;
-                mi[k] = i < NSRC ? rcv_ml[(i * HPC + g) * 2] : -INFINITY;
+                mi[k] = i < NSRC ? ml[2 * HPC * i] : -INFINITY;
                 M = fmaxf(M, mi[k]);
             }
 #pragma unroll
             for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o2));
             float Ls = 0.f;
 #pragma unroll
-            for (int k = 0; k < 2 * kK3MaxSplits * NW / 32; ++k) {
+            for (int k = 0; k < kPerLane; ++k) {
                 const int i = lane + 32 * k;
                 if (i < NSRC) {
-                    const float w = mi[k] == -INFINITY ? 0.f : ex2((mi[k] - M) * p.scale_log2);
-                    s_w[hl * NSRC + i] = w;
-                    Ls = fmaf(w, rcv_ml[(i * HPC + g) * 2 + 1], Ls);
+                    const float w = mi[k] == -INFINITY ? 0.f : ex2((mi[k] - M) * c);
+                    s_w[hl * kK3MaxSplits * NW + i] = w;
+                    Ls = fmaf(w, ml[2 * HPC * i + 1], Ls);
                 }
             }
 #pragma unroll
@@ -471,13 +505,15 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         __syncthreads();
         for (int k = threadIdx.x; k < E_me; k += blockDim.x) {
             const int e = e_lo + k, g = e / D, d = e % D, hl = g - g_lo;
-            const float *w = s_w + hl * NSRC;
-            // NSRC is a multiple of 4: four running sums, added in a fixed order.
-            float O4[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int i = 0; i < NSRC; i += 4) {
+            const float *w = s_w + hl * kK3MaxSplits * NW;
+            const float *src = rcv_o + k;
+            float O4[4] = {0.f, 0.f, 0.f, 0.f};  // four running sums, added in a fixed order
+            int i = 0;
+            for (; i + 4 <= NSRC; i += 4) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) O4[u] = fmaf(w[i + u], rcv_o[(i + u) * E + k], O4[u]);
+                for (int u = 0; u < 4; ++u) O4[u] = fmaf(w[i + u], src[(i + u) * E], O4[u]);
             }
+            for (; i < NSRC; ++i) O4[0] = fmaf(w[i], src[i * E], O4[0]);
             const float O = (O4[0] + O4[1]) + (O4[2] + O4[3]);
             p.out[(static_cast<int64_t>(b) * p.Hq + h_first + g) * D + d] =
                 __float2bfloat16_rn(O * s_linv[hl]);

@@ -56,7 +56,7 @@ struct alignas(64) K2Params {
 };
 
 // ---------------------------------------------------------------- K3
-constexpr int kK3ConsumerWarps = 4;
+constexpr int kK3ConsumerWarps = 5;
 constexpr int kK3Chunk = 32;        // keys per pipeline chunk
 constexpr int kK3MaxSplits = 16;   // splits of one (sequence, kv head) = CTAs of one cluster
 constexpr int kK3MaxSeqPerLaunch = 64;  // positions carried in one launch's parameters
