@@ -424,11 +424,16 @@ def traffic_for(kernel: str, algorithmic_bytes):
 
 # ---------------------------------------------------------------- decode sweep
 def run_sweep(args):
-    """Decode-only sweep (batch 1 and 4, cache lengths 512 to 16384): the cache
-    holds L raw N(0,1) keys/values per sequence, then `--steps` decode steps
-    run back to back (the length grows by one per step; bytes are counted
-    exactly).  One JSON line per point: mean µs per step and HBM GB/s of the
-    K/V read (events around the whole loop: launch gaps included)."""
+    """Decode-only sweep (batch 1 and 4, cache lengths 512 to 16384).  Each
+    point allocates NL layer caches, NL large enough that together they hold
+    at least 3x the L2 (129 MB), every one filled with L raw N(0,1) keys/values
+    per sequence; the timed `--sweep-steps` decode steps cycle through the
+    layers (step s decodes layer s mod NL, as a model's layer loop does), so
+    each step reads its layer's K/V from HBM, not from L2.  The length of a
+    layer grows by one per visit; bytes are counted exactly.  One JSON line per
+    point: mean µs per step, K/V bytes per step and HBM GB/s (events around the
+    whole loop: launch gaps included); `same_layer_us_per_step` repeats the
+    measurement on a single layer (its cache can stay in L2 when small)."""
     import numpy as np
     import torch
 
@@ -436,18 +441,26 @@ def run_sweep(args):
     from gqa_attention_preallocated_qa_gb300.configs import DECODE_SWEEP
 
     pk = peaks()
+    l2_bytes = 129 * 1000 * 1000
+    steps = args.sweep_steps
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
     for pt in DECODE_SWEEP:
         inp = pt.inputs()
-        steps = args.steps
-        cap = pt.L + steps + args.warmup
-        h = qa.qa_cache_alloc(1, pt.B, pt.Hq, pt.Hkv, pt.D, cap, pt.theta, pt.eps)
-        K, V, _ = qa.cache_tensors(h, 0, pt.B, pt.Hkv, cap, pt.D)
-
-        def dev(a):
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(
-                torch.bfloat16)
-        K[:, :, :pt.L] = dev(inp.cache_k)
-        V[:, :, :pt.L] = dev(inp.cache_v)
+        layer_bytes = pt.B * pt.Hkv * pt.L * pt.D * 4
+        NL = max(1, min(256, -(-3 * l2_bytes // layer_bytes)))
+        visits = -(-(steps + args.warmup) // NL) + args.warmup + 1
+        same_steps = 200
+        cap = pt.L + visits + same_steps
+        h = qa.qa_cache_alloc(NL, pt.B, pt.Hq, pt.Hkv, pt.D, cap, pt.theta, pt.eps)
+        ck, cv = dev(inp.cache_k), dev(inp.cache_v)
+        for layer in range(NL):
+            K, V, _ = qa.cache_tensors(h, layer, pt.B, pt.Hkv, cap, pt.D)
+            K[:, :, :pt.L] = ck
+            V[:, :, :pt.L] = cv
+            qa.qa_cache_set_lengths(h, layer, [pt.L] * pt.B)
         q, k, v, wq, wk = (dev(a) for a in (inp.dq[0], inp.dk[0], inp.dv[0], inp.wq, inp.wk))
         out = torch.empty_like(q)
         stream = torch.cuda.current_stream()
@@ -455,28 +468,44 @@ def run_sweep(args):
         lib = qa.lib
         args_c = (q.data_ptr(), k.data_ptr(), v.data_ptr(), wq.data_ptr(), wk.data_ptr(),
                   out.data_ptr())
-        qa.qa_cache_set_lengths(h, 0, [pt.L] * pt.B)
-        for _ in range(args.warmup):
-            lib.qa_decode_step(h, 0, pt.B, *args_c, sh)
-        start = pt.L + args.warmup
+        lens = [pt.L] * NL
+        st = 0
+        for i in range(args.warmup):
+            st |= lib.qa_decode_step(h, i % NL, pt.B, *args_c, sh)
+            lens[i % NL] += 1
         splits = qa.qa_decode_splits(h, 0, pt.B)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        byts = 0
         torch.cuda.synchronize()
         e0.record(stream)
-        st = 0
-        for _ in range(steps):
-            st |= lib.qa_decode_step(h, 0, pt.B, *args_c, sh)
+        for i in range(steps):
+            layer = (args.warmup + i) % NL
+            st |= lib.qa_decode_step(h, layer, pt.B, *args_c, sh)
+            lens[layer] += 1
+            byts += pt.B * pt.Hkv * lens[layer] * pt.D * 4  # keys 0..pos, K and V
         e1.record(stream)
         torch.cuda.synchronize()
         if st or qa.qa_get_device_error(h)[0]:
             raise RuntimeError(f"decode sweep point {pt.name} failed")
         us = e0.elapsed_time(e1) * 1e3 / steps
-        byts = sum(pt.B * pt.Hkv * (start + s + 1) * pt.D * 4 for s in range(steps)) / steps
+        byts /= steps
         gbs = byts / (us * 1e-6) / 1e9
-        print(json.dumps({"sweep": pt.name, "B": pt.B, "L": pt.L, "steps": steps,
+        # the same on one layer, for reference (its K/V may stay in L2)
+        n1 = same_steps
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(n1):
+            st |= lib.qa_decode_step(h, 0, pt.B, *args_c, sh)
+        e3.record(stream)
+        torch.cuda.synchronize()
+        if st or qa.qa_get_device_error(h)[0]:
+            raise RuntimeError(f"decode sweep point {pt.name} failed")
+        print(json.dumps({"sweep": pt.name, "B": pt.B, "L": pt.L, "steps": steps, "layers": NL,
                           "splits": splits, "us_per_step": round(us, 3),
                           "kv_bytes_per_step": round(byts), "hbm_gbs": round(gbs, 1),
-                          "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4)}), flush=True)
+                          "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
+                          "same_layer_us_per_step": round(e2.elapsed_time(e3) * 1e3 / max(1, n1), 3),
+                          "same_layer_steps": n1}), flush=True)
         qa.qa_cache_free(h)
 
 
@@ -552,6 +581,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="decode-only sweep over batch 1/4 and cache lengths 512..16384")
+    ap.add_argument("--sweep-steps", type=int, default=1000,
+                    help="timed decode steps per sweep point")
     ap.add_argument("--profile-case", action="store_true",
                     help="run one small prefill + 4 decode steps (for ncu) and exit")
     args = ap.parse_args()
