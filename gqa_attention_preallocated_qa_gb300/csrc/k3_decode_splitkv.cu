@@ -34,7 +34,7 @@
 
 namespace qa {
 
-constexpr int kK3Stages = kK3ConsumerWarps;  // one stage per consumer warp
+constexpr int kK3Stages = kK3ConsumerWarps;  // one ring stage per consumer warp
 
 // Floats a CTA receives in the split merge, maximised over the split count S:
 // from each of S x kK3ConsumerWarps source warps, an o run of E elements (E a
