@@ -179,25 +179,31 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 
             // S_t = Q_t K^T: K-major A and B, 128-byte swizzle, 8-row groups 1024 B apart;
             // K-step k of 16 elements = 32 bytes inside the 128-byte row of box k/4.
+            // Descriptors are built once per operand tile; a K-step only moves the
+            // start address (bits 0-13, in 16-byte units, never carrying out at
+            // shared-memory addresses), so it is one 32-bit add on the low word.
+            auto desc_at = [](uint64_t base, uint32_t byte_off) -> uint64_t {
+                return (base & 0xFFFFFFFF00000000ull) |
+                       static_cast<uint32_t>(static_cast<uint32_t>(base) + (byte_off >> 4));
+            };
+            const uint64_t dQ[2] = {sdesc_sw128(sQ, 16, 1024), sdesc_sw128(sQ + Lay::kTileBytes, 16, 1024)};
             auto issue_s = [&](int t, int st) {
-                const uint32_t qa = sQ + t * Lay::kTileBytes;
-                const uint32_t ka = sKV + st * Lay::kTileBytes;
+                const uint64_t dK = sdesc_sw128(sKV + st * Lay::kTileBytes, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k / 4) * Lay::kBoxBytes + (k % 4) * 32;
-                    mma_ss(tS[t], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                           idesc_qk, k > 0 ? 1u : 0u);
+                    mma_ss(tS[t], desc_at(dQ[t], off), desc_at(dK, off), idesc_qk, k > 0 ? 1u : 0u);
                 }
             };
             // O_t += P_t V: P (bf16, 2 per column) from TMEM, V MN-major in smem:
             // 64-wide d blocks one box (16 KB) apart, 8-row key groups 1024 B apart;
             // K-step k of 16 keys = 16 rows = 2048 bytes.
             auto issue_pv = [&](int t, int st, bool acc) {
-                const uint32_t va = sKV + st * Lay::kTileBytes;
+                const uint64_t dV = sdesc_sw128(sKV + st * Lay::kTileBytes, Lay::kBoxBytes, 1024);
 #pragma unroll
                 for (int k = 0; k < 128 / 16; ++k)
-                    mma_ts(tO[t], tS[t] + k * 8, sdesc_sw128(va + k * 2048, Lay::kBoxBytes, 1024),
-                           idesc_pv, (acc || k > 0) ? 1u : 0u);
+                    mma_ts(tO[t], tS[t] + k * 8, desc_at(dV, k * 2048), idesc_pv,
+                           (acc || k > 0) ? 1u : 0u);
             };
 
             if (ok) ok = mbar_wait(smem_u32(&bar_kv_full[0]), 0, &s_abort, p.err, kKernK2, 5);
