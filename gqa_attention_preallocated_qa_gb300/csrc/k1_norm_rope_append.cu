@@ -46,11 +46,12 @@ __global__ void __launch_bounds__(256) k1_norm_rope_append_kernel(const __grid_c
     const int64_t t = tok_valid ? t0 : 0;
     int b = 0;
     while (b + 1 < p.nseq && t >= p.cu[b + 1]) ++b;
-    const int pos = static_cast<int>(t - p.cu[b]);
+    const int pos = p.start[b] + static_cast<int>(t - p.cu[b]);
     const int64_t slot = static_cast<int64_t>(p.seq_slot0 + b) * p.seq_stride;
 
     if (blockIdx.x == 0 && threadIdx.x < p.nseq)
-        p.lens[p.seq_slot0 + threadIdx.x] = p.cu[threadIdx.x + 1] - p.cu[threadIdx.x];
+        p.lens[p.seq_slot0 + threadIdx.x] =
+            p.start[threadIdx.x] + p.cu[threadIdx.x + 1] - p.cu[threadIdx.x];
     if (tok_valid && pos >= p.cap)  // cannot happen after host validation; never write out of bounds
         set_error(p.err, kErrBounds, kKernK1, 1);
     const bool tok_active = tok_valid && pos < p.cap;

@@ -107,8 +107,13 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     if (!k2_decode_item(p, blockIdx.x, b, kvh, pair, qb)) return;  // uniform per CTA
     const bool two = 2 * pair + 1 < p.G;
     const int h0 = kvh * p.G + 2 * pair;
-    const int nkv = qb + 1;  // key tiles 0..qb; tile qb is the diagonal
     const int L = p.len[b];
+    // Query row r of the block is new token qb*128 + r at position qmin + r; it
+    // sees keys 0..qmin + r.  Key tiles 0..nkv-1 reach the block's last visible
+    // key; tiles from jmask on may hold keys past a row's position.
+    const int qmin = p.start[b] + qb * 128;
+    const int nkv = (qmin + min(127, L - 1 - qb * 128)) / 128 + 1;
+    const int jmask = qmin / 128;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bar_q), 1);
@@ -265,6 +270,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             const uint32_t tS = tmem + (t ? Lay::kColS1 : Lay::kColS0) + lane_off;
             const uint32_t tO = tmem + (t ? Lay::kColO1 : Lay::kColO0) + lane_off;
             const float c = p.scale_log2;
+            const int qpos = qmin + r;  // this row's position
             // mref: the reference max of this row in the exp2 domain's units (raw
             // scores).  It only moves when the row max exceeds it by more than
             // kRescaleLog2 / c, so O is rescaled rarely; p = 2^(s*c - mref*c) then
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 tc_fence_after();
-                const bool diag = j == nkv - 1;
+                const int thr = qpos - j * 128;  // last visible key index in tile j
                 // The row of S: 4 TMEM loads in flight, one wait.
                 uint32_t sr[128];
                 {
@@ -290,10 +296,10 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                     tmem_ld32_async(tS + 96, s3);
                     tmem_wait_ld4(s0, s1, s2, s3);
                 }
-                if (diag) {  // keys after the row's own position are masked
+                if (j >= jmask) {  // keys after the row's own position are masked
 #pragma unroll
                     for (int i = 0; i < 128; ++i)
-                        if (i > r) sr[i] = __float_as_uint(-INFINITY);
+                        if (i > thr) sr[i] = __float_as_uint(-INFINITY);
                 }
                 // Row max with 8 independent partial chains.
                 float mx8[8];
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             if (ok) {
                 tc_fence_after();
                 const float inv = 1.f / l;
-                const int row = qb * 128 + r;
+                const int row = qb * 128 + r;  // new token index within the sequence
                 const bool valid = row < L;
                 __nv_bfloat16 *dst =
                     p.out + (static_cast<int64_t>(p.cu[b] + row) * p.Hq + h0 + t) * D;

@@ -159,14 +159,15 @@ qa_status check_prefill(const qa_cache *c, int layer, int batch, const int32_t *
     qa_status st = check_layer(c, layer, batch);
     if (st != QA_OK) return st;
     if (!prompt_lens) return QA_ERR_INVALID_ARG;
+    // The new tokens of sequence b take positions len_b .. len_b + prompt_lens[b] - 1
+    // after what the layer already holds (a chunked prefill appends).
+    const int32_t *cur = c->lens_host.data() + static_cast<size_t>(layer) * c->cfg.max_batch;
     int64_t T = 0;
     for (int b = 0; b < batch; ++b) {
         if (prompt_lens[b] < 0) return QA_ERR_INVALID_ARG;
-        if (prompt_lens[b] > c->cfg.capacity) return QA_ERR_CAPACITY;
+        if (static_cast<int64_t>(cur[b]) + prompt_lens[b] > c->cfg.capacity) return QA_ERR_CAPACITY;
         T += prompt_lens[b];
     }
-    for (int b = 0; b < batch; ++b)
-        if (c->lens_host[static_cast<size_t>(layer) * c->cfg.max_batch + b] != 0) return QA_ERR_STATE;
     if (T > 0) {
         if (!q || !k || !v || !wq || !wk || !dst) return QA_ERR_INVALID_ARG;
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(wq) || !aligned16(wk) ||
@@ -218,7 +219,11 @@ qa_status run_k1(qa_cache *c, int layer, int batch, const int32_t *lens, const v
         p.nseq = n;
         p.seq_slot0 = s0;
         p.cu[0] = 0;
-        for (int i = 0; i < n; ++i) p.cu[i + 1] = p.cu[i] + lens[s0 + i];
+        const int32_t *cur = c->lens_host.data() + static_cast<size_t>(layer) * g.max_batch;
+        for (int i = 0; i < n; ++i) {
+            p.cu[i + 1] = p.cu[i] + lens[s0 + i];
+            p.start[i] = cur[s0 + i];
+        }
         p.T = p.cu[n];
         if (p.T > 0) {
             if (qa::launch_k1(p, D, s) != cudaSuccess) return QA_ERR_CUDA;
@@ -242,7 +247,7 @@ QA_API const char *qa_status_str(qa_status s) {
         case QA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
         case QA_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
         case QA_ERR_CAPACITY: return "cache capacity exceeded";
-        case QA_ERR_STATE: return "layer already holds tokens";
+        case QA_ERR_STATE: return "invalid cache state";
         case QA_ERR_CUDA: return "CUDA runtime error";
         case QA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
         case QA_ERR_DEVICE_BOUNDS: return "device position out of bounds";
@@ -351,7 +356,7 @@ QA_API qa_status qa_prefill_transform(qa_cache *c, int layer, int batch,
                 static_cast<cudaStream_t>(stream));
     if (st != QA_OK) return st;
     for (int b = 0; b < batch; ++b)
-        c->lens_host[static_cast<size_t>(layer) * c->cfg.max_batch + b] = prompt_lens[b];
+        c->lens_host[static_cast<size_t>(layer) * c->cfg.max_batch + b] += prompt_lens[b];
     return QA_OK;
 }
 
@@ -375,15 +380,17 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
         int nseq = 0, rows = 0, maxqb = 0;
         for (int i = 0; i < n; ++i) {
             const int L = prompt_lens[s0 + i];
+            const int P = c->lens_host[static_cast<size_t>(layer) * g.max_batch + s0 + i];
             if (L > 0) {
                 __nv_bfloat16 *kb = c->K + layer * c->layer_elems +
                                     static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
                 __nv_bfloat16 *vb = c->V + layer * c->layer_elems +
                                     static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
-                if (!encode_kv_map(&p.tm_k[nseq], kb, D, L, g.n_kv_heads, g.capacity) ||
-                    !encode_kv_map(&p.tm_v[nseq], vb, D, L, g.n_kv_heads, g.capacity))
+                if (!encode_kv_map(&p.tm_k[nseq], kb, D, P + L, g.n_kv_heads, g.capacity) ||
+                    !encode_kv_map(&p.tm_v[nseq], vb, D, P + L, g.n_kv_heads, g.capacity))
                     return QA_ERR_CUDA;
                 p.len[nseq] = L;
+                p.start[nseq] = P;
                 p.cu[nseq] = rows;
                 maxqb = std::max(maxqb, (L + 127) / 128);
                 ++nseq;
@@ -420,7 +427,7 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
         c->launches[QA_KERNEL_PREFILL_ATTN]++;
     }
     for (int b = 0; b < batch; ++b)
-        c->lens_host[static_cast<size_t>(layer) * g.max_batch + b] = prompt_lens[b];
+        c->lens_host[static_cast<size_t>(layer) * g.max_batch + b] += prompt_lens[b];
     return QA_OK;
 }
 

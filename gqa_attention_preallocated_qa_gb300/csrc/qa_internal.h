@@ -35,6 +35,7 @@ struct K1Params {
     int seq_slot0;                       // cache slot of the first sequence of this launch
     float eps;
     int cu[kMaxSeqPerLaunch + 1];        // row offsets of the sequences (relative to q/k/v)
+    int start[kMaxSeqPerLaunch];         // position of each sequence's first new token
 };
 
 // ---------------------------------------------------------------- K2
@@ -44,12 +45,13 @@ constexpr int kK2BlockN = 128;    // keys per tile
 
 struct alignas(64) K2Params {
     CUtensorMap tm_q;                         // q' [T][Hq][D] as (D, Hq, T)
-    CUtensorMap tm_k[kMaxSeqPerLaunch];       // per sequence: (D, L_b, Hkv) over the cache
+    CUtensorMap tm_k[kMaxSeqPerLaunch];       // per sequence: (D, start_b + L_b, Hkv) over the cache
     CUtensorMap tm_v[kMaxSeqPerLaunch];
     __nv_bfloat16 *out;                       // [T][Hq][D]
     uint32_t *err;
     int nseq, Hq, Hkv, G, npairs;             // npairs: query-head pairs per kv head
-    int len[kMaxSeqPerLaunch];
+    int len[kMaxSeqPerLaunch];                // new tokens of each sequence
+    int start[kMaxSeqPerLaunch];              // position of each sequence's first new token
     int cu[kMaxSeqPerLaunch];                 // first row of each sequence in q'/out
     int max_qblocks;
     float scale_log2;                         // log2(e) / sqrt(D)

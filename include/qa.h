@@ -45,7 +45,7 @@ typedef enum {
     QA_ERR_UNSUPPORTED_SHAPE = 2,  /* head_dim not in {64,128}, Hq % Hkv != 0, group > 8 ... */
     QA_ERR_ALIGNMENT = 3,          /* a tensor pointer is not 16-byte aligned */
     QA_ERR_CAPACITY = 4,           /* a sequence would exceed the cache capacity (no eviction) */
-    QA_ERR_STATE = 5,              /* prefill on a layer that already holds tokens */
+    QA_ERR_STATE = 5,              /* reserved (no current entry point returns it) */
     QA_ERR_CUDA = 6,               /* a CUDA runtime call failed (no device, launch error ...) */
     QA_ERR_DEVICE_TIMEOUT = 7,     /* a kernel gave up a bounded wait (reported by qa_get_device_error) */
     QA_ERR_DEVICE_BOUNDS = 8       /* a kernel saw a position outside the cache (qa_get_device_error) */
@@ -97,19 +97,21 @@ qa_status qa_cache_free(qa_cache *cache);
  * ever reads a slot at or beyond its sequence's length. */
 qa_status qa_cache_reset(qa_cache *cache, void *stream);
 
-/* Prefill one layer for `batch` prompts (sequence slots 0..batch-1).
- * prompt_lens: HOST array [batch], each in [0, capacity].  T = sum of lengths.
- * q: [T][Hq][D], k, v: [T][Hkv][D], packed in sequence order (sequence b's
- * tokens follow sequence b-1's), positions restart at 0 per sequence.
- * q_norm_w, k_norm_w: [D].  out: [T][Hq][D]; it also serves as the staging
- * buffer for the normed, rotated queries, so it must not alias q, k or v.
+/* Prefill one layer for `batch` prompts (sequence slots 0..batch-1), or the
+ * next chunk of them: the L_b = prompt_lens[b] new tokens of sequence b take
+ * positions P_b .. P_b + L_b - 1 after the P_b tokens the layer already holds
+ * (P_b = 0 after a reset).
+ * prompt_lens: HOST array [batch], each >= 0 with P_b + L_b <= capacity.
+ * T = sum of L_b.  q: [T][Hq][D], k, v: [T][Hkv][D], packed in sequence order
+ * (sequence b's tokens follow sequence b-1's).  q_norm_w, k_norm_w: [D].
+ * out: [T][Hq][D]; it also serves as the staging buffer for the normed,
+ * rotated queries, so it must not alias q, k or v.
  * Work: K1 writes q' = RoPE(RMSNorm(q)) into out and k' = RoPE(RMSNorm(k)),
- * v into cache slots 0..L_b-1, and sets the layer's lengths to prompt_lens;
- * K2 then computes out[t][h] = sum_{j<=i} softmax_j(q'_t,h . K_j / sqrt(D)) V_j
- * over the same sequence with kv head h / (Hq/Hkv).
- * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (a length above capacity), STATE
- * (the layer already holds tokens for one of the sequences: prefill appends to
- * an empty layer only). */
+ * v into cache slots P_b..P_b+L_b-1 and sets the layer's lengths to
+ * P_b + L_b; K2 then computes, for the new token at position i,
+ * out[t][h] = sum_{j<=i} softmax_j(q'_t,h . K_j / sqrt(D)) V_j over all of
+ * sequence b's cached keys 0..i, with kv head h / (Hq/Hkv).
+ * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (P_b + L_b above capacity). */
 qa_status qa_prefill(qa_cache *cache, int layer, int batch, const int32_t *prompt_lens,
                      const void *q, const void *k, const void *v,
                      const void *q_norm_w, const void *k_norm_w, void *out, void *stream);

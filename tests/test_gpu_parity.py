@@ -259,8 +259,8 @@ def test_errors_leave_state_unchanged(qa):
         assert e.value.status == 4  # capacity
         qa.qa_prefill(c.h, 0, [8], q, k, v, wq, wk, out)  # exactly the capacity
         with pytest.raises(qa.QaError) as e:
-            qa.qa_prefill(c.h, 0, [8], q, k, v, wq, wk, out)
-        assert e.value.status == 5  # layer not empty
+            qa.qa_prefill(c.h, 0, [1], q[:1], k[:1], v[:1], wq, wk, out[:1])
+        assert e.value.status == 4  # a further chunk would pass the capacity
         dq, dk, dv = (dev(a) for a in (inp.dq[0], inp.dk[0], inp.dv[0]))
         o = torch.empty_like(dq)
         with pytest.raises(qa.QaError) as e:
