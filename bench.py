@@ -509,6 +509,79 @@ def run_sweep(args):
         qa.qa_cache_free(h)
 
 
+def run_verify(args):
+    """Multi-token query against the cache (the verify step of speculative
+    decoding), served by a chunked prefill of k tokens per sequence, against k
+    decode steps of the same tokens: B = 4, cache length 2048, k in {2, 4, 8}.
+    Layers cycle as in --sweep (>= 3x L2 of caches), so K/V come from HBM.
+    One JSON line per k: µs per verify call and per k decode steps."""
+    import numpy as np
+    import torch
+
+    from gqa_attention_preallocated_qa_gb300 import binding as qa
+    from gqa_attention_preallocated_qa_gb300.configs import SweepPoint
+    from gqa_attention_preallocated_qa_gb300.inputs import layer_inputs
+
+    pt = SweepPoint(4, 2048)
+    inp = pt.inputs()
+    l2_bytes = 129 * 1000 * 1000
+    NL = max(1, -(-3 * l2_bytes // (pt.B * pt.Hkv * pt.L * pt.D * 4)))
+    reps = 40
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+    for k in (2, 4, 8):
+        tok = layer_inputs(5, [k] * pt.B, pt.Hq, pt.Hkv, pt.D, k)
+        cap = pt.L + 2 * k * (reps // NL + 2)
+        h = qa.qa_cache_alloc(NL, pt.B, pt.Hq, pt.Hkv, pt.D, cap, pt.theta, pt.eps)
+        ck, cv = dev(inp.cache_k), dev(inp.cache_v)
+        for layer in range(NL):
+            K, V, _ = qa.cache_tensors(h, layer, pt.B, pt.Hkv, cap, pt.D)
+            K[:, :, :pt.L] = ck
+            V[:, :, :pt.L] = cv
+            qa.qa_cache_set_lengths(h, layer, [pt.L] * pt.B)
+        q, kk, v, wq, wk = (dev(a) for a in (tok.q, tok.k, tok.v, tok.wq, tok.wk))
+        out = torch.empty_like(q)
+        dq, dk, dv = dev(tok.dq), dev(tok.dk), dev(tok.dv)
+        dout = torch.empty((pt.B, pt.Hq, pt.D), dtype=torch.bfloat16, device="cuda")
+        stream = torch.cuda.current_stream()
+        sh = stream.cuda_stream
+        lib = qa.lib
+        lens_arr = qa._i32([k] * pt.B)
+        pv = [t.data_ptr() for t in (q, kk, v, wq, wk, out)]
+        pd = [(dq[s].data_ptr(), dk[s].data_ptr(), dv[s].data_ptr()) for s in range(k)]
+        st = 0
+
+        def verify(layer):
+            return lib.qa_prefill(h, layer, pt.B, lens_arr, *pv, sh)
+
+        def decode(layer):
+            r = 0
+            for s in range(k):
+                r |= lib.qa_decode_step(h, layer, pt.B, *pd[s], pv[3], pv[4], dout.data_ptr(), sh)
+            return r
+        times = {}
+        for name, fn in (("verify", verify), ("decode", decode)):
+            for i in range(NL):  # warm-up pass over the layers
+                st |= fn(i % NL)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for i in range(reps):
+                st |= fn(i % NL)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times[name] = e0.elapsed_time(e1) * 1e3 / reps
+        if st or qa.qa_get_device_error(h)[0]:
+            raise RuntimeError(f"verify bench k={k} failed")
+        print(json.dumps({"verify": f"b{pt.B}_l{pt.L}_k{k}", "B": pt.B, "L": pt.L, "k": k,
+                          "layers": NL, "verify_us": round(times["verify"], 2),
+                          "decode_k_steps_us": round(times["decode"], 2),
+                          "speedup_vs_decode": round(times["decode"] / times["verify"], 3)}), flush=True)
+        qa.qa_cache_free(h)
+
+
 def run_profile_case(args):
     """A short program for ncu: one reset + prefill and four decode steps of the
     benchmark workload (B=4, prompt 2048), nothing else on the device."""
@@ -583,6 +656,8 @@ def main():
                     help="decode-only sweep over batch 1/4 and cache lengths 512..16384")
     ap.add_argument("--sweep-steps", type=int, default=1000,
                     help="timed decode steps per sweep point")
+    ap.add_argument("--verify", action="store_true",
+                    help="k-token verify (chunked prefill) vs k decode steps, B=4, L=2048")
     ap.add_argument("--profile-case", action="store_true",
                     help="run one small prefill + 4 decode steps (for ncu) and exit")
     args = ap.parse_args()
@@ -591,6 +666,8 @@ def main():
         run_profile_case(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.verify:
+        run_verify(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

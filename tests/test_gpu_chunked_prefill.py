@@ -160,3 +160,51 @@ def test_chunked_prefill_matches_one_shot_prefill(qa):
     np.testing.assert_array_equal(caches[0][1], caches[1][1])
     d = np.abs(outs[0] - outs[1])
     assert d.max() <= 2e-2 and d.mean() <= 2e-3
+
+
+def test_multi_token_verify_equals_sequential_decode(qa):
+    """A k-token query against the cache (the verify step of speculative
+    decoding) is a chunked prefill of k tokens: it matches k decode steps of
+    the same tokens within the parity bar, and leaves the same cache (V bit for
+    bit, K within the rounding bound)."""
+    Hq, Hkv, D, B, k = 32, 8, 128, 4, 4
+    prompt = (200, 129, 1, 300)
+    inp = layer_inputs(73, prompt, Hq, Hkv, D, k)
+    q, kk, v, wq, wk = (dev(a) for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+    # verify tokens packed per sequence: [B*k] rows, sequence b's k tokens together
+    vq = dev(np.ascontiguousarray(inp.dq.transpose(1, 0, 2, 3)).reshape(B * k, Hq, D))
+    vk = dev(np.ascontiguousarray(inp.dk.transpose(1, 0, 2, 3)).reshape(B * k, Hkv, D))
+    vv = dev(np.ascontiguousarray(inp.dv.transpose(1, 0, 2, 3)).reshape(B * k, Hkv, D))
+    res = []
+    for mode in ("verify", "decode"):
+        c = GpuCache(qa, 1, B, Hq, Hkv, D, 320)
+        try:
+            out = torch.empty_like(q)
+            qa.qa_prefill(c.h, 0, list(prompt), q, kk, v, wq, wk, out)
+            if mode == "verify":
+                o = torch.empty_like(vq)
+                qa.qa_prefill(c.h, 0, [k] * B, vq, vk, vv, wq, wk, o)
+                got = f64(o).reshape(B, k, Hq, D)
+            else:
+                steps = []
+                for s in range(k):
+                    o = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+                    qa.qa_decode_step(c.h, 0, B, dev(inp.dq[s]), dev(inp.dk[s]), dev(inp.dv[s]), wq, wk, o)
+                    steps.append(f64(o))
+                got = np.stack(steps, axis=1)
+            torch.cuda.synchronize()
+            K, V, L = c.views()
+            res.append((got, bits(K), bits(V), list(L.cpu().numpy()[:B])))
+            assert c.device_error() == (0, 0)
+        finally:
+            c.free()
+    (gv, kv_, vv_, lv), (gd, kd, vd, ld) = res
+    assert lv == ld == [n + k for n in prompt]
+    np.testing.assert_array_equal(vv_, vd)  # v is copied
+    # k' comes from K1 on one side and from the decode kernel on the other: the
+    # same formula, compiled apart, so equal within the bf16 rounding bound
+    for b, n in enumerate(ld):
+        kd_b = F(kd[b, :, :n])
+        assert (np.abs(F(kv_[b, :, :n]) - kd_b) <= rope_pair_tolerance(kd_b)).all()
+    d = np.abs(gv - gd)
+    assert d.max() <= 2e-2 and d.mean() <= 2e-3
