@@ -582,6 +582,82 @@ def run_verify(args):
         qa.qa_cache_free(h)
 
 
+def run_graph(args):
+    """The multi-layer decode step of the 36-layer ragged workload (B = 4,
+    prompt lengths 512/1024/1536/2048, cache capacity 2112): 36 layer decode
+    steps per generated token, eager through qa_decode_step (host positions),
+    and captured once as a CUDA graph of qa_decode_step_device_lengths calls
+    and replayed (positions advance on the device).  The caches hold seeded
+    N(0,1) keys/values (timing only; parity of this path is in the tests); at
+    1.25 GB they do not fit in L2, so every layer reads its K/V from HBM.  One
+    JSON line: µs per 36-layer step each way and per layer."""
+    import torch
+
+    from gqa_attention_preallocated_qa_gb300 import binding as qa
+    from gqa_attention_preallocated_qa_gb300.configs import RAGGED_36L as w
+
+    steps = 20
+    stream = torch.cuda.current_stream()
+    res = {}
+    for mode in ("eager", "graph"):
+        h = qa.qa_cache_alloc(w.layers, w.B, w.Hq, w.Hkv, w.D, w.cap, w.theta, w.eps)
+        gen = torch.Generator(device="cuda").manual_seed(w.seed)
+        bufs = []
+        for l in range(w.layers):  # caches hold the prompts' lengths of N(0,1) keys/values
+            K, V, _ = qa.cache_tensors(h, l, w.B, w.Hkv, w.cap, w.D)
+            K.normal_(generator=gen)
+            V.normal_(generator=gen)
+            qa.qa_cache_set_lengths(h, l, list(w.prompt_lens))
+
+            def rnd(*shape):
+                return torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+            bufs.append((rnd(w.B, w.Hq, w.D), rnd(w.B, w.Hkv, w.D), rnd(w.B, w.Hkv, w.D),
+                         (1 + 0.1 * rnd(w.D).float()).to(torch.bfloat16),
+                         (1 + 0.1 * rnd(w.D).float()).to(torch.bfloat16),
+                         torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")))
+        torch.cuda.synchronize()
+        lib = qa.lib
+        ptrs = [[t.data_ptr() for t in b] for b in bufs]
+        fn = lib.qa_decode_step if mode == "eager" else lib.qa_decode_step_device_lengths
+
+        def step(sh):
+            st = 0
+            for l in range(w.layers):
+                st |= fn(h, l, w.B, *ptrs[l], sh)
+            return st
+        st = step(stream.cuda_stream)  # warm-up (configures the kernels outside capture)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if mode == "eager":
+            e0.record(stream)
+            for _ in range(steps):
+                st |= step(stream.cuda_stream)
+            e1.record(stream)
+        else:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g):
+                    st |= step(torch.cuda.current_stream().cuda_stream)
+            stream.wait_stream(side)
+            g.replay()  # first replay outside the timing
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if st or qa.qa_get_device_error(h)[0]:
+            raise RuntimeError(f"graph bench ({mode}) failed")
+        res[mode] = e0.elapsed_time(e1) * 1e3 / steps
+        qa.qa_cache_free(h)
+    print(json.dumps({"graph": "ragged_36l_b4", "layers": w.layers, "batch": w.B,
+                      "eager_us_per_step": round(res["eager"], 1),
+                      "graph_us_per_step": round(res["graph"], 1),
+                      "eager_us_per_layer": round(res["eager"] / w.layers, 2),
+                      "graph_us_per_layer": round(res["graph"] / w.layers, 2)}), flush=True)
+
+
 def run_profile_case(args):
     """A short program for ncu: one reset + prefill and four decode steps of the
     benchmark workload (B=4, prompt 2048), nothing else on the device."""
@@ -658,6 +734,8 @@ def main():
                     help="timed decode steps per sweep point")
     ap.add_argument("--verify", action="store_true",
                     help="k-token verify (chunked prefill) vs k decode steps, B=4, L=2048")
+    ap.add_argument("--graph", action="store_true",
+                    help="36-layer decode step: eager vs one CUDA graph replay")
     ap.add_argument("--profile-case", action="store_true",
                     help="run one small prefill + 4 decode steps (for ncu) and exit")
     args = ap.parse_args()
@@ -668,6 +746,8 @@ def main():
         run_sweep(args)
     elif args.verify:
         run_verify(args)
+    elif args.graph:
+        run_graph(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -50,6 +50,9 @@ SIGNATURES = {
                                   _vp, _vp]),
     "qa_decode_step": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _vp]),
+    "qa_decode_step_device_lengths": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp,
+                                                     _vp, _vp, _vp, _vp]),
+    "qa_cache_sync_lengths": (ctypes.c_int, [_vp, ctypes.c_int, _vp]),
     "qa_cache_view": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                      ctypes.POINTER(_vp), _i64p]),
     "qa_cache_set_lengths": (ctypes.c_int, [_vp, ctypes.c_int, _i32p, _vp]),
@@ -152,6 +155,18 @@ def qa_decode_step(cache, layer, batch, q, k, v, q_norm_w, k_norm_w, out, stream
     _check(lib.qa_decode_step(cache, layer, batch, _ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w),
                               _ptr(k_norm_w), _ptr(out), _stream(stream)),
            "qa_decode_step")
+
+
+def qa_decode_step_device_lengths(cache, layer, batch, q, k, v, q_norm_w, k_norm_w, out,
+                                  stream=None) -> None:
+    _check(lib.qa_decode_step_device_lengths(cache, layer, batch, _ptr(q), _ptr(k), _ptr(v),
+                                             _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out),
+                                             _stream(stream)),
+           "qa_decode_step_device_lengths")
+
+
+def qa_cache_sync_lengths(cache, layer, stream=None) -> None:
+    _check(lib.qa_cache_sync_lengths(cache, layer, _stream(stream)), "qa_cache_sync_lengths")
 
 
 def qa_decode_step_noalloc(cfg: qa_config, positions, k_cache, v_cache, q, k, v, q_norm_w,

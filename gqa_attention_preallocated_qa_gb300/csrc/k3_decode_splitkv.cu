@@ -66,6 +66,14 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// One gpu-scope acquire-release increment (publishes this thread's earlier
+// writes and sees every earlier incrementer's).
+__device__ __forceinline__ uint32_t atomic_inc_acq_rel(uint32_t *p) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
     f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
     f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
@@ -214,7 +222,7 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk,
 // row per sequence, its own pos, which for the next step of the same layer is
 // row pos - 1; the chunk holding it is loaded after the wait.  Every write
 // (cache slot, lengths, out) also comes after the wait.
-template <int D, int HPC, bool kTableRope>
+template <int D, int HPC, bool kTableRope, bool kDevPos>
 __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
                                         const CUtensorMap *tmk, const CUtensorMap *tmv) {
     using Sh = K3Shape<D, HPC>;
@@ -239,7 +247,9 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     const int split = blockIdx.x;
     const int kvh = blockIdx.y / p.HG, hg = blockIdx.y % p.HG;
     const int bl = blockIdx.z, b = p.b0 + bl;
-    const int pos = p.pos[bl];
+    // Host positions travel in the parameters; device positions (dev_pos) are
+    // the lengths the previous kernel left, read after the launch wait.
+    int pos = kDevPos ? 0 : p.pos[bl];
     const int S = p.S;
 
     // Merge geometry.  The group's HPC x D outputs are dealt to the S CTAs of
@@ -259,13 +269,20 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     // The cache chunks plus the new key (one unit, the last) are dealt to the
     // splits in shares that differ by one at most: split `split` streams chunks
     // [c_begin, c_end) and the last split also attends to the new key.
-    const bool pos_ok = pos >= 0 && pos < p.cap;
-    const int nchunks = pos_ok ? (pos + kK3Chunk - 1) / kK3Chunk : 0;
-    const int64_t units = nchunks + 1;
-    const int c_begin = static_cast<int>(split * units / S);
-    const int c_end = static_cast<int>(min((split + 1) * units / S, static_cast<int64_t>(nchunks)));
-    const int my_chunks = max(0, c_end - c_begin);
-    const int c_safe = pos > 0 ? (pos - 1) / kK3Chunk : 0;  // chunks below row pos - 1
+    bool pos_ok = false;
+    int c_begin = 0, my_chunks = 0, c_safe = 0, first_round = 0;
+    auto plan = [&]() {
+        pos_ok = pos >= 0 && pos < p.cap;
+        const int nchunks = pos_ok ? (pos + kK3Chunk - 1) / kK3Chunk : 0;
+        const int64_t units = nchunks + 1;
+        c_begin = static_cast<int>(split * units / S);
+        const int c_end =
+            static_cast<int>(min((split + 1) * units / S, static_cast<int64_t>(nchunks)));
+        my_chunks = max(0, c_end - c_begin);
+        c_safe = pos > 0 ? (pos - 1) / kK3Chunk : 0;  // chunks below row pos - 1
+        first_round = min(NS, my_chunks);
+    };
+    if (!kDevPos) plan();
     const bool owner = split == S - 1;
     const int64_t kv_base = static_cast<int64_t>(b) * p.seq_stride + kvh * p.head_stride;
     const int h_first = kvh * p.G + hg * HPC;  // first query head of this CTA
@@ -284,7 +301,6 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
                              tm_z, fb, policy);
         }
     };
-    const int first_round = min(NS, my_chunks);
     int issued_early = 0;
     if (warp == NW && lane == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -296,8 +312,9 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         if (E_me > 0) mbar_expect_tx(smem_u32(&bar_recv), NSRC * (E_me * 4 + nh_me * 8));
         fence_mbar_init();
         policy = policy_evict_first();
-        // First loads at once, for the chunks no running kernel can be writing.
-        while (issued_early < first_round && c_begin + issued_early < c_safe) {
+        // First loads at once, for the chunks no running kernel can be writing
+        // (with host positions: device positions are not known yet).
+        while (!kDevPos && issued_early < first_round && c_begin + issued_early < c_safe) {
             issue(c_begin + issued_early, issued_early);
             ++issued_early;
         }
@@ -306,7 +323,9 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
 
     // ---------------------------------------------------------------- prologue
     // q' on the consumer warps, the new key on the producer warp of the last
-    // split; the first loads are in flight meanwhile.
+    // split; the first loads are in flight meanwhile.  With host positions it
+    // runs before the launch wait, with device positions after it.
+    auto prologue = [&]() {
     if (pos_ok && (warp < NW || owner)) {
         const int sub = lane % LPR;
         float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims at pos
@@ -341,11 +360,18 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             }
         }
     }
+    };
+    if (!kDevPos) prologue();
 
     // Programmatic dependent launch: what follows may read or overwrite what the
     // previous kernel on the stream wrote.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (kDevPos) {
+        pos = p.lens[b];
+        plan();
+        prologue();
+    }
     if (!pos_ok) {
         if (threadIdx.x == 0) set_error(p.err, kErrBounds, kKernK3, 1);
         return;
@@ -360,7 +386,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             reinterpret_cast<const uint4 *>(s_newv)[lane];
     }
     if constexpr (kTableRope) {
-        if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + 1;
+        if (!kDevPos && split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + 1;
     }
     __syncthreads();  // ring initialised, q' and the new key in shared memory
 
@@ -399,7 +425,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         for (int nt = 0; nt < D / 8; ++nt) o[nt] = make_float2(0.f, 0.f);
         float z0 = 0.f, z1 = 0.f;  // rows 8-15 of every MMA tile (all zero, never read)
 
-        for (int c = c_begin + warp, i = warp; c < c_end; c += NW, i += NW) {
+        for (int c = c_begin + warp, i = warp; i < my_chunks; c += NW, i += NW) {
             const int st = i % NS;
             bool ok = mbar_wait(smem_u32(&bar_full[st]), (i / NS) & 1, &s_abort, p.err, kKernK3, 4);
             ok = __all_sync(FULL, ok);
@@ -475,6 +501,15 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         bool ok = mbar_wait_cluster(smem_u32(&bar_recv), 0, &s_abort, p.err, kKernK3, 5);
         ok = __syncthreads_and(ok);
         if (!ok) return;
+        if (kDevPos && split == 0 && threadIdx.x == 0) {
+            // Every CTA of this group has pushed, so it has read lens[b]: count the
+            // group towards sequence b; the last group of the sequence advances it.
+            const uint32_t prev = atomic_inc_acq_rel(p.seq_cnt + b);
+            if (prev == static_cast<uint32_t>(p.Hkv * p.HG) - 1u) {
+                p.lens[b] = pos + 1;
+                p.seq_cnt[b] = 0u;
+            }
+        }
         const float c = p.scale_log2;
         constexpr int kPerLane = (kK3MaxSplits * NW + 31) / 32;
         for (int hl = warp; hl < nh_me; hl += NW + 1) {
@@ -521,23 +556,23 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     }
 }
 
-template <int D, int HPC>
+template <int D, int HPC, bool kDevPos>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_kernel(const __grid_constant__ K3Params p) {
-    k3_body<D, HPC, true>(p, nullptr, p.tm_k, p.tm_v);
+    k3_body<D, HPC, true, kDevPos>(p, nullptr, p.tm_k, p.tm_v);
 }
 
-template <int D, int HPC>
+template <int D, int HPC, bool kDevPos>
 static cudaError_t launch_k3_t(const K3Params &p, cudaStream_t stream) {
     constexpr int smem = K3Shape<D, HPC>::kSmemBytes;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 31 && !(configured_mask & (1 << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(k3_decode_kernel<D, HPC>,
+        cudaError_t e = cudaFuncSetAttribute(k3_decode_kernel<D, HPC, kDevPos>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k3_decode_kernel<D, HPC>,
+            e = cudaFuncSetAttribute(k3_decode_kernel<D, HPC, kDevPos>,
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << dev;
@@ -556,13 +591,13 @@ static cudaError_t launch_k3_t(const K3Params &p, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k3_decode_kernel<D, HPC>, p);
+    return cudaLaunchKernelEx(&cfg, k3_decode_kernel<D, HPC, kDevPos>, p);
 }
 
 template <int D, int HPC>
 static int cluster_capacity_t(int S) {
     constexpr int smem = K3Shape<D, HPC>::kSmemBytes;
-    auto kern = k3_decode_kernel<D, HPC>;
+    auto kern = k3_decode_kernel<D, HPC, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
@@ -620,17 +655,22 @@ int k3_choose_splits(int D, int HPC, int groups, int pos_max) {
     return best;
 }
 
-cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream) {
+template <bool kDevPos>
+static cudaError_t launch_k3_d(const K3Params &p, int D, int HPC, cudaStream_t stream) {
     if (D == 128) {
-        if (HPC == 4) return launch_k3_t<128, 4>(p, stream);
-        if (HPC == 2) return launch_k3_t<128, 2>(p, stream);
-        if (HPC == 1) return launch_k3_t<128, 1>(p, stream);
+        if (HPC == 4) return launch_k3_t<128, 4, kDevPos>(p, stream);
+        if (HPC == 2) return launch_k3_t<128, 2, kDevPos>(p, stream);
+        if (HPC == 1) return launch_k3_t<128, 1, kDevPos>(p, stream);
     } else if (D == 64) {
-        if (HPC == 4) return launch_k3_t<64, 4>(p, stream);
-        if (HPC == 2) return launch_k3_t<64, 2>(p, stream);
-        if (HPC == 1) return launch_k3_t<64, 1>(p, stream);
+        if (HPC == 4) return launch_k3_t<64, 4, kDevPos>(p, stream);
+        if (HPC == 2) return launch_k3_t<64, 2, kDevPos>(p, stream);
+        if (HPC == 1) return launch_k3_t<64, 1, kDevPos>(p, stream);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream) {
+    return p.dev_pos ? launch_k3_d<true>(p, D, HPC, stream) : launch_k3_d<false>(p, D, HPC, stream);
 }
 
 }  // namespace qa
@@ -660,7 +700,7 @@ struct alignas(64) K3NoAllocParams {
 template <int D, int HPC>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_noalloc_kernel(const __grid_constant__ K3NoAllocParams p) {
-    k3_body<D, HPC, false>(p.base, p.cs, &p.tmk, &p.tmv);
+    k3_body<D, HPC, false, false>(p.base, p.cs, &p.tmk, &p.tmv);
 }
 
 template <int D, int HPC>
@@ -806,6 +846,8 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     bp.head_stride = static_cast<int64_t>(g.capacity) * D;
     bp.seq_stride = bp.head_stride * g.n_kv_heads;
     bp.b0 = 0;
+    bp.dev_pos = 0;
+    bp.seq_cnt = nullptr;
     bp.B = batch;
     bp.Hq = g.n_q_heads;
     bp.Hkv = g.n_kv_heads;

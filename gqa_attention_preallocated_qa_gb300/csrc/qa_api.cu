@@ -34,6 +34,7 @@ struct qa_cache {
     int32_t *lens_dev = nullptr;
     float2 *rope = nullptr;
     uint32_t *err = nullptr;
+    uint32_t *seq_cnt = nullptr;  // decode with device lengths: groups done per sequence
     CUtensorMap *dmaps = nullptr;  // device: [layer][K, V] decode tensor maps
     std::vector<int32_t> lens_host;
     uint64_t kv_bytes = 0, scratch_bytes = 0;
@@ -42,9 +43,11 @@ struct qa_cache {
 
 namespace {
 
-__global__ void qa_reset_kernel(int32_t *lens, int n_lens) {
+__global__ void qa_reset_kernel(int32_t *lens, int n_lens, uint32_t *seq_cnt, int n_seq) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_lens; i += gridDim.x * blockDim.x)
         lens[i] = 0;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_seq; i += gridDim.x * blockDim.x)
+        seq_cnt[i] = 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -76,6 +79,7 @@ void free_all(qa_cache *c) {
     cudaFree(c->lens_dev);
     cudaFree(c->rope);
     cudaFree(c->err);
+    cudaFree(c->seq_cnt);
     cudaFree(c->dmaps);
 }
 
@@ -285,7 +289,8 @@ QA_API qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out) {
     bool ok = dev_alloc(&c->K, kv, kvb) && dev_alloc(&c->V, kv, kvb) &&
               dev_alloc(&c->lens_dev, static_cast<size_t>(g.num_layers) * g.max_batch, scr) &&
               dev_alloc(&c->rope, static_cast<size_t>(g.capacity) * (D / 2), scr) &&
-              dev_alloc(&c->err, 1, scr);
+              dev_alloc(&c->err, 1, scr) &&
+              dev_alloc(&c->seq_cnt, static_cast<size_t>(g.max_batch), scr);
     if (ok) {
         // Rotary table in fp64, stored as fp32 (cos, sin): angle = pos * theta^(-2i/D).
         std::vector<float2> tab(static_cast<size_t>(g.capacity) * (D / 2));
@@ -337,7 +342,8 @@ QA_API qa_status qa_cache_reset(qa_cache *c, void *stream) {
     if (!c) return QA_ERR_INVALID_ARG;
     const qa_config &g = c->cfg;
     const int n_lens = g.num_layers * g.max_batch;
-    qa_reset_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(c->lens_dev, n_lens);
+    qa_reset_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(c->lens_dev, n_lens,
+                                                                       c->seq_cnt, g.max_batch);
     if (cudaGetLastError() != cudaSuccess) return QA_ERR_CUDA;
     c->launches[QA_KERNEL_RESET]++;
     std::fill(c->lens_host.begin(), c->lens_host.end(), 0);
@@ -440,9 +446,14 @@ QA_API int qa_decode_splits(qa_cache *c, int layer, int batch) {
     return choose_splits(c, batch, pos_max);
 }
 
-QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q, const void *k,
-                                const void *v, const void *q_norm_w, const void *k_norm_w,
-                                void *out, void *stream) {
+namespace {
+// One decode step of `layer` for sequences 0..batch-1, one launch per 64 of
+// them.  dev_pos = false: positions from the host copy of the lengths (checked
+// against the capacity here), which advances; true: the kernel reads and
+// advances the device lengths and checks the capacity itself.
+qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const void *k,
+                      const void *v, const void *q_norm_w, const void *k_norm_w, void *out,
+                      void *stream, bool dev_pos) {
     qa_status st = check_layer(c, layer, batch);
     if (st != QA_OK) return st;
     if (!q || !k || !v || !q_norm_w || !k_norm_w || !out) return QA_ERR_INVALID_ARG;
@@ -450,12 +461,14 @@ QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q
         !aligned16(k_norm_w) || !aligned16(out))
         return QA_ERR_ALIGNMENT;
     const qa_config &g = c->cfg;
-    // The host copy of the lengths is exact (every change goes through this
-    // library), so the positions travel in the launch parameters and the kernel
-    // never waits on reading them; the kernel still sets the device lengths.
+    // The host copy of the lengths is exact while every change goes through
+    // this library, so host positions travel in the launch parameters and the
+    // kernel never waits on reading them; the kernel still sets the device
+    // lengths.  With device lengths the host copy only sizes the split plan.
     int32_t *mirror = c->lens_host.data() + static_cast<size_t>(layer) * g.max_batch;
-    for (int b = 0; b < batch; ++b)
-        if (mirror[b] + 1 > g.capacity) return QA_ERR_CAPACITY;
+    if (!dev_pos)
+        for (int b = 0; b < batch; ++b)
+            if (mirror[b] + 1 > g.capacity) return QA_ERR_CAPACITY;
     K3Params p{};
     p.tm_k = c->dmaps + 2 * layer;
     p.tm_v = c->dmaps + 2 * layer + 1;
@@ -479,6 +492,8 @@ QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q
     p.cap = g.capacity;
     p.eps = g.rms_eps;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.head_dim)));
+    p.dev_pos = dev_pos ? 1 : 0;
+    p.seq_cnt = c->seq_cnt;
     for (int b0 = 0; b0 < batch; b0 += qa::kK3MaxSeqPerLaunch) {
         const int nb = std::min(qa::kK3MaxSeqPerLaunch, batch - b0);
         int pos_max = 0;
@@ -493,7 +508,33 @@ QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q
             return QA_ERR_CUDA;
         c->launches[QA_KERNEL_DECODE_ATTN]++;
     }
-    for (int b = 0; b < batch; ++b) mirror[b] += 1;
+    if (!dev_pos)
+        for (int b = 0; b < batch; ++b) mirror[b] += 1;
+    return QA_OK;
+}
+}  // namespace
+
+QA_API qa_status qa_decode_step(qa_cache *c, int layer, int batch, const void *q, const void *k,
+                                const void *v, const void *q_norm_w, const void *k_norm_w,
+                                void *out, void *stream) {
+    return decode_step(c, layer, batch, q, k, v, q_norm_w, k_norm_w, out, stream, false);
+}
+
+QA_API qa_status qa_decode_step_device_lengths(qa_cache *c, int layer, int batch, const void *q,
+                                               const void *k, const void *v, const void *q_norm_w,
+                                               const void *k_norm_w, void *out, void *stream) {
+    return decode_step(c, layer, batch, q, k, v, q_norm_w, k_norm_w, out, stream, true);
+}
+
+QA_API qa_status qa_cache_sync_lengths(qa_cache *c, int layer, void *stream) {
+    if (!c || layer < 0 || layer >= c->cfg.num_layers) return QA_ERR_INVALID_ARG;
+    const qa_config &g = c->cfg;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(c->lens_host.data() + static_cast<size_t>(layer) * g.max_batch,
+                        c->lens_dev + static_cast<int64_t>(layer) * g.max_batch,
+                        sizeof(int32_t) * g.max_batch, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return QA_ERR_CUDA;
     return QA_OK;
 }
 

@@ -76,6 +76,8 @@ struct K3Params {
     int B, Hq, Hkv, G, HG, cap, S;
     float eps, scale_log2;
     int b0;                          // first sequence of this launch (blockIdx.z = b - b0)
+    int dev_pos;                     // 1: positions are the device lengths (pos unused)
+    uint32_t *seq_cnt;               // [max_batch] groups done per sequence (dev_pos only)
     int pos[kK3MaxSeqPerLaunch];     // slot of each launched sequence's new token
 };
 

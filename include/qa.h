@@ -136,6 +136,33 @@ qa_status qa_decode_step(qa_cache *cache, int layer, int batch,
                          const void *q, const void *k, const void *v,
                          const void *q_norm_w, const void *k_norm_w, void *out, void *stream);
 
+/* The same decode step with positions read from the DEVICE lengths, for
+ * CUDA-graph capture: a captured step advances the lengths on the device at
+ * every replay, so one graph serves every position.  (No counterpart in the
+ * pages; it serves the NEXT item "CUDA-graph-captured multi-layer decode step".)
+ * Arguments, layouts and ownership as qa_decode_step.  Differences:
+ *  - the kernel reads lens[b] after the previous kernel on the stream has
+ *    finished, and the last kv-head group of each sequence sets lens[b] + 1
+ *    (a per-sequence counter, reset by qa_cache_reset);
+ *  - the host copy of the lengths is not advanced (call qa_cache_sync_lengths
+ *    before any call that uses it: qa_prefill, qa_decode_step, the split plan);
+ *  - a sequence already at capacity is detected on the device: the step does
+ *    nothing for that sequence and qa_get_device_error returns
+ *    QA_ERR_DEVICE_BOUNDS;
+ *  - the split count is planned from the host copy at capture time (any count
+ *    is correct; it only sets the speed).
+ * Capture requires that the first call on this device for this geometry ran
+ * outside capture (it configures the kernel and caches the occupancy query).
+ * Errors: INVALID_ARG, ALIGNMENT (host side); DEVICE_BOUNDS (device side). */
+qa_status qa_decode_step_device_lengths(qa_cache *cache, int layer, int batch,
+                                        const void *q, const void *k, const void *v,
+                                        const void *q_norm_w, const void *k_norm_w, void *out,
+                                        void *stream);
+
+/* Copy one layer's device lengths into the host copy (synchronises `stream`),
+ * after decode steps that advanced them on the device. */
+qa_status qa_cache_sync_lengths(qa_cache *cache, int layer, void *stream);
+
 /* ---- test and benchmark hooks ------------------------------------------ */
 
 /* Device pointers of one layer's K, V ([max_batch][Hkv][capacity][D] bf16)

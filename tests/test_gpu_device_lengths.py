@@ -1,0 +1,151 @@
+"""Decode steps that take their positions from the device lengths
+(qa_decode_step_device_lengths), and their capture in a CUDA graph: one graph
+of a multi-layer decode step replays at every position because the kernel
+reads and advances the lengths on the device."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import GpuCache, bits, dev, f64
+from gqa_attention_preallocated_qa_gb300.inputs import layer_inputs
+
+pytestmark = pytest.mark.gpu
+
+HQ, HKV, D = 32, 8, 128
+
+
+@pytest.fixture(scope="module")
+def qa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gqa_attention_preallocated_qa_gb300 import _build
+    _build.build()
+    from gqa_attention_preallocated_qa_gb300 import binding
+    return binding
+
+
+def prefilled(qa, layers, prompt, cap, inps):
+    c = GpuCache(qa, layers, len(prompt), HQ, HKV, D, cap)
+    for l, inp in enumerate(inps):
+        q, k, v, wq, wk = (dev(a) for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+        out = torch.empty_like(q)
+        qa.qa_prefill(c.h, l, list(prompt), q, k, v, wq, wk, out)
+    torch.cuda.synchronize()
+    return c
+
+
+def test_device_lengths_step_equals_host_position_step(qa):
+    prompt, steps, cap = (300, 129, 1, 512), 5, 600
+    inp = layer_inputs(81, prompt, HQ, HKV, D, steps)
+    wq, wk = dev(inp.wq), dev(inp.wk)
+    a = prefilled(qa, 1, prompt, cap, [inp])
+    b = prefilled(qa, 1, prompt, cap, [inp])
+    try:
+        for s in range(steps):
+            dq, dk, dv = dev(inp.dq[s]), dev(inp.dk[s]), dev(inp.dv[s])
+            oa, ob = torch.empty_like(dq), torch.empty_like(dq)
+            qa.qa_decode_step(a.h, 0, 4, dq, dk, dv, wq, wk, oa)
+            qa.qa_decode_step_device_lengths(b.h, 0, 4, dq, dk, dv, wq, wk, ob)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(bits(oa), bits(ob))
+        final = [n + steps for n in prompt]
+        assert list(b.views()[2].cpu().numpy()) == final
+        assert qa.qa_cache_lengths(b.h, 0, 4) == list(prompt)  # host copy not advanced
+        qa.qa_cache_sync_lengths(b.h, 0)
+        assert qa.qa_cache_lengths(b.h, 0, 4) == final
+        Ka, Va, _ = a.views()
+        Kb, Vb, _ = b.views()
+        np.testing.assert_array_equal(bits(Ka), bits(Kb))
+        np.testing.assert_array_equal(bits(Va), bits(Vb))
+        # after the sync, host-position steps continue where the device ones left off
+        dq, dk, dv = dev(inp.dq[0]), dev(inp.dk[0]), dev(inp.dv[0])
+        oa, ob = torch.empty_like(dq), torch.empty_like(dq)
+        qa.qa_decode_step(a.h, 0, 4, dq, dk, dv, wq, wk, oa)
+        qa.qa_decode_step(b.h, 0, 4, dq, dk, dv, wq, wk, ob)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits(oa), bits(ob))
+        assert a.device_error() == (0, 0) and b.device_error() == (0, 0)
+    finally:
+        a.free()
+        b.free()
+
+
+def test_cuda_graph_of_a_two_layer_decode_step_replays_at_every_position(qa):
+    prompt, cap, replays = (200, 77, 512, 129), 560, 4
+    inps = [layer_inputs(83 + l, prompt, HQ, HKV, D, replays) for l in range(2)]
+    ws = [(dev(i.wq), dev(i.wk)) for i in inps]
+    g_cache = prefilled(qa, 2, prompt, cap, inps)
+    e_cache = prefilled(qa, 2, prompt, cap, inps)
+    try:
+        # static buffers of the captured step
+        sq = [torch.empty((4, HQ, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        sk = [torch.empty((4, HKV, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        sv = [torch.empty((4, HKV, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        so = [torch.empty((4, HQ, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+
+        def load(s):
+            for l in range(2):
+                sq[l].copy_(dev(inps[l].dq[s]))
+                sk[l].copy_(dev(inps[l].dk[s]))
+                sv[l].copy_(dev(inps[l].dv[s]))
+
+        def step(h):
+            for l in range(2):
+                qa.qa_decode_step_device_lengths(h, l, 4, sq[l], sk[l], sv[l], *ws[l], so[l])
+
+        # step 0 eagerly on both caches (configures the kernel outside capture)
+        load(0)
+        step(g_cache.h)
+        torch.cuda.synchronize()
+        want = [[f64(so[l])] for l in range(2)]
+        step(e_cache.h)
+        torch.cuda.synchronize()
+        for l in range(2):
+            np.testing.assert_array_equal(f64(so[l]), want[l][0])
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph):
+                step(g_cache.h)
+        torch.cuda.current_stream().wait_stream(side)
+        for s in range(1, replays):
+            load(s)
+            step(e_cache.h)  # eager reference of step s
+            torch.cuda.synchronize()
+            ref = [f64(so[l]) for l in range(2)]
+            load(s)
+            graph.replay()
+            torch.cuda.synchronize()
+            for l in range(2):
+                np.testing.assert_array_equal(f64(so[l]), ref[l], err_msg=f"replay {s} layer {l}")
+        final = [n + replays for n in prompt]
+        for l in range(2):
+            assert list(g_cache.views(l)[2].cpu().numpy()) == final
+            Kg, Vg, _ = g_cache.views(l)
+            Ke, Ve, _ = e_cache.views(l)
+            np.testing.assert_array_equal(bits(Kg), bits(Ke))
+            np.testing.assert_array_equal(bits(Vg), bits(Ve))
+        assert g_cache.device_error() == (0, 0) and e_cache.device_error() == (0, 0)
+    finally:
+        g_cache.free()
+        e_cache.free()
+
+
+def test_device_lengths_capacity_is_checked_on_the_device(qa):
+    prompt, cap = (40, 63), 64
+    inp = layer_inputs(89, prompt, HQ, HKV, D, 2)
+    wq, wk = dev(inp.wq), dev(inp.wk)
+    c = prefilled(qa, 1, prompt, cap, [inp])
+    try:
+        for s in range(2):
+            dq, dk, dv = dev(inp.dq[s]), dev(inp.dk[s]), dev(inp.dv[s])
+            o = torch.empty_like(dq)
+            qa.qa_decode_step_device_lengths(c.h, 0, 2, dq, dk, dv, wq, wk, o)
+        torch.cuda.synchronize()
+        # sequence 1 reached the capacity at the first step; the second found it full
+        assert list(c.views()[2].cpu().numpy()) == [42, 64]
+        st, word = c.device_error()
+        assert st == 8 and word != 0  # QA_ERR_DEVICE_BOUNDS
+    finally:
+        c.free()
