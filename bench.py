@@ -658,6 +658,83 @@ def run_graph(args):
                       "graph_us_per_layer": round(res["graph"] / w.layers, 2)}), flush=True)
 
 
+def run_window(args):
+    """Sliding-window attention against full attention: decode steps at B = 4,
+    cache length 8192 (layers cycled as in --sweep, so K/V come from HBM) with
+    W = 1024 and without; and the B = 4 x 2048 prefill with W = 512 and
+    without.  One JSON line per case: µs and the keys each query reads."""
+    import numpy as np
+    import torch
+
+    from gqa_attention_preallocated_qa_gb300 import binding as qa
+    from gqa_attention_preallocated_qa_gb300.configs import QWEN3_4B_B4, SweepPoint
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    pt = SweepPoint(4, 8192)
+    inp = pt.inputs()
+    NL = max(1, -(-3 * 129 * 1000 * 1000 // (pt.B * pt.Hkv * pt.L * pt.D * 4)))
+    reps = 200
+    for window in (0, 1024):
+        cap = pt.L + reps // NL + 20
+        h = qa.qa_cache_alloc(NL, pt.B, pt.Hq, pt.Hkv, pt.D, cap, pt.theta, pt.eps)
+        ck, cv = dev(inp.cache_k), dev(inp.cache_v)
+        for layer in range(NL):
+            K, V, _ = qa.cache_tensors(h, layer, pt.B, pt.Hkv, cap, pt.D)
+            K[:, :, :pt.L] = ck
+            V[:, :, :pt.L] = cv
+            qa.qa_cache_set_lengths(h, layer, [pt.L] * pt.B)
+            qa.qa_cache_set_window(h, layer, window)
+        q, k, v, wq, wk = (dev(a) for a in (inp.dq[0], inp.dk[0], inp.dv[0], inp.wq, inp.wk))
+        out = torch.empty_like(q)
+        ptrs = [t.data_ptr() for t in (q, k, v, wq, wk, out)]
+        st = 0
+        for i in range(NL):
+            st |= qa.lib.qa_decode_step(h, i % NL, pt.B, *ptrs, sh)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(reps):
+            st |= qa.lib.qa_decode_step(h, i % NL, pt.B, *ptrs, sh)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if st or qa.qa_get_device_error(h)[0]:
+            raise RuntimeError("window bench (decode) failed")
+        print(json.dumps({"window_decode": f"b4_l{pt.L}", "window": window,
+                          "keys_per_query": window if window else pt.L,
+                          "us_per_step": round(e0.elapsed_time(e1) * 1e3 / reps, 3)}), flush=True)
+        qa.qa_cache_free(h)
+    w = QWEN3_4B_B4
+    pin = w.inputs()
+    q, k, v, wq, wk = (dev(a) for a in (pin.q, pin.k, pin.v, pin.wq, pin.wk))
+    out = torch.empty_like(q)
+    lens_arr = qa._i32(w.prompt_lens)
+    ptrs = [t.data_ptr() for t in (q, k, v, wq, wk, out)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for window in (0, 512):
+        h = qa.qa_cache_alloc(1, w.B, w.Hq, w.Hkv, w.D, w.cap, w.theta, w.eps)
+        qa.qa_cache_set_window(h, 0, window)
+        ts = []
+        for it in range(13):
+            flush.zero_()
+            qa.lib.qa_cache_reset(h, sh)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            st = qa.lib.qa_prefill(h, 0, w.B, lens_arr, *ptrs, sh)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if st:
+                raise RuntimeError("window bench (prefill) failed")
+            if it >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        print(json.dumps({"window_prefill": "b4_p2048", "window": window,
+                          "prefill_us": round(statistics.median(ts), 2)}), flush=True)
+        qa.qa_cache_free(h)
+
+
 def run_profile_case(args):
     """A short program for ncu: one reset + prefill and four decode steps of the
     benchmark workload (B=4, prompt 2048), nothing else on the device."""
@@ -736,6 +813,8 @@ def main():
                     help="k-token verify (chunked prefill) vs k decode steps, B=4, L=2048")
     ap.add_argument("--graph", action="store_true",
                     help="36-layer decode step: eager vs one CUDA graph replay")
+    ap.add_argument("--window", action="store_true",
+                    help="sliding-window decode (L=8192, W=1024) and prefill (W=512) vs full")
     ap.add_argument("--profile-case", action="store_true",
                     help="run one small prefill + 4 decode steps (for ncu) and exit")
     args = ap.parse_args()
@@ -748,6 +827,8 @@ def main():
         run_verify(args)
     elif args.graph:
         run_graph(args)
+    elif args.window:
+        run_window(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -53,6 +53,7 @@ SIGNATURES = {
     "qa_decode_step_device_lengths": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp,
                                                      _vp, _vp, _vp, _vp]),
     "qa_cache_sync_lengths": (ctypes.c_int, [_vp, ctypes.c_int, _vp]),
+    "qa_cache_set_window": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int]),
     "qa_cache_view": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                      ctypes.POINTER(_vp), _i64p]),
     "qa_cache_set_lengths": (ctypes.c_int, [_vp, ctypes.c_int, _i32p, _vp]),
@@ -163,6 +164,10 @@ def qa_decode_step_device_lengths(cache, layer, batch, q, k, v, q_norm_w, k_norm
                                              _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out),
                                              _stream(stream)),
            "qa_decode_step_device_lengths")
+
+
+def qa_cache_set_window(cache, layer, window) -> None:
+    _check(lib.qa_cache_set_window(cache, layer, window), "qa_cache_set_window")
 
 
 def qa_cache_sync_lengths(cache, layer, stream=None) -> None:

@@ -84,7 +84,7 @@ __device__ __forceinline__ bool k2_decode_item(const K2Params &p, int idx, int &
     return false;
 }
 
-template <int D>
+template <int D, bool kWindow>
 __global__ void __launch_bounds__(kK2Threads, 1)
     k2_prefill_kernel(const __grid_constant__ K2Params p) {
     using Lay = K2Layout<D>;
@@ -109,10 +109,13 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     const int h0 = kvh * p.G + 2 * pair;
     const int L = p.len[b];
     // Query row r of the block is new token qb*128 + r at position qmin + r; it
-    // sees keys 0..qmin + r.  Key tiles 0..nkv-1 reach the block's last visible
-    // key; tiles from jmask on may hold keys past a row's position.
+    // sees keys 0..qmin + r, or with an attention window of W keys
+    // qmin + r + 1 - W..qmin + r.  Key tiles j0..j0+nkv-1 reach from row 0's
+    // first visible key to the block's last one; tiles from jmask on may hold
+    // keys past a row's position.
     const int qmin = p.start[b] + qb * 128;
-    const int nkv = (qmin + min(127, L - 1 - qb * 128)) / 128 + 1;
+    const int j0 = kWindow ? max(0, qmin + 1 - p.window) / 128 : 0;
+    const int nkv = (qmin + min(127, L - 1 - qb * 128)) / 128 + 1 - j0;
     const int jmask = qmin / 128;
 
     if (threadIdx.x == 0) {
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 const CUtensorMap *tm = (idx & 1) ? &p.tm_v[b] : &p.tm_k[b];
                 for (int x = 0; x < Lay::kBoxes; ++x)
                     tma_load_3d(sKV + st * Lay::kTileBytes + x * Lay::kBoxBytes, tm, x * 64,
-                                (idx >> 1) * 128, kvh, fb);
+                                (j0 + (idx >> 1)) * 128, kvh, fb);
             }
             // Never leave a copy in flight: bounded wait for the last ones and Q.
             int dummy = 0;
@@ -282,7 +285,9 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 tc_fence_after();
-                const int thr = qpos - j * 128;  // last visible key index in tile j
+                const int jt = j0 + j;            // key tile
+                const int thr = qpos - jt * 128;  // last visible key index in the tile
+                const int tlo = kWindow ? qpos + 1 - p.window - jt * 128 : 0;  // first visible
                 // The row of S: 4 TMEM loads in flight, one wait.
                 uint32_t sr[128];
                 {
@@ -296,10 +301,10 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                     tmem_ld32_async(tS + 96, s3);
                     tmem_wait_ld4(s0, s1, s2, s3);
                 }
-                if (j >= jmask) {  // keys after the row's own position are masked
+                if (jt >= jmask || tlo > 0) {  // keys outside the row's range are masked
 #pragma unroll
                     for (int i = 0; i < 128; ++i)
-                        if (i > thr) sr[i] = __float_as_uint(-INFINITY);
+                        if (i > thr || i < tlo) sr[i] = __float_as_uint(-INFINITY);
                 }
                 // Row max with 8 independent partial chains.
                 float mx8[8];
@@ -314,7 +319,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 bool rescale = false;
                 float alpha = 1.f;
                 if (j == 0) {
-                    mref = mx;
+                    // (a window can mask a whole first tile of a row: keep mref finite)
+                    mref = mx == -INFINITY ? 0.f : mx;
                 } else {
                     const bool grow = (mx - mref) * c > kRescaleLog2;
                     rescale = __any_sync(FULL, grow);
@@ -409,26 +415,29 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     }
 }
 
-template <int D>
+template <int D, bool kWindow>
 static cudaError_t launch_k2_t(const K2Params &p, int nitems, cudaStream_t stream) {
     constexpr int smem = K2Layout<D>::kSmemBytes;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 31 && !(configured_mask & (1 << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(k2_prefill_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(k2_prefill_kernel<D, kWindow>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << dev;
     }
-    k2_prefill_kernel<D><<<nitems, kK2Threads, smem, stream>>>(p);
+    k2_prefill_kernel<D, kWindow><<<nitems, kK2Threads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_k2(const K2Params &p, int D, int nitems, cudaStream_t stream) {
     if (nitems <= 0) return cudaSuccess;
-    if (D == 128) return launch_k2_t<128>(p, nitems, stream);
-    if (D == 64) return launch_k2_t<64>(p, nitems, stream);
+    const bool win = p.window > 0;
+    if (D == 128)
+        return win ? launch_k2_t<128, true>(p, nitems, stream) : launch_k2_t<128, false>(p, nitems, stream);
+    if (D == 64)
+        return win ? launch_k2_t<64, true>(p, nitems, stream) : launch_k2_t<64, false>(p, nitems, stream);
     return cudaErrorInvalidValue;
 }
 

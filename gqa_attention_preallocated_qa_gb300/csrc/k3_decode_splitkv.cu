@@ -135,7 +135,7 @@ __device__ __forceinline__ uint32_t keep_pair(uint32_t x, bool lo, bool hi) {
 // shared addresses sK, sV.  Lane L < 16 owns query head L/4 (rows 4..15 of the
 // MMA tile are padding); its score fragment covers keys nt*8 + 2(L%4) + {0,1}.
 template <int D>
-__device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk,
+__device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, int klo,
                                               const uint32_t (&qa0)[D / 16],
                                               const uint32_t (&qa2)[D / 16], float c, float &m,
                                               float &l, float2 (&o)[D / 8], float &z0, float &z1,
@@ -157,12 +157,13 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk,
             mma_bf16_16816(s[2 * ntp + 1], z0, z1, qa0[kk], qa2[kk], b[2], b[3]);
         }
     }
-    // Online softmax on the fragment (keys past nk are masked out).
+    // Online softmax on the fragment (keys past nk, and before klo, are masked out).
     float mx = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-        if (nt * 8 + 2 * q4 >= nk) s[nt].x = -INFINITY;
-        if (nt * 8 + 2 * q4 + 1 >= nk) s[nt].y = -INFINITY;
+        const int k0 = nt * 8 + 2 * q4;
+        if (k0 >= nk || k0 < klo) s[nt].x = -INFINITY;
+        if (k0 + 1 >= nk || k0 + 1 < klo) s[nt].y = -INFINITY;
         mx = fmaxf(mx, fmaxf(s[nt].x, s[nt].y));
     }
     mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
@@ -185,8 +186,9 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk,
 #pragma unroll
     for (int nt = 0; nt < D / 8; ++nt) o[nt] = __fmul2_rn(o[nt], a2);
     // O += P V: B fragments from the V rows by transposing loads.  In a partial
-    // chunk the rows past nk may hold anything (stale or poisoned): drop them.
-    const bool partial = nk < kK3Chunk;
+    // chunk the rows outside [klo, nk) may hold anything (stale or poisoned, or
+    // outside an attention window): drop them.
+    const bool partial = nk < kK3Chunk || klo > 0;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
@@ -198,7 +200,7 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk,
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int k0 = ks * 16 + (i & 1) * 8 + 2 * q4;
-                    b[i] = keep_pair(b[i], k0 < nk, k0 + 1 < nk);
+                    b[i] = keep_pair(b[i], k0 < nk && k0 >= klo, k0 + 1 < nk && k0 + 1 >= klo);
                 }
             }
             mma_bf16_16816(o[2 * ndp], z0, z1, pa[ks][0], pa[ks][1], b[0], b[1]);
@@ -270,14 +272,18 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     // splits in shares that differ by one at most: split `split` streams chunks
     // [c_begin, c_end) and the last split also attends to the new key.
     bool pos_ok = false;
-    int c_begin = 0, my_chunks = 0, c_safe = 0, first_round = 0;
+    int c_begin = 0, my_chunks = 0, c_safe = 0, first_round = 0, key_lo = 0;
     auto plan = [&]() {
         pos_ok = pos >= 0 && pos < p.cap;
         const int nchunks = pos_ok ? (pos + kK3Chunk - 1) / kK3Chunk : 0;
-        const int64_t units = nchunks + 1;
-        c_begin = static_cast<int>(split * units / S);
-        const int c_end =
-            static_cast<int>(min((split + 1) * units / S, static_cast<int64_t>(nchunks)));
+        // An attention window of W keys starts at key pos + 1 - W: only the
+        // chunks from the one holding it are streamed.
+        key_lo = (pos_ok && p.window > 0) ? max(0, pos + 1 - p.window) : 0;
+        const int c_lo = key_lo / kK3Chunk;
+        const int64_t units = nchunks - c_lo + 1;
+        c_begin = c_lo + static_cast<int>(split * units / S);
+        const int c_end = c_lo + static_cast<int>(min((split + 1) * units / S,
+                                                      static_cast<int64_t>(nchunks - c_lo)));
         my_chunks = max(0, c_end - c_begin);
         c_safe = pos > 0 ? (pos - 1) / kK3Chunk : 0;  // chunks below row pos - 1
         first_round = min(NS, my_chunks);
@@ -432,8 +438,9 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             if (!ok) break;
             const int nk = min(kK3Chunk, pos - c * kK3Chunk);
             const uint32_t sk = sRing + st * Sh::kStageBytes;
-            consume_chunk<D>(sk, sk + Sh::kTileBytes, nk, qa0, qa2, p.scale_log2, m, l, o, z0, z1,
-                             lane);
+            const int klo = c == key_lo / kK3Chunk ? key_lo % kK3Chunk : 0;
+            consume_chunk<D>(sk, sk + Sh::kTileBytes, nk, klo, qa0, qa2, p.scale_log2, m, l, o, z0,
+                             z1, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_empty[st]));
         }
@@ -848,6 +855,7 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     bp.b0 = 0;
     bp.dev_pos = 0;
     bp.seq_cnt = nullptr;
+    bp.window = 0;
     bp.B = batch;
     bp.Hq = g.n_q_heads;
     bp.Hkv = g.n_kv_heads;

@@ -35,6 +35,7 @@ struct qa_cache {
     float2 *rope = nullptr;
     uint32_t *err = nullptr;
     uint32_t *seq_cnt = nullptr;  // decode with device lengths: groups done per sequence
+    std::vector<int> window;      // per layer: attention window in keys (0: full)
     CUtensorMap *dmaps = nullptr;  // device: [layer][K, V] decode tensor maps
     std::vector<int32_t> lens_host;
     uint64_t kv_bytes = 0, scratch_bytes = 0;
@@ -324,6 +325,7 @@ QA_API qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out) {
         return QA_ERR_CUDA;
     }
     c->lens_host.assign(static_cast<size_t>(g.num_layers) * g.max_batch, 0);
+    c->window.assign(static_cast<size_t>(g.num_layers), 0);
     c->kv_bytes = kvb;
     c->scratch_bytes = scr;
     *out = c;
@@ -415,6 +417,7 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
             p.G = c->G;
             p.npairs = (c->G + 1) / 2;
             p.max_qblocks = maxqb;
+            p.window = c->window[layer];
             p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
             int items = 0;
             for (int i = 0; i < nseq; ++i) items += (p.len[i] + 127) / 128;
@@ -494,6 +497,7 @@ qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const vo
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.head_dim)));
     p.dev_pos = dev_pos ? 1 : 0;
     p.seq_cnt = c->seq_cnt;
+    p.window = c->window[layer];
     for (int b0 = 0; b0 < batch; b0 += qa::kK3MaxSeqPerLaunch) {
         const int nb = std::min(qa::kK3MaxSeqPerLaunch, batch - b0);
         int pos_max = 0;
@@ -524,6 +528,12 @@ QA_API qa_status qa_decode_step_device_lengths(qa_cache *c, int layer, int batch
                                                const void *k, const void *v, const void *q_norm_w,
                                                const void *k_norm_w, void *out, void *stream) {
     return decode_step(c, layer, batch, q, k, v, q_norm_w, k_norm_w, out, stream, true);
+}
+
+QA_API qa_status qa_cache_set_window(qa_cache *c, int layer, int window) {
+    if (!c || layer < 0 || layer >= c->cfg.num_layers || window < 0) return QA_ERR_INVALID_ARG;
+    c->window[layer] = window;
+    return QA_OK;
 }
 
 QA_API qa_status qa_cache_sync_lengths(qa_cache *c, int layer, void *stream) {

@@ -54,6 +54,7 @@ struct alignas(64) K2Params {
     int start[kMaxSeqPerLaunch];              // position of each sequence's first new token
     int cu[kMaxSeqPerLaunch];                 // first row of each sequence in q'/out
     int max_qblocks;
+    int window;                               // attention window in keys (0: all earlier keys)
     float scale_log2;                         // log2(e) / sqrt(D)
 };
 
@@ -76,6 +77,7 @@ struct K3Params {
     int B, Hq, Hkv, G, HG, cap, S;
     float eps, scale_log2;
     int b0;                          // first sequence of this launch (blockIdx.z = b - b0)
+    int window;                      // attention window in keys (0: the whole cache)
     int dev_pos;                     // 1: positions are the device lengths (pos unused)
     uint32_t *seq_cnt;               // [max_batch] groups done per sequence (dev_pos only)
     int pos[kK3MaxSeqPerLaunch];     // slot of each launched sequence's new token

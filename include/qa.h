@@ -159,6 +159,16 @@ qa_status qa_decode_step_device_lengths(qa_cache *cache, int layer, int batch,
                                         const void *q_norm_w, const void *k_norm_w, void *out,
                                         void *stream);
 
+/* Sliding-window attention for one layer: from now on a token at position i
+ * attends to keys max(0, i + 1 - window) .. i in qa_prefill and the decode
+ * steps (the new token always included); window = 0 restores attention over
+ * all earlier keys (the default).  The cache keeps every key (nothing is
+ * evicted); the window only limits what is read.  (No counterpart in the
+ * pages' kernels; it serves the NEXT item "sliding-window mask variant".)
+ * Host-side only, takes effect for launches after the call.
+ * Errors: INVALID_ARG (no such layer, window < 0). */
+qa_status qa_cache_set_window(qa_cache *cache, int layer, int window);
+
 /* Copy one layer's device lengths into the host copy (synchronises `stream`),
  * after decode steps that advanced them on the device. */
 qa_status qa_cache_sync_lengths(qa_cache *cache, int layer, void *stream);
