@@ -367,50 +367,61 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         }
     }
     };
-    if (!kDevPos) prologue();
-
-    // Programmatic dependent launch: what follows may read or overwrite what the
-    // previous kernel on the stream wrote.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Programmatic dependent launch: the next kernel on the stream may start as
+    // soon as every CTA of this one runs; griddepcontrol.wait (the previous
+    // kernel has finished and its writes are visible) is executed only where
+    // this step depends on it: with host positions, before loading the chunk
+    // holding row pos - 1 and before every global write; with device
+    // positions, before reading them.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (kDevPos) {
+    if constexpr (!kDevPos) {
+        prologue();
+    } else {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         pos = p.lens[b];
         plan();
+        if (warp == NW && lane == 0) {
+            for (; issued_early < first_round; ++issued_early) issue(c_begin + issued_early, issued_early);
+        }
         prologue();
     }
     if (!pos_ok) {
         if (threadIdx.x == 0) set_error(p.err, kErrBounds, kKernK3, 1);
         return;
     }
-    if (warp == NW && lane == 0)
-        for (int i = issued_early; i < first_round; ++i) issue(c_begin + i, i);
-    if (owner && warp == NW && hg == 0 && lane < LPR) {
-        // Slot pos of the cache, read only by later launches.
-        reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
-            reinterpret_cast<const uint4 *>(s_newk)[lane];
-        reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
-            reinterpret_cast<const uint4 *>(s_newv)[lane];
-    }
-    if constexpr (kTableRope) {
-        if (!kDevPos && split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + 1;
-    }
     __syncthreads();  // ring initialised, q' and the new key in shared memory
 
     if (warp == NW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued = min(NS, my_chunks);
+            bool waited = kDevPos;
+            int issued = issued_early;
             for (; issued < my_chunks; ++issued) {
                 const int st = issued % NS;
-                if (!mbar_wait(smem_u32(&bar_empty[st]), ((issued / NS) - 1) & 1, &s_abort, p.err,
+                if (issued >= NS &&
+                    !mbar_wait(smem_u32(&bar_empty[st]), ((issued / NS) - 1) & 1, &s_abort, p.err,
                                kKernK3, 2))
                     break;
+                if (!waited && c_begin + issued >= c_safe) {  // may hold the previous step's row
+                    asm volatile("griddepcontrol.wait;" ::: "memory");
+                    waited = true;
+                }
                 issue(c_begin + issued, st);
             }
             // No copy may land after the CTA exits: wait (bounded) for the last ones.
             for (int i = max(0, issued - NS); i < issued; ++i) {
                 int dummy = 0;
                 mbar_wait(smem_u32(&bar_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK3, 3);
+            }
+        }
+        if (owner && hg == 0) {
+            // Slot pos of the cache, read only by later launches.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (lane < LPR) {
+                reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
+                    reinterpret_cast<const uint4 *>(s_newk)[lane];
+                reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
+                    reinterpret_cast<const uint4 *>(s_newv)[lane];
             }
         }
     } else {
@@ -504,6 +515,10 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     // each), w_i = 2^((m_i - M) c) with M = max_i m_i and 1 / sum_i w_i l_i;
     // then each output of the run is sum_i w_i o_i times that, over the sources
     // in a fixed order (deterministic).
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // before any global write below
+    if constexpr (kTableRope && !kDevPos) {
+        if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + 1;
+    }
     if (E_me > 0) {
         bool ok = mbar_wait_cluster(smem_u32(&bar_recv), 0, &s_abort, p.err, kKernK3, 5);
         ok = __syncthreads_and(ok);
