@@ -25,7 +25,8 @@ namespace qa {
 constexpr int kRowsPerGroup = 4;
 
 template <int D>
-__global__ void __launch_bounds__(256) k1_norm_rope_append_kernel(const __grid_constant__ K1Params p) {
+// Four resident blocks per SM (<= 64 registers): more 16-byte loads in flight.
+__global__ void __launch_bounds__(256, 4) k1_norm_rope_append_kernel(const __grid_constant__ K1Params p) {
     constexpr int LPR = D / 8;     // lanes per head row
     constexpr int RPW = 32 / LPR;  // row groups per warp
     constexpr int HALF = LPR / 2;  // lane distance of the rotate-half partner
