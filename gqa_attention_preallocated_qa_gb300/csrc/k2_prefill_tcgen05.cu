@@ -7,8 +7,9 @@
 // the order of the arithmetic differs from the definition ("reorderings are
 // affordable", same guide, "Numerics").
 //
-// One CTA = one 128-row query block of one sequence for TWO query heads of the
-// same kv head (GQA: both share every K/V tile).  Warp roles (320 threads):
+// One CTA = one 128-row block of a sequence's new tokens (a whole prompt, or a
+// chunk appended after the tokens the layer already holds) for TWO query heads
+// of the same kv head (GQA: both share every K/V tile).  Warp roles (320 threads):
 //   warps 0-3  softmax warpgroup 0 (query head h0): thread r owns row r
 //   warps 4-7  softmax warpgroup 1 (query head h1)
 //   warp  8    TMA producer: Q0/Q1 once, then K_j, V_j tiles into a ring
@@ -23,8 +24,11 @@
 // thread, so it overwrites P_t only after PV_t(j) has read it.
 //
 // K and V come straight out of the cache through one 3-D tensor map per
-// sequence, (D, L_b, Hkv), so rows at or past the sequence's length read as
-// zero; the causal mask on the diagonal tile removes them from the softmax.
+// sequence, (D, P_b + L_b, Hkv), so rows at or past the sequence's length read
+// as zero; the causal mask (keys after the row's position) on the last one or
+// two key tiles of a block removes them from the softmax, and an attention
+// window adds a lower band (keys before position + 1 - W) and starts the
+// block at its window's first tile.
 // Every mbarrier wait is bounded (qa_device.cuh): a stuck pipeline records a
 // timeout in the error word and the CTA still frees its TMEM and exits.
 #include "qa_device.cuh"

@@ -1,14 +1,17 @@
 // k3_decode_splitkv.cu -- K3: one fused launch per decode step of one layer.
 //
 // For every (sequence b, kv head, head group, split) CTA:
-//   1. read pos = lens[b] (device lengths; the host never passes positions),
+//   1. take pos, the slot of the new token: from the launch parameters (the
+//      cache's exact host copy of the lengths), or, in the variant built for
+//      CUDA-graph capture, from the device lengths,
 //   2. RMSNorm + RoPE the HPC (<= 4) query heads of the group at pos, rounded
 //      to bf16 like the prefill path, staged in shared memory,
 //   3. the CTA owning the last split also norms + rotates k, appends k' and v
-//      to cache slot pos and attends to that new key from shared memory,
-//   4. stream its share of cache keys [0, pos) in 32-key chunks through a ring
-//      of shared-memory stages filled by TMA tensor copies (128-byte swizzle,
-//      evict-first L2 policy); all query heads of the group share every load,
+//      to cache slot pos and attends to that new key in registers,
+//   4. stream its share of cache keys [0, pos) (or the attention window's part
+//      of them) in 32-key chunks through a ring of shared-memory stages filled
+//      by TMA tensor copies (128-byte swizzle, evict-first L2 policy), one
+//      stage per consumer warp; all query heads of the group share every load,
 //   5. per chunk and warp: S = q' K^T and O += P V as warp-level bf16 MMAs
 //      (m16n8k16, fp32 accumulate; the 4 heads of a group fill rows 0-3 of the
 //      16-row tile, so the tile's unused rows cost tensor time, not memory),
@@ -17,9 +20,14 @@
 //   6. the S split CTAs of a group form one thread-block cluster: every
 //      consumer warp pushes its partial (m, l, o) with st.async straight into
 //      the shared memory of the CTA that owns each run of outputs, counted on
-//      that CTA's receive mbarrier; each owner merges the S x 4 partials of its
-//      run in a fixed order (deterministic), writes out[b][h] in bf16, and the
-//      last group of the sequence advances lens[b] (acquire-release counter).
+//      that CTA's receive mbarrier; each owner merges the S x 5 partials of its
+//      run in a fixed order (deterministic) and writes out[b][h] in bf16; the
+//      length of b becomes pos + 1 (written by one CTA, or, with device
+//      lengths, by the last group of the sequence through a counter).
+// With programmatic dependent launch the step overlaps the previous kernel on
+// the stream: it waits for it only before loading the chunk holding row
+// pos - 1 (the only cache row a previous decode step of the layer writes) and
+// before its global writes.
 // This serves the decode step of the dryft-flash-infer agent guide ("Where the
 // wins are": per-step overhead is the largest cost at batch 1 and 4, so the
 // step is one launch) against the preallocated cache of the same section.
@@ -210,20 +218,22 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, 
 }
 
 // The kernel body.  Sequence b = b0 + blockIdx.z takes its new token at slot
-// pos[blockIdx.z] (launch parameters).  kTableRope = true is the decode step
-// of the cache object: (cos, sin) at pos from the library's table, and the
-// device length of b set to pos + 1.  kTableRope = false is the
-// allocation-free variant: (cos, sin) of each sequence's position in cs_arr
-// (cs_arr[blockIdx.z * D/2 + i]) and the caller keeps the lengths.
-// tmk / tmv: tensor maps (D, capacity, max_batch * Hkv) over this layer's K / V.
+// pos[blockIdx.z] (launch parameters), or at lens[b] when kDevPos.
+// kTableRope = true is the decode step of the cache object: (cos, sin) at pos
+// from the library's table, and the device length of b set to pos + 1.
+// kTableRope = false is the allocation-free variant: (cos, sin) of each
+// sequence's position in cs_arr (cs_arr[blockIdx.z * D/2 + i]) and the caller
+// keeps the lengths.  tmk / tmv: tensor maps (D, capacity, max_batch * Hkv)
+// over this layer's K / V.
 //
 // Launches may overlap the tail of the previous kernel on the stream
-// (programmatic dependent launch).  Before griddepcontrol.wait the body only
-// reads what that kernel cannot be writing: its inputs (q, k, v, weights,
-// rotary table) and the cache rows below pos - 1.  A decode step writes one
-// row per sequence, its own pos, which for the next step of the same layer is
-// row pos - 1; the chunk holding it is loaded after the wait.  Every write
-// (cache slot, lengths, out) also comes after the wait.
+// (programmatic dependent launch).  With host positions, before
+// griddepcontrol.wait the body only reads what that kernel cannot be writing:
+// its inputs (q, k, v, weights, rotary table) and the cache rows below
+// pos - 1.  A decode step writes one row per sequence, its own pos, which for
+// the next step of the same layer is row pos - 1; the producer waits before
+// loading the chunk holding it, and every global write (cache slot, lengths,
+// out) comes after a wait.  With device positions everything follows the wait.
 template <int D, int HPC, bool kTableRope, bool kDevPos>
 __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
                                         const CUtensorMap *tmk, const CUtensorMap *tmv) {

@@ -1,8 +1,10 @@
 /*
  * qa.h -- C ABI of the GB300 (sm_103a) attention hot path of a greedy
  * Qwen3-style decoder: per-head QK-RMSNorm + rotary embedding + KV-cache
- * append, causal grouped-query prefill attention and single-token decode
- * attention against a preallocated bf16 KV cache.
+ * append, causal grouped-query prefill attention (whole prompts or chunks
+ * appended to what a layer holds, which also serves multi-token verify
+ * queries) and single-token decode attention against a preallocated bf16 KV
+ * cache, with an optional per-layer attention window.
  *
  * The arguments follow the pages' statement of the problem: a batch of
  * prompts with their lengths, one new token per sequence per decode step,
@@ -37,7 +39,7 @@
 extern "C" {
 #endif
 
-#define QA_ABI_VERSION 1
+#define QA_ABI_VERSION 2
 
 typedef enum {
     QA_OK = 0,
