@@ -45,13 +45,13 @@ namespace qa {
 constexpr int kK3Stages = kK3ConsumerWarps;  // one ring stage per consumer warp
 
 // Floats a CTA receives in the split merge, maximised over the split count S:
-// from each of S x kK3ConsumerWarps source warps, an o run of E elements (E a
-// multiple of 8) and (m, l) of every head.
+// from each of the S CTAs of the cluster, an o run of E elements (E a multiple
+// of 8) and (m, l) of every head.
 constexpr int k3_recv_floats(int total, int hpc) {
     int best = 0;
     for (int S = 1; S <= kK3MaxSplits; ++S) {
         const int E = ((total + S - 1) / S + 7) & ~7;
-        const int f = S * kK3ConsumerWarps * (E + 2 * hpc);
+        const int f = S * (E + 2 * hpc);
         best = f > best ? f : best;
     }
     return best;
@@ -65,7 +65,10 @@ struct K3Shape {
     static constexpr int kRingBytes = kK3Stages * kStageBytes;
     static constexpr int kQBytes = (HPC * D * 2 + 15) & ~15;
     static constexpr int kRecvFloats = k3_recv_floats(HPC * D, HPC);
-    static constexpr int kSmemBytes = 1024 + kRingBytes + kQBytes + kRecvFloats * 4;
+    // The consumer warps' partials, combined inside the CTA before the push:
+    // o [warp][head][D], then (m, l) [warp][head][2].
+    static constexpr int kRedFloats = kK3ConsumerWarps * HPC * (D + 2);
+    static constexpr int kSmemBytes = 1024 + kRingBytes + kQBytes + (kRecvFloats + kRedFloats) * 4;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -247,13 +250,14 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_recv;
     __shared__ int s_abort;
     __shared__ __align__(16) __nv_bfloat16 s_newk[D], s_newv[D];  // k', v of the new token
-    __shared__ float s_w[HPC * kK3MaxSplits * NW], s_linv[HPC];     // merge weights
+    __shared__ float s_w[HPC * kK3MaxSplits], s_linv[HPC];          // merge weights
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sRing = smem_u32(smem);
     __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes);
     float *recv = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kQBytes);
+    float *red = recv + Sh::kRecvFloats;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x;
@@ -266,10 +270,11 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
 
     // Merge geometry.  The group's HPC x D outputs are dealt to the S CTAs of
     // the cluster in runs of E (a multiple of 8); every consumer warp of every
-    // CTA (NSRC sources) sends the owner of each run its partial o for the run
+    // CTA (NSRC = S sources, its warps' partials combined first) sends the owner
+    // of each run its partial o for the run
     // and (m, l) of the heads the run touches.
     const int total = HPC * D;
-    const int NSRC = S * NW;
+    const int NSRC = S;
     const int E = ((total + S - 1) / S + 7) & ~7;
     const int e_lo = split * E;
     const int E_me = max(0, min(E, total - e_lo));
@@ -424,16 +429,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
                 mbar_wait(smem_u32(&bar_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK3, 3);
             }
         }
-        if (owner && hg == 0) {
-            // Slot pos of the cache, read only by later launches.
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            if (lane < LPR) {
-                reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
-                    reinterpret_cast<const uint4 *>(s_newk)[lane];
-                reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
-                    reinterpret_cast<const uint4 *>(s_newv)[lane];
-            }
-        }
+
     } else {
         // ------------------------------------------------------------ consumers
         // A fragments of q' (rows = heads 0..3 of the 16-row tile; padding rows zero).
@@ -497,25 +493,62 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         l += __shfl_xor_sync(FULL, l, 1);
         l += __shfl_xor_sync(FULL, l, 2);
 
-        // ------------------------------------------------------------ push the partial
-        // Lane (hrow, q4) holds o[hrow][nt*8 + 2*q4 + {0,1}]; each pair goes to the
-        // CTA owning that output run, (m, l) of head hrow to every owner it touches.
-        cluster_wait();  // every peer's receive barrier is initialised
+        // The warp's partial to shared memory: lane (hrow, q4) holds
+        // o[hrow][nt*8 + 2*q4 + {0,1}] and (m, l) of head hrow.
         if (real) {
-            const int src = split * NW + warp;
-            const uint32_t a_o = smem_u32(rcv_o + src * E);
-            const uint32_t a_bar = smem_u32(&bar_recv);
+            float *dst = red + (warp * HPC + hrow) * D;
 #pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt) {
-                const int e = hrow * D + nt * 8 + 2 * q4;
-                const int dst = e / E;
-                st_async_f32x2(map_rank(a_o + 4u * (e - dst * E), dst), o[nt].x, o[nt].y,
-                               map_rank(a_bar, dst));
-            }
+            for (int nt = 0; nt < D / 8; ++nt)
+                *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * q4) = o[nt];
             if (q4 == 0) {
-                const uint32_t a_ml = smem_u32(rcv_ml + (src * HPC + hrow) * 2);
-                for (int dst = hrow * D / E; dst <= (hrow * D + D - 1) / E; ++dst)
-                    st_async_f32x2(map_rank(a_ml, dst), m, l, map_rank(a_bar, dst));
+                float *ml = red + NW * HPC * D + (warp * HPC + hrow) * 2;
+                ml[0] = m;
+                ml[1] = l;
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- combine and push
+    // The NW warp partials of the CTA become one (m, l, o) per head, in a fixed
+    // order; each pair of outputs goes to the CTA owning its run, (m, l) of a
+    // head to every owner whose run touches the head.
+    __syncthreads();
+    cluster_wait();  // every peer's receive barrier is initialised
+    {
+        const float c = p.scale_log2;
+        const float *rml = red + NW * HPC * D;
+        const uint32_t a_bar = smem_u32(&bar_recv);
+        const uint32_t a_o = smem_u32(rcv_o + split * E);
+        for (int pe = threadIdx.x; pe < total / 2; pe += blockDim.x) {
+            const int e = 2 * pe, g = e / D, d = e % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, rml[(w * HPC + g) * 2]);
+            float2 O = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float mw = rml[(w * HPC + g) * 2];
+                const float wt = mw == -INFINITY ? 0.f : ex2((mw - M) * c);
+                const float2 ow = *reinterpret_cast<const float2 *>(red + (w * HPC + g) * D + d);
+                O = make_float2(fmaf(wt, ow.x, O.x), fmaf(wt, ow.y, O.y));
+            }
+            const int dst = e / E;
+            st_async_f32x2(map_rank(a_o + 4u * (e - dst * E), dst), O.x, O.y, map_rank(a_bar, dst));
+        }
+        for (int k = threadIdx.x; k < HPC * S; k += blockDim.x) {
+            const int g = k / S, dst = k % S;
+            const int lo = dst * E, hi = min(lo + E, total);
+            if (lo < hi && lo < (g + 1) * D && hi > g * D) {
+                float M = -INFINITY, Lsum = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) M = fmaxf(M, rml[(w * HPC + g) * 2]);
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const float mw = rml[(w * HPC + g) * 2];
+                    if (mw != -INFINITY) Lsum = fmaf(ex2((mw - M) * c), rml[(w * HPC + g) * 2 + 1], Lsum);
+                }
+                st_async_f32x2(map_rank(smem_u32(rcv_ml + (split * HPC + g) * 2), dst), M, Lsum,
+                               map_rank(a_bar, dst));
             }
         }
     }
@@ -526,6 +559,13 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     // then each output of the run is sum_i w_i o_i times that, over the sources
     // in a fixed order (deterministic).
     asm volatile("griddepcontrol.wait;" ::: "memory");  // before any global write below
+    if (owner && hg == 0 && warp == NW && lane < LPR) {
+        // Slot pos of the cache, read only by later launches.
+        reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
+            reinterpret_cast<const uint4 *>(s_newk)[lane];
+        reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
+            reinterpret_cast<const uint4 *>(s_newv)[lane];
+    }
     if constexpr (kTableRope && !kDevPos) {
         if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + 1;
     }
@@ -543,7 +583,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             }
         }
         const float c = p.scale_log2;
-        constexpr int kPerLane = (kK3MaxSplits * NW + 31) / 32;
+        constexpr int kPerLane = (kK3MaxSplits + 31) / 32;
         for (int hl = warp; hl < nh_me; hl += NW + 1) {
             const float *ml = rcv_ml + 2 * (g_lo + hl);  // source i: ml[2 * HPC * i], l after it
             float mi[kPerLane], M = -INFINITY;
@@ -561,7 +601,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
                 const int i = lane + 32 * k;
                 if (i < NSRC) {
                     const float w = mi[k] == -INFINITY ? 0.f : ex2((mi[k] - M) * c);
-                    s_w[hl * kK3MaxSplits * NW + i] = w;
+                    s_w[hl * kK3MaxSplits + i] = w;
                     Ls = fmaf(w, ml[2 * HPC * i + 1], Ls);
                 }
             }
@@ -572,7 +612,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         __syncthreads();
         for (int k = threadIdx.x; k < E_me; k += blockDim.x) {
             const int e = e_lo + k, g = e / D, d = e % D, hl = g - g_lo;
-            const float *w = s_w + hl * kK3MaxSplits * NW;
+            const float *w = s_w + hl * kK3MaxSplits;
             const float *src = rcv_o + k;
             float O4[4] = {0.f, 0.f, 0.f, 0.f};  // four running sums, added in a fixed order
             int i = 0;
