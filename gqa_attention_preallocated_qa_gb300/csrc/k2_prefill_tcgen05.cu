@@ -47,6 +47,13 @@ struct K2Layout {
     static constexpr uint32_t kTmemCols = 512;
 };
 
+// max(a, b, c) in one instruction (NaN inputs are ignored, as by fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float k2_ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -310,14 +317,19 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                     for (int i = 0; i < 128; ++i)
                         if (i > thr || i < tlo) sr[i] = __float_as_uint(-INFINITY);
                 }
-                // Row max with 8 independent partial chains.
+                // Row max: 8 independent chains of three-input maxima.
                 float mx8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(sr[k]);
+                for (int k = 0; k < 8; ++k)
+                    mx8[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
 #pragma unroll
-                for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int i = 16; i < 128; i += 16) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mx8[k] = fmax3(mx8[k], __uint_as_float(sr[i + k]), __uint_as_float(sr[i + 8 + k]));
+                }
+                const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                                       fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 // The first P.V overwrites O, so tile 0 just sets mref; later tiles move
                 // it (and rescale O by alpha, after P is written) only when it grew.
                 bool rescale = false;
