@@ -17,11 +17,12 @@
 //      16-row tile, so the tile's unused rows cost tensor time, not memory),
 //      online softmax in fp32 on the score fragments, P reused in registers as
 //      the A operand of P V,
-//   6. the S split CTAs of a group form one thread-block cluster: every
-//      consumer warp pushes its partial (m, l, o) with st.async straight into
-//      the shared memory of the CTA that owns each run of outputs, counted on
-//      that CTA's receive mbarrier; each owner merges the S x 5 partials of its
-//      run in a fixed order (deterministic) and writes out[b][h] in bf16; the
+//   6. the S split CTAs of a group form one thread-block cluster: each CTA
+//      combines its consumer warps' partials in shared memory and pushes the
+//      result (m, l, o) with st.async straight into the shared memory of the
+//      CTA that owns each run of outputs, counted on that CTA's receive
+//      mbarrier; each owner merges the S partials of its run in a fixed order
+//      (deterministic) and writes out[b][h] in bf16; the
 //      length of b becomes pos + 1 (written by one CTA, or, with device
 //      lengths, by the last group of the sequence through a counter).
 // With programmatic dependent launch the step overlaps the previous kernel on
@@ -149,8 +150,7 @@ template <int D>
 __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, int klo,
                                               const uint32_t (&qa0)[D / 16],
                                               const uint32_t (&qa2)[D / 16], float c, float &m,
-                                              float &l, float2 (&o)[D / 8], float &z0, float &z1,
-                                              int lane) {
+                                              float &l, float2 (&o)[D / 8], int lane) {
     const unsigned FULL = 0xffffffffu;
     const int mat = lane >> 3, r = lane & 7, q4 = lane & 3;
     float2 s[4];
@@ -164,8 +164,8 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, 
             const int key = (2 * ntp + (mat >> 1)) * 8 + r;
             uint32_t b[4];
             ldmatrix_x4(b, sK + swz(key, 2 * kk + (mat & 1)));
-            mma_bf16_16816(s[2 * ntp], z0, z1, qa0[kk], qa2[kk], b[0], b[1]);
-            mma_bf16_16816(s[2 * ntp + 1], z0, z1, qa0[kk], qa2[kk], b[2], b[3]);
+            mma_bf16_16816(s[2 * ntp], qa0[kk], qa2[kk], b[0], b[1]);
+            mma_bf16_16816(s[2 * ntp + 1], qa0[kk], qa2[kk], b[2], b[3]);
         }
     }
     // Online softmax on the fragment (keys past nk, and before klo, are masked out).
@@ -214,8 +214,8 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, 
                     b[i] = keep_pair(b[i], k0 < nk && k0 >= klo, k0 + 1 < nk && k0 + 1 >= klo);
                 }
             }
-            mma_bf16_16816(o[2 * ndp], z0, z1, pa[ks][0], pa[ks][1], b[0], b[1]);
-            mma_bf16_16816(o[2 * ndp + 1], z0, z1, pa[ks][0], pa[ks][1], b[2], b[3]);
+            mma_bf16_16816(o[2 * ndp], pa[ks][0], pa[ks][1], b[0], b[1]);
+            mma_bf16_16816(o[2 * ndp + 1], pa[ks][0], pa[ks][1], b[2], b[3]);
         }
     }
 }
@@ -269,10 +269,9 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     const int S = p.S;
 
     // Merge geometry.  The group's HPC x D outputs are dealt to the S CTAs of
-    // the cluster in runs of E (a multiple of 8); every consumer warp of every
-    // CTA (NSRC = S sources, its warps' partials combined first) sends the owner
-    // of each run its partial o for the run
-    // and (m, l) of the heads the run touches.
+    // the cluster in runs of E (a multiple of 8); each of the NSRC = S CTAs
+    // (its warps' partials combined first) sends the owner of each run its
+    // partial o for the run and (m, l) of the heads the run touches.
     const int total = HPC * D;
     const int NSRC = S;
     const int E = ((total + S - 1) / S + 7) & ~7;
@@ -446,7 +445,6 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         float2 o[D / 8];
 #pragma unroll
         for (int nt = 0; nt < D / 8; ++nt) o[nt] = make_float2(0.f, 0.f);
-        float z0 = 0.f, z1 = 0.f;  // rows 8-15 of every MMA tile (all zero, never read)
 
         for (int c = c_begin + warp, i = warp; i < my_chunks; c += NW, i += NW) {
             const int st = i % NS;
@@ -456,8 +454,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             const int nk = min(kK3Chunk, pos - c * kK3Chunk);
             const uint32_t sk = sRing + st * Sh::kStageBytes;
             const int klo = c == key_lo / kK3Chunk ? key_lo % kK3Chunk : 0;
-            consume_chunk<D>(sk, sk + Sh::kTileBytes, nk, klo, qa0, qa2, p.scale_log2, m, l, o, z0,
-                             z1, lane);
+            consume_chunk<D>(sk, sk + Sh::kTileBytes, nk, klo, qa0, qa2, p.scale_log2, m, l, o, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_empty[st]));
         }

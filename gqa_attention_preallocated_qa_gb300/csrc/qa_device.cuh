@@ -172,14 +172,17 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t add
                  : "r"(addr));
 }
 // D (16x8 fp32) += A (16x16 bf16) * B (16x8 bf16) where rows 8-15 of A are
-// zero (a1 = a3 = 0): rows 8-15 of D then stay as they were, so every call can
-// share one dummy pair (z0, z1) for them; d holds this lane's row-0..7 pair.
-__device__ __forceinline__ void mma_bf16_16816(float2 &d, float &z0, float &z1, uint32_t a0,
-                                               uint32_t a2, uint32_t b0, uint32_t b1) {
+// zero (a1 = a3 = 0); d holds this lane's row-0..7 pair.  Rows 8-15 of the
+// accumulator are read as constant zero and written to registers nobody reads,
+// so no two calls share an accumulator (a shared dummy pair would chain every
+// MMA of a warp into one dependency chain).
+__device__ __forceinline__ void mma_bf16_16816(float2 &d, uint32_t a0, uint32_t a2, uint32_t b0,
+                                               uint32_t b1) {
+    float t0, t1;
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
-        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d.x), "+f"(d.y), "+f"(z0), "+f"(z1)
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%10,%10};"
+        : "+f"(d.x), "+f"(d.y), "=f"(t0), "=f"(t1)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
