@@ -511,8 +511,10 @@ def run_sweep(args):
 
 def run_verify(args):
     """Multi-token query against the cache (the verify step of speculative
-    decoding), served by a chunked prefill of k tokens per sequence, against k
-    decode steps of the same tokens: B = 4, cache length 2048, k in {2, 4, 8}.
+    decoding), served by a chunked prefill of k tokens per sequence (up to 8
+    tokens: the decode kernel's multi-token form; more: the prefill kernels),
+    against k decode steps of the same tokens: B = 4, cache length 2048,
+    k in {2, 4, 8, 16}.
     Layers cycle as in --sweep (>= 3x L2 of caches), so K/V come from HBM.
     One JSON line per k: µs per verify call and per k decode steps."""
     import numpy as np
@@ -531,7 +533,7 @@ def run_verify(args):
     def dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
 
-    for k in (2, 4, 8):
+    for k in (2, 4, 8, 16):
         tok = layer_inputs(5, [k] * pt.B, pt.Hq, pt.Hkv, pt.D, k)
         cap = pt.L + 2 * k * (reps // NL + 2)
         h = qa.qa_cache_alloc(NL, pt.B, pt.Hq, pt.Hkv, pt.D, cap, pt.theta, pt.eps)

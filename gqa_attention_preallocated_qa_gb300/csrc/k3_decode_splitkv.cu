@@ -58,18 +58,19 @@ constexpr int k3_recv_floats(int total, int hpc) {
     return best;
 }
 
-template <int D, int HPC>
+// R = query rows of a CTA: HPC heads x TPS tokens (TPS = 1 for a decode step).
+template <int D, int R>
 struct K3Shape {
     static constexpr int kBoxBytes = kK3Chunk * 128;         // 32 rows x 64 bf16, swizzled
     static constexpr int kTileBytes = (D / 64) * kBoxBytes;  // K (or V) of one chunk
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kK3Stages * kStageBytes;
-    static constexpr int kQBytes = (HPC * D * 2 + 15) & ~15;
-    static constexpr int kRecvFloats = k3_recv_floats(HPC * D, HPC);
-    // The consumer warps' partials, combined inside the CTA before the push:
-    // o [warp][head][D], then (m, l) [warp][head][2].
-    static constexpr int kRedFloats = kK3ConsumerWarps * HPC * (D + 2);
-    static constexpr int kSmemBytes = 1024 + kRingBytes + kQBytes + (kRecvFloats + kRedFloats) * 4;
+    static constexpr int kQBytes = (R * D * 2 + 15) & ~15;
+    static constexpr int kRecvFloats = k3_recv_floats(R * D, R);
+    static constexpr int kSmemBytes = 1024 + kRingBytes + kQBytes + kRecvFloats * 4;
+    // Each consumer warp leaves its partial (o [row][D], then (m, l) [row][2])
+    // in its own ring stage once it has consumed its last chunk.
+    static_assert(R * (D + 2) * 4 <= kStageBytes, "partial must fit a ring stage");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -144,10 +145,12 @@ __device__ __forceinline__ uint32_t keep_pair(uint32_t x, bool lo, bool hi) {
 }
 
 // One warp consumes one chunk of nk (1..32) keys whose K and V tiles start at
-// shared addresses sK, sV.  Lane L < 16 owns query head L/4 (rows 4..15 of the
-// MMA tile are padding); its score fragment covers keys nt*8 + 2(L%4) + {0,1}.
+// shared addresses sK, sV.  Lane L owns query row L/4 of the MMA tile (rows
+// 8..15 are padding); its score fragment covers keys nt*8 + 2(L%4) + {0,1}.
+// The lane's row sees keys [klo, nk) of the chunk; kvlo <= klo of every row is
+// the first key any row sees (rows below it, and from nk on, may hold anything).
 template <int D>
-__device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, int klo,
+__device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, int klo, int kvlo,
                                               const uint32_t (&qa0)[D / 16],
                                               const uint32_t (&qa2)[D / 16], float c, float &m,
                                               float &l, float2 (&o)[D / 8], int lane) {
@@ -181,7 +184,7 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, 
     mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
     const float m_new = fmaxf(m, mx);
     const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * c);
-    const float neg = m_new * c;
+    const float neg = (m_new == -INFINITY) ? 0.f : m_new * c;  // a row with no key yet: p = 0
     float ps = 0.f;
     uint32_t pa[2][2];  // P as A fragments: [k-step][a0 | a2]
 #pragma unroll
@@ -197,9 +200,9 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, 
 #pragma unroll
     for (int nt = 0; nt < D / 8; ++nt) o[nt] = __fmul2_rn(o[nt], a2);
     // O += P V: B fragments from the V rows by transposing loads.  In a partial
-    // chunk the rows outside [klo, nk) may hold anything (stale or poisoned, or
+    // chunk the rows outside [kvlo, nk) may hold anything (stale or poisoned, or
     // outside an attention window): drop them.
-    const bool partial = nk < kK3Chunk || klo > 0;
+    const bool partial = nk < kK3Chunk || kvlo > 0;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
@@ -211,7 +214,7 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, 
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int k0 = ks * 16 + (i & 1) * 8 + 2 * q4;
-                    b[i] = keep_pair(b[i], k0 < nk && k0 >= klo, k0 + 1 < nk && k0 + 1 >= klo);
+                    b[i] = keep_pair(b[i], k0 < nk && k0 >= kvlo, k0 + 1 < nk && k0 + 1 >= kvlo);
                 }
             }
             mma_bf16_16816(o[2 * ndp], pa[ks][0], pa[ks][1], b[0], b[1]);
@@ -220,27 +223,38 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, 
     }
 }
 
-// The kernel body.  Sequence b = b0 + blockIdx.z takes its new token at slot
-// pos[blockIdx.z] (launch parameters), or at lens[b] when kDevPos.
-// kTableRope = true is the decode step of the cache object: (cos, sin) at pos
-// from the library's table, and the device length of b set to pos + 1.
-// kTableRope = false is the allocation-free variant: (cos, sin) of each
-// sequence's position in cs_arr (cs_arr[blockIdx.z * D/2 + i]) and the caller
-// keeps the lengths.  tmk / tmv: tensor maps (D, capacity, max_batch * Hkv)
-// over this layer's K / V.
+// The kernel body.  A CTA serves the R = HPC x TPS query rows (token t, head
+// h) -> row t * HPC + h of one (sequence, kv head, head group) for one split.
+// TPS = 1 is the decode step: sequence b = b0 + blockIdx.z, one new token at
+// slot pos[blockIdx.z] (launch parameters), or at lens[b] when kDevPos.
+// TPS > 1 takes up to TPS new tokens of sequence mt->seq[blockIdx.z] at slots
+// pos .. pos + ntok - 1: token t attends to the cache keys and to the new
+// tokens 0..t (causal), and the cache takes all of them.
+// kTableRope = true is the cache object's path: (cos, sin) from the library's
+// table and the device length of b set after the step.  kTableRope = false is
+// the allocation-free variant (TPS = 1): (cos, sin) of each sequence's
+// position in cs_arr (cs_arr[blockIdx.z * D/2 + i]) and the caller keeps the
+// lengths.  tmk / tmv: tensor maps (D, capacity, max_batch * Hkv) over this
+// layer's K / V.
 //
-// Launches may overlap the tail of the previous kernel on the stream
-// (programmatic dependent launch).  With host positions, before
-// griddepcontrol.wait the body only reads what that kernel cannot be writing:
-// its inputs (q, k, v, weights, rotary table) and the cache rows below
-// pos - 1.  A decode step writes one row per sequence, its own pos, which for
-// the next step of the same layer is row pos - 1; the producer waits before
-// loading the chunk holding it, and every global write (cache slot, lengths,
-// out) comes after a wait.  With device positions everything follows the wait.
-template <int D, int HPC, bool kTableRope, bool kDevPos>
+// Launches overlap the tail of the previous kernel on the stream
+// (programmatic dependent launch).  Every CTA signals its dependents only
+// after its own griddepcontrol.wait, so when a launch starts, every kernel
+// before the immediately preceding one has finished.  That one, if it is a
+// step of this family on the same layer, writes at most kK3MaxTokens rows just
+// below this step's first slot.  So before its own wait the body reads only its
+// inputs (q, k, v, weights, rotary table) and the cache rows below
+// pos - kK3MaxTokens; the producer waits before loading the chunk holding that
+// row, and every global write (cache slots, lengths, out) comes after a wait.
+// With device positions everything follows the wait.
+template <int D, int HPC, int TPS, bool kTableRope, bool kDevPos>
 __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
-                                        const CUtensorMap *tmk, const CUtensorMap *tmv) {
-    using Sh = K3Shape<D, HPC>;
+                                        const CUtensorMap *tmk, const CUtensorMap *tmv,
+                                        const K3Multi *mt) {
+    constexpr int R = HPC * TPS;
+    static_assert(R <= 8, "query rows live in rows 0-7 of the MMA tile");
+    static_assert(TPS == 1 || (kTableRope && !kDevPos), "multi-token steps use host positions");
+    using Sh = K3Shape<D, R>;
     constexpr int LPR = D / 8;
     constexpr int NW = kK3ConsumerWarps;
     constexpr int NS = kK3Stages;
@@ -249,30 +263,32 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_recv;
     __shared__ int s_abort;
-    __shared__ __align__(16) __nv_bfloat16 s_newk[D], s_newv[D];  // k', v of the new token
-    __shared__ float s_w[HPC * kK3MaxSplits], s_linv[HPC];          // merge weights
+    __shared__ __align__(16) __nv_bfloat16 s_newk[TPS * D], s_newv[TPS * D];  // new k', v
+    __shared__ float s_w[R * kK3MaxSplits], s_linv[R];                         // merge weights
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sRing = smem_u32(smem);
     __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + Sh::kRingBytes);
     float *recv = reinterpret_cast<float *>(smem + Sh::kRingBytes + Sh::kQBytes);
-    float *red = recv + Sh::kRecvFloats;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x;
     const int kvh = blockIdx.y / p.HG, hg = blockIdx.y % p.HG;
-    const int bl = blockIdx.z, b = p.b0 + bl;
+    const int bl = blockIdx.z;
+    const int b = TPS == 1 ? p.b0 + bl : mt->seq[bl];
+    const int ntok = TPS == 1 ? 1 : mt->ntok[bl];
+    const int qrow0 = TPS == 1 ? b : mt->row0[bl];  // row of token 0 in q, k, v, out
     // Host positions travel in the parameters; device positions (dev_pos) are
     // the lengths the previous kernel left, read after the launch wait.
     int pos = kDevPos ? 0 : p.pos[bl];
     const int S = p.S;
 
-    // Merge geometry.  The group's HPC x D outputs are dealt to the S CTAs of
-    // the cluster in runs of E (a multiple of 8); each of the NSRC = S CTAs
-    // (its warps' partials combined first) sends the owner of each run its
-    // partial o for the run and (m, l) of the heads the run touches.
-    const int total = HPC * D;
+    // Merge geometry.  The CTA's R x D outputs are dealt to the S CTAs of the
+    // cluster in runs of E (a multiple of 8); each of the NSRC = S CTAs (its
+    // warps' partials combined first) sends the owner of each run its partial
+    // o for the run and (m, l) of the rows the run touches.
+    const int total = R * D;
     const int NSRC = S;
     const int E = ((total + S - 1) / S + 7) & ~7;
     const int e_lo = split * E;
@@ -280,18 +296,18 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     const int g_lo = e_lo / D;
     const int nh_me = E_me > 0 ? (e_lo + E_me - 1) / D - g_lo + 1 : 0;
     float *rcv_o = recv;               // [NSRC][E]
-    float *rcv_ml = recv + NSRC * E;   // [NSRC][HPC][2]
+    float *rcv_ml = recv + NSRC * E;   // [NSRC][R][2]
 
-    // The cache chunks plus the new key (one unit, the last) are dealt to the
+    // The cache chunks plus the new tokens (one unit, the last) are dealt to the
     // splits in shares that differ by one at most: split `split` streams chunks
-    // [c_begin, c_end) and the last split also attends to the new key.
+    // [c_begin, c_end) and the last split also attends to the new tokens.
     bool pos_ok = false;
     int c_begin = 0, my_chunks = 0, c_safe = 0, first_round = 0, key_lo = 0;
     auto plan = [&]() {
-        pos_ok = pos >= 0 && pos < p.cap;
+        pos_ok = pos >= 0 && ntok >= 1 && ntok <= TPS && pos + ntok <= p.cap;
         const int nchunks = pos_ok ? (pos + kK3Chunk - 1) / kK3Chunk : 0;
-        // An attention window of W keys starts at key pos + 1 - W: only the
-        // chunks from the one holding it are streamed.
+        // An attention window of W keys starts token t at key pos + t + 1 - W:
+        // only the chunks from the one holding token 0's first key are streamed.
         key_lo = (pos_ok && p.window > 0) ? max(0, pos + 1 - p.window) : 0;
         const int c_lo = key_lo / kK3Chunk;
         const int64_t units = nchunks - c_lo + 1;
@@ -299,7 +315,8 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         const int c_end = c_lo + static_cast<int>(min((split + 1) * units / S,
                                                       static_cast<int64_t>(nchunks - c_lo)));
         my_chunks = max(0, c_end - c_begin);
-        c_safe = pos > 0 ? (pos - 1) / kK3Chunk : 0;  // chunks below row pos - 1
+        // chunks wholly below row pos - kK3MaxTokens
+        c_safe = pos > kK3MaxTokens ? (pos - kK3MaxTokens) / kK3Chunk : 0;
         first_round = min(NS, my_chunks);
     };
     if (!kDevPos) plan();
@@ -342,56 +359,64 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     cluster_arrive();  // peers may push into this CTA once they have waited on this
 
     // ---------------------------------------------------------------- prologue
-    // q' on the consumer warps, the new key on the producer warp of the last
-    // split; the first loads are in flight meanwhile.  With host positions it
-    // runs before the launch wait, with device positions after it.
+    // The R query rows q' and, on the last split, the new tokens' k' and v go
+    // to shared memory; all six warps share the rows (warp w takes items w,
+    // w + 6, ...: query rows first, then new tokens) while the first loads are
+    // in flight.  With host positions it runs before the launch wait, with
+    // device positions after it.
     auto prologue = [&]() {
-    if (pos_ok && (warp < NW || owner)) {
+    if (pos_ok) {
         const int sub = lane % LPR;
-        float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims at pos
-        if constexpr (!kTableRope) {
-            const float4 *src = reinterpret_cast<const float4 *>(cs_arr + bl * (D / 2) +
-                                                                 8 * (sub % (LPR / 2)));
+        const int nitems = R + (owner ? ntok : 0);
+        for (int it = warp; it < nitems; it += NW + 1) {  // warp-uniform
+            const int t = it < R ? it / HPC : it - R;  // the item's token
+            if (t >= ntok) continue;
+            float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims at pos + t
+            if constexpr (!kTableRope) {
+                const float4 *src = reinterpret_cast<const float4 *>(cs_arr + bl * (D / 2) +
+                                                                     8 * (sub % (LPR / 2)));
 #pragma unroll
-            for (int e = 0; e < 4; ++e) cs[e] = src[e];
-        } else {
-            const float4 *tab = reinterpret_cast<const float4 *>(
-                p.rope + static_cast<int64_t>(pos) * (D / 2) + 8 * (sub % (LPR / 2)));
+                for (int e = 0; e < 4; ++e) cs[e] = src[e];
+            } else {
+                const float4 *tab = reinterpret_cast<const float4 *>(
+                    p.rope + static_cast<int64_t>(pos + t) * (D / 2) + 8 * (sub % (LPR / 2)));
 #pragma unroll
-            for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + e);
-        }
-        // Warp w norms and rotates query head w of the CTA into shared memory.
-        if (warp < HPC && warp < NW) {
-            const uint4 qp = norm_rope_row<D>(
-                p.q + (static_cast<int64_t>(b) * p.Hq + h_first + warp) * D, p.wq, cs, p.eps, sub);
-            if (lane < LPR) reinterpret_cast<uint4 *>(qs + warp * D)[sub] = qp;
-        }
-        if (owner && warp == NW) {
-            // The new token: k' and v into shared memory; the copy into cache slot
-            // pos waits for the previous kernel below.
-            const uint4 kp = norm_rope_row<D>(p.k + (static_cast<int64_t>(b) * p.Hkv + kvh) * D,
-                                              p.wk, cs, p.eps, sub);
-            const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(
-                                       p.v + (static_cast<int64_t>(b) * p.Hkv + kvh) * D) +
-                                   sub);
-            if (lane < LPR) {
-                reinterpret_cast<uint4 *>(s_newk)[sub] = kp;
-                reinterpret_cast<uint4 *>(s_newv)[sub] = vv;
+                for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + e);
+            }
+            if (it < R) {
+                const uint4 qp = norm_rope_row<D>(
+                    p.q + (static_cast<int64_t>(qrow0 + t) * p.Hq + h_first + it % HPC) * D, p.wq,
+                    cs, p.eps, sub);
+                if (lane < LPR) reinterpret_cast<uint4 *>(qs + it * D)[sub] = qp;
+            } else {
+                // A new token: k' and v; the copy into cache slot pos + t waits for
+                // the previous kernel below.
+                const int64_t kr = (static_cast<int64_t>(qrow0 + t) * p.Hkv + kvh) * D;
+                const uint4 kp = norm_rope_row<D>(p.k + kr, p.wk, cs, p.eps, sub);
+                const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(p.v + kr) + sub);
+                if (lane < LPR) {
+                    reinterpret_cast<uint4 *>(s_newk + t * D)[sub] = kp;
+                    reinterpret_cast<uint4 *>(s_newv + t * D)[sub] = vv;
+                }
             }
         }
     }
     };
-    // Programmatic dependent launch: the next kernel on the stream may start as
-    // soon as every CTA of this one runs; griddepcontrol.wait (the previous
-    // kernel has finished and its writes are visible) is executed only where
-    // this step depends on it: with host positions, before loading the chunk
-    // holding row pos - 1 and before every global write; with device
-    // positions, before reading them.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Programmatic dependent launch: griddepcontrol.wait (the previous kernel
+    // has finished and its writes are visible) is executed only where this step
+    // depends on it: with host positions, before loading the chunk holding row
+    // pos - kK3MaxTokens and before every global write; with device positions,
+    // before reading them.  launch_dependents comes right after a wait: with
+    // device positions the first one; with host positions that of the last
+    // consumer warp, which waits as soon as the prologue is done (the other
+    // warps go on; every thread waits before the global writes in any case,
+    // so even a CTA that counts as signalling only when it exits does so
+    // after a wait).
     if constexpr (!kDevPos) {
         prologue();
     } else {
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         pos = p.lens[b];
         plan();
         if (warp == NW && lane == 0) {
@@ -400,10 +425,11 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         prologue();
     }
     if (!pos_ok) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         if (threadIdx.x == 0) set_error(p.err, kErrBounds, kKernK3, 1);
         return;
     }
-    __syncthreads();  // ring initialised, q' and the new key in shared memory
+    __syncthreads();  // ring initialised, q' and the new tokens in shared memory
 
     if (warp == NW) {
         // ------------------------------------------------------------ producer
@@ -416,7 +442,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
                     !mbar_wait(smem_u32(&bar_empty[st]), ((issued / NS) - 1) & 1, &s_abort, p.err,
                                kKernK3, 2))
                     break;
-                if (!waited && c_begin + issued >= c_safe) {  // may hold the previous step's row
+                if (!waited && c_begin + issued >= c_safe) {  // may hold a previous step's rows
                     asm volatile("griddepcontrol.wait;" ::: "memory");
                     waited = true;
                 }
@@ -431,9 +457,14 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
 
     } else {
         // ------------------------------------------------------------ consumers
-        // A fragments of q' (rows = heads 0..3 of the 16-row tile; padding rows zero).
+        if (!kDevPos && warp == NW - 1) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        }
+        // A fragments of q' (row r = lane / 4 of the 16-row tile; padding rows zero).
         const int hrow = lane >> 2, q4 = lane & 3;
-        const bool real = lane < 16 && hrow < HPC;
+        const int trow = TPS == 1 ? 0 : hrow / HPC;  // the row's token
+        const bool real = hrow < R && trow < ntok;
         uint32_t qa0[D / 16], qa2[D / 16];
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -441,6 +472,9 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             qa0[kk] = real ? qrow[q4] : 0u;
             qa2[kk] = real ? qrow[4 + q4] : 0u;
         }
+        // First cache key of the row's window: token t at pos + t sees keys from
+        // pos + t + 1 - W.
+        const int row_lo = p.window > 0 ? max(0, pos + trow + 1 - p.window) : 0;
         float m = -INFINITY, l = 0.f;
         float2 o[D / 8];
 #pragma unroll
@@ -451,120 +485,153 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             bool ok = mbar_wait(smem_u32(&bar_full[st]), (i / NS) & 1, &s_abort, p.err, kKernK3, 4);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
-            const int nk = min(kK3Chunk, pos - c * kK3Chunk);
+            const int base = c * kK3Chunk;
+            const int nk = min(kK3Chunk, pos - base);
             const uint32_t sk = sRing + st * Sh::kStageBytes;
-            const int klo = c == key_lo / kK3Chunk ? key_lo % kK3Chunk : 0;
-            consume_chunk<D>(sk, sk + Sh::kTileBytes, nk, klo, qa0, qa2, p.scale_log2, m, l, o, lane);
+            const int kvlo = max(0, key_lo - base);
+            const int klo = TPS == 1 ? kvlo : min(kK3Chunk, max(0, row_lo - base));
+            consume_chunk<D>(sk, sk + Sh::kTileBytes, nk, klo, kvlo, qa0, qa2, p.scale_log2, m, l,
+                             o, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_empty[st]));
         }
         if (owner && warp == my_chunks % NW) {
-            // The new key, on the warp whose turn is next: s = q'.k' (the 4 lanes of a
-            // head split the dims), then the online-softmax update of the lane's o.
+            // The new tokens, on the warp whose turn is next: s_u = q'.k'_u (the 4
+            // lanes of a row split the dims) for the tokens u <= t the row's token
+            // t sees (and, with a window of W keys, t - u < W), then one
+            // online-softmax update of the lane's o.
             const float c = p.scale_log2;
-            float sd = 0.f;
-            if (real) {
-                const __nv_bfloat162 *qh =
-                    reinterpret_cast<const __nv_bfloat162 *>(qs + hrow * D) + q4 * (D / 8);
-                const __nv_bfloat162 *kh = reinterpret_cast<const __nv_bfloat162 *>(s_newk) + q4 * (D / 8);
+            float sd[TPS];
+            float mx = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < D / 8; ++i) {
-                    const float2 a = __bfloat1622float2(qh[i]), kk = __bfloat1622float2(kh[i]);
-                    sd = fmaf(a.x, kk.x, fmaf(a.y, kk.y, sd));
+            for (int u = 0; u < TPS; ++u) {
+                float x = 0.f;
+                if (real && u <= trow) {
+                    const __nv_bfloat162 *qh =
+                        reinterpret_cast<const __nv_bfloat162 *>(qs + hrow * D) + q4 * (D / 8);
+                    const __nv_bfloat162 *kh =
+                        reinterpret_cast<const __nv_bfloat162 *>(s_newk + u * D) + q4 * (D / 8);
+#pragma unroll
+                    for (int i = 0; i < D / 8; ++i) {
+                        const float2 a = __bfloat1622float2(qh[i]), kk = __bfloat1622float2(kh[i]);
+                        x = fmaf(a.x, kk.x, fmaf(a.y, kk.y, x));
+                    }
                 }
+                x += __shfl_xor_sync(FULL, x, 1);
+                x += __shfl_xor_sync(FULL, x, 2);
+                const bool seen = real && u <= trow && (p.window <= 0 || trow - u < p.window);
+                sd[u] = seen ? x : -INFINITY;
+                mx = fmaxf(mx, sd[u]);
             }
-            sd += __shfl_xor_sync(FULL, sd, 1);
-            sd += __shfl_xor_sync(FULL, sd, 2);
-            const float m_new = fmaxf(m, sd);
+            const float m_new = fmaxf(m, mx);
             const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * c);
-            const float pn = ex2((sd - m_new) * c);
-            l = fmaf(l, alpha, q4 == 0 ? pn : 0.f);  // l is summed over the quad below
+            const float neg = (m_new == -INFINITY) ? 0.f : m_new * c;
+            float pn[TPS], ps = 0.f;
+#pragma unroll
+            for (int u = 0; u < TPS; ++u) {
+                pn[u] = ex2(fmaf(sd[u], c, -neg));
+                ps += pn[u];
+            }
+            l = fmaf(l, alpha, q4 == 0 ? ps : 0.f);  // l is summed over the quad below
             m = m_new;
-            const __nv_bfloat162 *vh = reinterpret_cast<const __nv_bfloat162 *>(s_newv);
 #pragma unroll
             for (int nt = 0; nt < D / 8; ++nt) {
-                const float2 vv = __bfloat1622float2(vh[nt * 4 + q4]);
-                o[nt] = make_float2(fmaf(pn, vv.x, o[nt].x * alpha), fmaf(pn, vv.y, o[nt].y * alpha));
+                float2 acc = make_float2(o[nt].x * alpha, o[nt].y * alpha);
+#pragma unroll
+                for (int u = 0; u < TPS; ++u) {
+                    if (u < ntok) {
+                        const float2 vv = __bfloat1622float2(
+                            reinterpret_cast<const __nv_bfloat162 *>(s_newv + u * D)[nt * 4 + q4]);
+                        acc = make_float2(fmaf(pn[u], vv.x, acc.x), fmaf(pn[u], vv.y, acc.y));
+                    }
+                }
+                o[nt] = acc;
             }
         }
         l += __shfl_xor_sync(FULL, l, 1);
         l += __shfl_xor_sync(FULL, l, 2);
 
-        // The warp's partial to shared memory: lane (hrow, q4) holds
-        // o[hrow][nt*8 + 2*q4 + {0,1}] and (m, l) of head hrow.
+        // The warp's partial into its own ring stage (no copy lands there any
+        // more): lane (hrow, q4) holds o[hrow][nt*8 + 2*q4 + {0,1}] and (m, l)
+        // of row hrow.
         if (real) {
-            float *dst = red + (warp * HPC + hrow) * D;
+            float *red = reinterpret_cast<float *>(smem + warp * Sh::kStageBytes);
+            float *dst = red + hrow * D;
 #pragma unroll
             for (int nt = 0; nt < D / 8; ++nt)
                 *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * q4) = o[nt];
             if (q4 == 0) {
-                float *ml = red + NW * HPC * D + (warp * HPC + hrow) * 2;
-                ml[0] = m;
-                ml[1] = l;
+                red[R * D + hrow * 2] = m;
+                red[R * D + hrow * 2 + 1] = l;
             }
         }
     }
 
     // ---------------------------------------------------------------- combine and push
-    // The NW warp partials of the CTA become one (m, l, o) per head, in a fixed
+    // The NW warp partials of the CTA become one (m, l, o) per row, in a fixed
     // order; each pair of outputs goes to the CTA owning its run, (m, l) of a
-    // head to every owner whose run touches the head.
+    // row to every owner whose run touches the row.  Rows of tokens past ntok
+    // are carried along and never written out.
     __syncthreads();
     cluster_wait();  // every peer's receive barrier is initialised
     {
         const float c = p.scale_log2;
-        const float *rml = red + NW * HPC * D;
+        constexpr int kWF = Sh::kStageBytes / 4;  // floats between two warps' partials
+        const float *red = reinterpret_cast<const float *>(smem);
         const uint32_t a_bar = smem_u32(&bar_recv);
         const uint32_t a_o = smem_u32(rcv_o + split * E);
         for (int pe = threadIdx.x; pe < total / 2; pe += blockDim.x) {
             const int e = 2 * pe, g = e / D, d = e % D;
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) M = fmaxf(M, rml[(w * HPC + g) * 2]);
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * kWF + R * D + g * 2]);
             float2 O = make_float2(0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                const float mw = rml[(w * HPC + g) * 2];
+                const float mw = red[w * kWF + R * D + g * 2];
                 const float wt = mw == -INFINITY ? 0.f : ex2((mw - M) * c);
-                const float2 ow = *reinterpret_cast<const float2 *>(red + (w * HPC + g) * D + d);
+                const float2 ow = *reinterpret_cast<const float2 *>(red + w * kWF + g * D + d);
                 O = make_float2(fmaf(wt, ow.x, O.x), fmaf(wt, ow.y, O.y));
             }
             const int dst = e / E;
             st_async_f32x2(map_rank(a_o + 4u * (e - dst * E), dst), O.x, O.y, map_rank(a_bar, dst));
         }
-        for (int k = threadIdx.x; k < HPC * S; k += blockDim.x) {
+        for (int k = threadIdx.x; k < R * S; k += blockDim.x) {
             const int g = k / S, dst = k % S;
             const int lo = dst * E, hi = min(lo + E, total);
             if (lo < hi && lo < (g + 1) * D && hi > g * D) {
                 float M = -INFINITY, Lsum = 0.f;
 #pragma unroll
-                for (int w = 0; w < NW; ++w) M = fmaxf(M, rml[(w * HPC + g) * 2]);
+                for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * kWF + R * D + g * 2]);
 #pragma unroll
                 for (int w = 0; w < NW; ++w) {
-                    const float mw = rml[(w * HPC + g) * 2];
-                    if (mw != -INFINITY) Lsum = fmaf(ex2((mw - M) * c), rml[(w * HPC + g) * 2 + 1], Lsum);
+                    const float mw = red[w * kWF + R * D + g * 2];
+                    if (mw != -INFINITY)
+                        Lsum = fmaf(ex2((mw - M) * c), red[w * kWF + R * D + g * 2 + 1], Lsum);
                 }
-                st_async_f32x2(map_rank(smem_u32(rcv_ml + (split * HPC + g) * 2), dst), M, Lsum,
+                st_async_f32x2(map_rank(smem_u32(rcv_ml + (split * R + g) * 2), dst), M, Lsum,
                                map_rank(a_bar, dst));
             }
         }
     }
 
     // ---------------------------------------------------------------- merge
-    // Once every source's bytes have landed: per head of the run (one warp
+    // Once every source's bytes have landed: per row of the run (one warp
     // each), w_i = 2^((m_i - M) c) with M = max_i m_i and 1 / sum_i w_i l_i;
     // then each output of the run is sum_i w_i o_i times that, over the sources
     // in a fixed order (deterministic).
     asm volatile("griddepcontrol.wait;" ::: "memory");  // before any global write below
     if (owner && hg == 0 && warp == NW && lane < LPR) {
-        // Slot pos of the cache, read only by later launches.
-        reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
-            reinterpret_cast<const uint4 *>(s_newk)[lane];
-        reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos) * D)[lane] =
-            reinterpret_cast<const uint4 *>(s_newv)[lane];
+        // Slots pos.. of the cache, read only by later launches.
+        for (int t = 0; t < ntok; ++t) {
+            reinterpret_cast<uint4 *>(p.kc + kv_base + static_cast<int64_t>(pos + t) * D)[lane] =
+                reinterpret_cast<const uint4 *>(s_newk + t * D)[lane];
+            reinterpret_cast<uint4 *>(p.vc + kv_base + static_cast<int64_t>(pos + t) * D)[lane] =
+                reinterpret_cast<const uint4 *>(s_newv + t * D)[lane];
+        }
     }
     if constexpr (kTableRope && !kDevPos) {
-        if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + 1;
+        if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + ntok;
     }
     if (E_me > 0) {
         bool ok = mbar_wait_cluster(smem_u32(&bar_recv), 0, &s_abort, p.err, kKernK3, 5);
@@ -582,12 +649,12 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         const float c = p.scale_log2;
         constexpr int kPerLane = (kK3MaxSplits + 31) / 32;
         for (int hl = warp; hl < nh_me; hl += NW + 1) {
-            const float *ml = rcv_ml + 2 * (g_lo + hl);  // source i: ml[2 * HPC * i], l after it
+            const float *ml = rcv_ml + 2 * (g_lo + hl);  // source i: ml[2 * R * i], l after it
             float mi[kPerLane], M = -INFINITY;
 #pragma unroll
             for (int k = 0; k < kPerLane; ++k) {
                 const int i = lane + 32 * k;
-                mi[k] = i < NSRC ? ml[2 * HPC * i] : -INFINITY;
+                mi[k] = i < NSRC ? ml[2 * R * i] : -INFINITY;
                 M = fmaxf(M, mi[k]);
             }
 #pragma unroll
@@ -599,7 +666,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
                 if (i < NSRC) {
                     const float w = mi[k] == -INFINITY ? 0.f : ex2((mi[k] - M) * c);
                     s_w[hl * kK3MaxSplits + i] = w;
-                    Ls = fmaf(w, ml[2 * HPC * i + 1], Ls);
+                    Ls = fmaf(w, ml[2 * R * i + 1], Ls);
                 }
             }
 #pragma unroll
@@ -609,6 +676,8 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         __syncthreads();
         for (int k = threadIdx.x; k < E_me; k += blockDim.x) {
             const int e = e_lo + k, g = e / D, d = e % D, hl = g - g_lo;
+            const int t = g / HPC, hh = g % HPC;
+            if (t >= ntok) continue;
             const float *w = s_w + hl * kK3MaxSplits;
             const float *src = rcv_o + k;
             float O4[4] = {0.f, 0.f, 0.f, 0.f};  // four running sums, added in a fixed order
@@ -619,7 +688,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             }
             for (; i < NSRC; ++i) O4[0] = fmaf(w[i], src[i * E], O4[0]);
             const float O = (O4[0] + O4[1]) + (O4[2] + O4[3]);
-            p.out[(static_cast<int64_t>(b) * p.Hq + h_first + g) * D + d] =
+            p.out[(static_cast<int64_t>(qrow0 + t) * p.Hq + h_first + hh) * D + d] =
                 __float2bfloat16_rn(O * s_linv[hl]);
         }
     }
@@ -628,7 +697,19 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
 template <int D, int HPC, bool kDevPos>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_kernel(const __grid_constant__ K3Params p) {
-    k3_body<D, HPC, true, kDevPos>(p, nullptr, p.tm_k, p.tm_v);
+    k3_body<D, HPC, 1, true, kDevPos>(p, nullptr, p.tm_k, p.tm_v, nullptr);
+}
+
+// Up to TPS new tokens per sequence (HPC x TPS = 8 query rows per CTA).
+struct K3MultiParams {
+    K3Params base;
+    K3Multi mt;
+};
+
+template <int D, int HPC, int TPS>
+__global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
+    k3_multi_kernel(const __grid_constant__ K3MultiParams p) {
+    k3_body<D, HPC, TPS, true, false>(p.base, nullptr, p.base.tm_k, p.base.tm_v, &p.mt);
 }
 
 template <int D, int HPC, bool kDevPos>
@@ -663,10 +744,8 @@ static cudaError_t launch_k3_t(const K3Params &p, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, k3_decode_kernel<D, HPC, kDevPos>, p);
 }
 
-template <int D, int HPC>
-static int cluster_capacity_t(int S) {
-    constexpr int smem = K3Shape<D, HPC>::kSmemBytes;
-    auto kern = k3_decode_kernel<D, HPC, false>;
+template <typename Kern>
+static int cluster_capacity_k(Kern kern, int smem, int S) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
@@ -693,34 +772,43 @@ static int cluster_capacity_t(int S) {
     return n;
 }
 
-int k3_cluster_capacity(int D, int HPC, int S) {
+template <int D, int HPC>
+static int cluster_capacity_t(int S, bool multi) {
+    if (!multi) return cluster_capacity_k(k3_decode_kernel<D, HPC, false>, K3Shape<D, HPC>::kSmemBytes, S);
+    return cluster_capacity_k(k3_multi_kernel<D, HPC, 8 / HPC>, K3Shape<D, 8>::kSmemBytes, S);
+}
+
+int k3_cluster_capacity(int D, int HPC, int S, bool multi) {
     constexpr int kDev = 16;
-    // [device][D == 128][HPC 1/2/4][S]: 0 = not queried yet, -1 = query failed
-    static int cache[kDev][2][3][kK3MaxSplits + 1] = {};
+    // [device][D == 128][multi][HPC 1/2/4][S]: 0 = not queried yet, -1 = query failed
+    static int cache[kDev][2][2][3][kK3MaxSplits + 1] = {};
     static std::mutex mu;
     int dev = 0;
     if (S < 1 || S > kK3MaxSplits || cudaGetDevice(&dev) != cudaSuccess || dev >= kDev) return 0;
+    if ((D != 64 && D != 128) || (HPC != 1 && HPC != 2 && HPC != 4)) return 0;
     const int di = D == 128 ? 1 : 0, hi = HPC == 4 ? 2 : (HPC == 2 ? 1 : 0);
     std::lock_guard<std::mutex> lock(mu);
-    int &slot = cache[dev][di][hi][S];
+    int &slot = cache[dev][di][multi ? 1 : 0][hi][S];
     if (slot == 0) {
         int n = 0;
         if (D == 128)
-            n = HPC == 4 ? cluster_capacity_t<128, 4>(S)
-                         : (HPC == 2 ? cluster_capacity_t<128, 2>(S) : cluster_capacity_t<128, 1>(S));
+            n = HPC == 4 ? cluster_capacity_t<128, 4>(S, multi)
+                         : (HPC == 2 ? cluster_capacity_t<128, 2>(S, multi)
+                                     : cluster_capacity_t<128, 1>(S, multi));
         else
-            n = HPC == 4 ? cluster_capacity_t<64, 4>(S)
-                         : (HPC == 2 ? cluster_capacity_t<64, 2>(S) : cluster_capacity_t<64, 1>(S));
+            n = HPC == 4 ? cluster_capacity_t<64, 4>(S, multi)
+                         : (HPC == 2 ? cluster_capacity_t<64, 2>(S, multi)
+                                     : cluster_capacity_t<64, 1>(S, multi));
         slot = n > 0 ? n : -1;
     }
     return slot > 0 ? slot : 0;
 }
 
-int k3_choose_splits(int D, int HPC, int groups, int pos_max) {
+int k3_choose_splits(int D, int HPC, int groups, int pos_max, bool multi) {
     const int nchunks = (pos_max + kK3Chunk - 1) / kK3Chunk;
     int best = 1;
     for (int S = 2; S <= std::min(kK3MaxSplits, std::max(1, nchunks)); ++S)
-        if (k3_cluster_capacity(D, HPC, S) >= groups) best = S;
+        if (k3_cluster_capacity(D, HPC, S, multi) >= groups) best = S;
     return best;
 }
 
@@ -740,6 +828,54 @@ static cudaError_t launch_k3_d(const K3Params &p, int D, int HPC, cudaStream_t s
 
 cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream) {
     return p.dev_pos ? launch_k3_d<true>(p, D, HPC, stream) : launch_k3_d<false>(p, D, HPC, stream);
+}
+
+template <int D, int HPC>
+static cudaError_t launch_k3_multi_t(const K3MultiParams &p, cudaStream_t stream) {
+    constexpr int TPS = 8 / HPC;
+    constexpr int smem = K3Shape<D, 8>::kSmemBytes;
+    auto kern = k3_multi_kernel<D, HPC, TPS>;
+    static int configured_mask = 0;  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 31 && !(configured_mask & (1 << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        configured_mask |= 1 << dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.base.S, p.base.Hkv * p.base.HG, p.base.B);
+    cfg.blockDim = dim3((kK3ConsumerWarps + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.base.S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_k3_multi(const K3Params &p, const K3Multi &m, int D, int HPC,
+                            cudaStream_t stream) {
+    K3MultiParams mp;
+    mp.base = p;
+    mp.mt = m;
+    if (D == 128) {
+        if (HPC == 4) return launch_k3_multi_t<128, 4>(mp, stream);
+        if (HPC == 2) return launch_k3_multi_t<128, 2>(mp, stream);
+        if (HPC == 1) return launch_k3_multi_t<128, 1>(mp, stream);
+    } else if (D == 64) {
+        if (HPC == 4) return launch_k3_multi_t<64, 4>(mp, stream);
+        if (HPC == 2) return launch_k3_multi_t<64, 2>(mp, stream);
+        if (HPC == 1) return launch_k3_multi_t<64, 1>(mp, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace qa
@@ -769,7 +905,7 @@ struct alignas(64) K3NoAllocParams {
 template <int D, int HPC>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_noalloc_kernel(const __grid_constant__ K3NoAllocParams p) {
-    k3_body<D, HPC, false, false>(p.base, p.cs, &p.tmk, &p.tmv);
+    k3_body<D, HPC, 1, false, false>(p.base, p.cs, &p.tmk, &p.tmv, nullptr);
 }
 
 template <int D, int HPC>
@@ -882,7 +1018,7 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     if (st != QA_OK) return st;
 
     // Split plan as in qa_decode_step (the variant has the same resources).
-    const int S = k3_choose_splits(D, HPC, groups, pos_max);
+    const int S = k3_choose_splits(D, HPC, groups, pos_max, false);
 
     K3NoAllocParams p{};
     if (!encode_decode_map(&p.tmk, k_cache, D, g.capacity, g.max_batch * g.n_kv_heads) ||

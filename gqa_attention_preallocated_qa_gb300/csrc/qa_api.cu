@@ -154,7 +154,7 @@ namespace {
 
 int choose_splits(const qa_cache *c, int batch, int pos_max) {
     return qa::k3_choose_splits(c->cfg.head_dim, c->HPC, batch * c->cfg.n_kv_heads * c->HG,
-                                pos_max);
+                                pos_max, false);
 }
 
 // Validation shared by qa_prefill and qa_prefill_transform.
@@ -235,6 +235,82 @@ qa_status run_k1(qa_cache *c, int layer, int batch, const int32_t *lens, const v
             c->launches[QA_KERNEL_NORM_ROPE_APPEND]++;
         }
         row0 += p.T;
+    }
+    return QA_OK;
+}
+
+// The decode kernel's parameters common to every launch on `layer`.
+K3Params make_k3(qa_cache *c, int layer, const void *q, const void *k, const void *v,
+                 const void *wq, const void *wk, void *out) {
+    const qa_config &g = c->cfg;
+    K3Params p{};
+    p.tm_k = c->dmaps + 2 * layer;
+    p.tm_v = c->dmaps + 2 * layer + 1;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.wq = static_cast<const __nv_bfloat16 *>(wq);
+    p.wk = static_cast<const __nv_bfloat16 *>(wk);
+    p.kc = c->K + layer * c->layer_elems;
+    p.vc = c->V + layer * c->layer_elems;
+    p.lens = c->lens_dev + static_cast<int64_t>(layer) * g.max_batch;
+    p.rope = c->rope;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.err = c->err;
+    p.head_stride = static_cast<int64_t>(g.capacity) * g.head_dim;
+    p.seq_stride = p.head_stride * g.n_kv_heads;
+    p.Hq = g.n_q_heads;
+    p.Hkv = g.n_kv_heads;
+    p.G = c->G;
+    p.HG = c->HG;
+    p.cap = g.capacity;
+    p.eps = g.rms_eps;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.head_dim)));
+    p.seq_cnt = c->seq_cnt;
+    p.window = c->window[layer];
+    return p;
+}
+
+// A chunk of at most kK3MaxTokens new tokens per sequence (a verify step, a
+// short append) runs as multi-token launches of the decode kernel, one per 64
+// sequences that have new tokens: every (sequence, kv head) streams its cache
+// once for all of its new tokens.  A CTA holds HPC heads x 8 / HPC tokens.
+qa_status run_multi(qa_cache *c, int layer, int batch, const int32_t *lens, int tmax,
+                    const void *q, const void *k, const void *v, const void *wq, const void *wk,
+                    void *out, cudaStream_t s) {
+    const qa_config &g = c->cfg;
+    int HPC = c->HPC;
+    while (HPC > 1 && qa::kK3MaxTokens / HPC < tmax) HPC /= 2;
+    K3Params p = make_k3(c, layer, q, k, v, wq, wk, out);
+    p.HG = c->G / HPC;
+    const int32_t *mirror = c->lens_host.data() + static_cast<size_t>(layer) * g.max_batch;
+    std::vector<std::pair<K3Params, qa::K3Multi>> launches;
+    qa::K3Multi m{};
+    int nz = 0, row = 0, pos_max = 0;
+    auto flush = [&]() {
+        if (nz == 0) return;
+        p.B = nz;
+        p.S = qa::k3_choose_splits(g.head_dim, HPC, nz * g.n_kv_heads * p.HG, pos_max, true);
+        launches.emplace_back(p, m);
+        nz = 0;
+        pos_max = 0;
+    };
+    for (int b = 0; b < batch; ++b) {
+        if (lens[b] > 0) {
+            m.seq[nz] = b;
+            m.ntok[nz] = lens[b];
+            m.row0[nz] = row;
+            p.pos[nz] = mirror[b];
+            pos_max = std::max(pos_max, static_cast<int>(mirror[b]));
+            if (++nz == qa::kK3MaxSeqPerLaunch) flush();
+        }
+        row += lens[b];
+    }
+    flush();
+    for (const auto &l : launches) {
+        if (qa::launch_k3_multi(l.first, l.second, g.head_dim, HPC, s) != cudaSuccess)
+            return QA_ERR_CUDA;
+        c->launches[QA_KERNEL_DECODE_ATTN]++;
     }
     return QA_OK;
 }
@@ -378,6 +454,15 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
     const qa_config &g = c->cfg;
     const int D = g.head_dim;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int tmax = 0;
+    for (int b = 0; b < batch; ++b) tmax = std::max(tmax, static_cast<int>(prompt_lens[b]));
+    if (tmax > 0 && tmax <= qa::kK3MaxTokens) {
+        st = run_multi(c, layer, batch, prompt_lens, tmax, q, k, v, q_norm_w, k_norm_w, out, s);
+        if (st != QA_OK) return st;
+        for (int b = 0; b < batch; ++b)
+            c->lens_host[static_cast<size_t>(layer) * g.max_batch + b] += prompt_lens[b];
+        return QA_OK;
+    }
     // Build all tensor maps before the first launch so a failure enqueues nothing.
     std::vector<K2Params> k2s;
     std::vector<int> k2_items;
@@ -472,32 +557,8 @@ qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const vo
     if (!dev_pos)
         for (int b = 0; b < batch; ++b)
             if (mirror[b] + 1 > g.capacity) return QA_ERR_CAPACITY;
-    K3Params p{};
-    p.tm_k = c->dmaps + 2 * layer;
-    p.tm_v = c->dmaps + 2 * layer + 1;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.k = static_cast<const __nv_bfloat16 *>(k);
-    p.v = static_cast<const __nv_bfloat16 *>(v);
-    p.wq = static_cast<const __nv_bfloat16 *>(q_norm_w);
-    p.wk = static_cast<const __nv_bfloat16 *>(k_norm_w);
-    p.kc = c->K + layer * c->layer_elems;
-    p.vc = c->V + layer * c->layer_elems;
-    p.lens = c->lens_dev + static_cast<int64_t>(layer) * g.max_batch;
-    p.rope = c->rope;
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.err = c->err;
-    p.head_stride = static_cast<int64_t>(g.capacity) * g.head_dim;
-    p.seq_stride = p.head_stride * g.n_kv_heads;
-    p.Hq = g.n_q_heads;
-    p.Hkv = g.n_kv_heads;
-    p.G = c->G;
-    p.HG = c->HG;
-    p.cap = g.capacity;
-    p.eps = g.rms_eps;
-    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.head_dim)));
+    K3Params p = make_k3(c, layer, q, k, v, q_norm_w, k_norm_w, out);
     p.dev_pos = dev_pos ? 1 : 0;
-    p.seq_cnt = c->seq_cnt;
-    p.window = c->window[layer];
     for (int b0 = 0; b0 < batch; b0 += qa::kK3MaxSeqPerLaunch) {
         const int nb = std::min(qa::kK3MaxSeqPerLaunch, batch - b0);
         int pos_max = 0;

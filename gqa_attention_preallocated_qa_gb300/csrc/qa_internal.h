@@ -63,6 +63,9 @@ constexpr int kK3ConsumerWarps = 5;
 constexpr int kK3Chunk = 32;        // keys per pipeline chunk
 constexpr int kK3MaxSplits = 16;   // splits of one (sequence, kv head) = CTAs of one cluster
 constexpr int kK3MaxSeqPerLaunch = 64;  // positions carried in one launch's parameters
+// New tokens per sequence of one launch of the decode kernel family (1 for a
+// decode step, up to this many for a short chunk such as a verify step).
+constexpr int kK3MaxTokens = 8;
 
 struct K3Params {
     const CUtensorMap *tm_k, *tm_v;  // (D, capacity, max_batch * Hkv) over this layer's K / V
@@ -80,7 +83,17 @@ struct K3Params {
     int window;                      // attention window in keys (0: the whole cache)
     int dev_pos;                     // 1: positions are the device lengths (pos unused)
     uint32_t *seq_cnt;               // [max_batch] groups done per sequence (dev_pos only)
-    int pos[kK3MaxSeqPerLaunch];     // slot of each launched sequence's new token
+    int pos[kK3MaxSeqPerLaunch];     // slot of each launched sequence's (first) new token
+};
+
+// Per-sequence data of a multi-token launch of the decode kernel (a short
+// chunk, e.g. the tokens of a verify step): launched sequence z is cache slot
+// seq[z] and holds ntok[z] (1..kK3MaxTokens) new tokens whose rows in q, k,
+// v and out start at row0[z]; they take slots pos[z] .. pos[z] + ntok[z] - 1.
+struct K3Multi {
+    int seq[kK3MaxSeqPerLaunch];
+    int ntok[kK3MaxSeqPerLaunch];
+    int row0[kK3MaxSeqPerLaunch];
 };
 
 }  // namespace qa
@@ -95,10 +108,14 @@ bool encode_decode_map(CUtensorMap *m, void *base, int D, int capacity, int rows
 cudaError_t launch_k1(const K1Params &p, int D, cudaStream_t stream);
 cudaError_t launch_k2(const K2Params &p, int D, int nitems, cudaStream_t stream);
 cudaError_t launch_k3(const K3Params &p, int D, int HPC, cudaStream_t stream);
-// Number of clusters of S decode CTAs that can be resident at once on the
-// current device (cached per device, head_dim, heads per CTA and S); 0 on error.
-int k3_cluster_capacity(int D, int HPC, int S);
+// The multi-token form: p.HG = G / HPC groups of HPC heads, 8 / HPC tokens.
+cudaError_t launch_k3_multi(const K3Params &p, const K3Multi &m, int D, int HPC,
+                            cudaStream_t stream);
+// Number of clusters of S decode CTAs (multi: of the multi-token form) that can
+// be resident at once on the current device (cached per device, head_dim,
+// form, heads per CTA and S); 0 on error.
+int k3_cluster_capacity(int D, int HPC, int S, bool multi);
 // Largest split count (<= kK3MaxSplits, <= chunks) whose `groups` clusters all
 // fit on the device at once.
-int k3_choose_splits(int D, int HPC, int groups, int pos_max);
+int k3_choose_splits(int D, int HPC, int groups, int pos_max, bool multi);
 }  // namespace qa

@@ -108,11 +108,18 @@ qa_status qa_cache_reset(qa_cache *cache, void *stream);
  * (sequence b's tokens follow sequence b-1's).  q_norm_w, k_norm_w: [D].
  * out: [T][Hq][D]; it also serves as the staging buffer for the normed,
  * rotated queries, so it must not alias q, k or v.
- * Work: K1 writes q' = RoPE(RMSNorm(q)) into out and k' = RoPE(RMSNorm(k)),
- * v into cache slots P_b..P_b+L_b-1 and sets the layer's lengths to
- * P_b + L_b; K2 then computes, for the new token at position i,
- * out[t][h] = sum_{j<=i} softmax_j(q'_t,h . K_j / sqrt(D)) V_j over all of
- * sequence b's cached keys 0..i, with kv head h / (Hq/Hkv).
+ * Result: k' = RoPE(RMSNorm(k)) and v go to cache slots P_b..P_b+L_b-1, the
+ * layer's lengths become P_b + L_b, and for the new token at position i
+ * out[t][h] = sum_{j<=i} softmax_j(q'_t,h . K_j / sqrt(D)) V_j over sequence
+ * b's cached keys 0..i, q' = RoPE(RMSNorm(q)), kv head h / (Hq/Hkv).
+ * Work: when some L_b exceeds 8, K1 writes q' into out and k', v into the
+ * cache, then K2 (one launch per 8 sequences) computes the attention.  When
+ * every L_b is at most 8 (a verify step of speculative decoding, a short
+ * append), the decode kernel's multi-token form does all of it in one launch
+ * per 64 sequences that have new tokens (each streams its cache once for all
+ * of its new tokens; counted as QA_KERNEL_DECODE_ATTN).  That form overlaps
+ * the previous kernel on the stream like qa_decode_step, with the same
+ * condition on q, k and v.
  * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (P_b + L_b above capacity). */
 qa_status qa_prefill(qa_cache *cache, int layer, int batch, const int32_t *prompt_lens,
                      const void *q, const void *k, const void *v,
@@ -130,8 +137,12 @@ qa_status qa_prefill(qa_cache *cache, int layer, int batch, const int32_t *promp
  * launch parameters (one launch per 64 sequences).  Launches may overlap the
  * previous kernel on the stream (programmatic dependent launch): the step
  * reads q, k, v and the weights before that kernel has finished, so they must
- * not be written by the immediately preceding decode step (its out buffer in
- * particular must not be this step's q, k or v).
+ * not be written by the immediately preceding decode step or short chunk (its
+ * out buffer in particular must not be this step's q, k or v).  Each launch
+ * lets the next one start only after its own wait for the previous kernel, so
+ * at most that one kernel is still running; the cache rows it can be writing
+ * (at most 8 per sequence, just below this step's position) are read only
+ * after this step's wait.
  * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (a sequence already holds
  * `capacity` tokens; nothing is evicted or wrapped). */
 qa_status qa_decode_step(qa_cache *cache, int layer, int batch,
