@@ -237,16 +237,18 @@ __device__ __forceinline__ void consume_chunk(uint32_t sK, uint32_t sV, int nk, 
 // lengths.  tmk / tmv: tensor maps (D, capacity, max_batch * Hkv) over this
 // layer's K / V.
 //
-// Launches overlap the tail of the previous kernel on the stream
-// (programmatic dependent launch).  Every CTA signals its dependents only
-// after its own griddepcontrol.wait, so when a launch starts, every kernel
-// before the immediately preceding one has finished.  That one, if it is a
-// step of this family on the same layer, writes at most kK3MaxTokens rows just
-// below this step's first slot.  So before its own wait the body reads only its
-// inputs (q, k, v, weights, rotary table) and the cache rows below
-// pos - kK3MaxTokens; the producer waits before loading the chunk holding that
-// row, and every global write (cache slots, lengths, out) comes after a wait.
-// With device positions everything follows the wait.
+// Launches overlap the kernels before them on the stream (programmatic
+// dependent launch).  With host positions a launch signals its dependents at
+// once, and every CTA waits (griddepcontrol.wait) for the previous kernel
+// before it exits; launches of this family still running when a launch starts
+// may be writing cache rows of its layer just below its first new slot, and
+// the host, which tracks them, passes their number as p.guard.  So before its
+// own wait the body reads only its inputs (q, k, v, weights, rotary table)
+// and the cache rows below pos - guard; the producer waits before loading the
+// chunk holding that row, and every global write (cache slots, lengths, out)
+// comes after a wait.  With device positions everything follows the wait and
+// the signal comes right after it; the allocation-free variant (launched
+// without overlap) never signals early.
 template <int D, int HPC, int TPS, bool kTableRope, bool kDevPos>
 __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
                                         const CUtensorMap *tmk, const CUtensorMap *tmv,
@@ -315,8 +317,8 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         const int c_end = c_lo + static_cast<int>(min((split + 1) * units / S,
                                                       static_cast<int64_t>(nchunks - c_lo)));
         my_chunks = max(0, c_end - c_begin);
-        // chunks wholly below row pos - kK3MaxTokens
-        c_safe = pos > kK3MaxTokens ? (pos - kK3MaxTokens) / kK3Chunk : 0;
+        // chunks wholly below row pos - guard (all of them without a guard)
+        c_safe = p.guard <= 0 ? nchunks : (pos > p.guard ? (pos - p.guard) / kK3Chunk : 0);
         first_round = min(NS, my_chunks);
     };
     if (!kDevPos) plan();
@@ -405,14 +407,10 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     // Programmatic dependent launch: griddepcontrol.wait (the previous kernel
     // has finished and its writes are visible) is executed only where this step
     // depends on it: with host positions, before loading the chunk holding row
-    // pos - kK3MaxTokens and before every global write; with device positions,
-    // before reading them.  launch_dependents comes right after a wait: with
-    // device positions the first one; with host positions that of the last
-    // consumer warp, which waits as soon as the prologue is done (the other
-    // warps go on; every thread waits before the global writes in any case,
-    // so even a CTA that counts as signalling only when it exits does so
-    // after a wait).
+    // pos - guard and before every global write; with device positions, before
+    // reading them.  Every CTA passes a wait before it exits.
     if constexpr (!kDevPos) {
+        if constexpr (kTableRope) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         prologue();
     } else {
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -457,10 +455,6 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
 
     } else {
         // ------------------------------------------------------------ consumers
-        if (!kDevPos && warp == NW - 1) {
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        }
         // A fragments of q' (row r = lane / 4 of the 16-row tile; padding rows zero).
         const int hrow = lane >> 2, q4 = lane & 3;
         const int trow = TPS == 1 ? 0 : hrow / HPC;  // the row's token
@@ -804,6 +798,62 @@ int k3_cluster_capacity(int D, int HPC, int S, bool multi) {
     return slot > 0 ? slot : 0;
 }
 
+template <typename Kern>
+static int occupancy_k(Kern kern, int smem) {
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, (kK3ConsumerWarps + 1) * 32, smem) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return n;
+}
+
+template <int D>
+static int max_occupancy_d() {
+    const int v[] = {
+        occupancy_k(k3_decode_kernel<D, 1, false>, K3Shape<D, 1>::kSmemBytes),
+        occupancy_k(k3_decode_kernel<D, 2, false>, K3Shape<D, 2>::kSmemBytes),
+        occupancy_k(k3_decode_kernel<D, 4, false>, K3Shape<D, 4>::kSmemBytes),
+        occupancy_k(k3_decode_kernel<D, 1, true>, K3Shape<D, 1>::kSmemBytes),
+        occupancy_k(k3_decode_kernel<D, 2, true>, K3Shape<D, 2>::kSmemBytes),
+        occupancy_k(k3_decode_kernel<D, 4, true>, K3Shape<D, 4>::kSmemBytes),
+        occupancy_k(k3_multi_kernel<D, 1, 8>, K3Shape<D, 8>::kSmemBytes),
+        occupancy_k(k3_multi_kernel<D, 2, 4>, K3Shape<D, 8>::kSmemBytes),
+        occupancy_k(k3_multi_kernel<D, 4, 2>, K3Shape<D, 8>::kSmemBytes)};
+    int best = 0;
+    for (int x : v) {
+        if (x < 0) return -1;
+        best = std::max(best, x);
+    }
+    return best;
+}
+
+int k3_max_resident_ctas() {
+    constexpr int kDev = 64;
+    static int cache[kDev] = {};
+    static std::mutex mu;
+    int dev = 0;
+    int sms = 0, per_sm_limit = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&per_sm_limit, cudaDevAttrMaxBlocksPerMultiprocessor, dev) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return 1 << 20;
+    }
+    if (dev >= kDev) return sms * per_sm_limit;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        const int a = max_occupancy_d<64>(), b = max_occupancy_d<128>();
+        // a failed query falls back to the architectural limit of CTAs per SM
+        const int per_sm = (a < 0 || b < 0) ? per_sm_limit : std::max(std::max(a, b), 1);
+        cache[dev] = sms * per_sm;
+    }
+    return cache[dev];
+}
+
 int k3_choose_splits(int D, int HPC, int groups, int pos_max, bool multi) {
     const int nchunks = (pos_max + kK3Chunk - 1) / kK3Chunk;
     int best = 1;
@@ -1054,6 +1104,7 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     bp.dev_pos = 0;
     bp.seq_cnt = nullptr;
     bp.window = 0;
+    bp.guard = 0;  // launched without overlap: the previous kernel has finished
     bp.B = batch;
     bp.Hq = g.n_q_heads;
     bp.Hkv = g.n_kv_heads;

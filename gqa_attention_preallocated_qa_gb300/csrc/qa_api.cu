@@ -11,8 +11,10 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <deque>
 #include <mutex>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "qa.h"
@@ -43,6 +45,76 @@ struct qa_cache {
 };
 
 namespace {
+
+// ---------------------------------------------------------------- launch ordering
+// Decode-family launches with host positions (qa_decode_step, short chunks of
+// qa_prefill) signal their dependents at kernel start (programmatic dependent
+// launch), and every one of their CTAs waits for the previous kernel before it
+// exits, so a launch that has finished implies that its predecessor has.  When
+// launch X starts, the launches that may still run are N, N-1, ..., N-k (N
+// the one just before X) where all CTAs of N-k+1..N were resident together
+// with a CTA of N-k: the walk back stops where that would exceed the CTAs the
+// device can hold, at a launch that signals only after its wait (device
+// positions: nothing before it still runs), or at a kernel that never signals
+// (the prefill kernels, reset, the allocation-free step; the stream
+// synchronised: nothing before the next launch still runs).  X loads only
+// after its own wait the cache rows such launches append to its layer: at
+// most the sum of their new tokens per sequence, just below X's first slot.
+class LaunchTracker {
+  public:
+    int admit(cudaStream_t s, const qa_cache *cache, int layer, int ctas, int tmax, bool early,
+              int resident_max) {
+        std::lock_guard<std::mutex> lock(mu_);
+        Hist &h = hist_[s];
+        int64_t guard = 0, resident = 0;
+        bool bounded = false;
+        for (auto it = h.recs.rbegin(); it != h.recs.rend(); ++it) {
+            if (it->cache == cache && it->layer == layer) guard += it->tmax;
+            if (!it->early) {
+                bounded = true;
+                break;
+            }
+            resident += it->ctas;
+            if (resident + 1 > resident_max) {
+                bounded = true;
+                break;
+            }
+        }
+        if (!bounded && h.truncated) guard = qa::kK3GuardAll;  // older launches unknown
+        h.recs.push_back({cache, layer, ctas, tmax, early});
+        if (h.recs.size() > kCap) {
+            h.recs.pop_front();
+            h.truncated = true;
+        }
+        return static_cast<int>(std::min<int64_t>(guard, qa::kK3GuardAll));
+    }
+    // A kernel that never signals early was enqueued on s, or s was synchronised.
+    void barrier(cudaStream_t s) {
+        std::lock_guard<std::mutex> lock(mu_);
+        auto it = hist_.find(s);
+        if (it != hist_.end()) hist_.erase(it);
+    }
+    // The device was synchronised.
+    void clear() {
+        std::lock_guard<std::mutex> lock(mu_);
+        hist_.clear();
+    }
+
+  private:
+    struct Rec {
+        const qa_cache *cache;
+        int layer, ctas, tmax;
+        bool early;
+    };
+    struct Hist {
+        std::deque<Rec> recs;
+        bool truncated = false;
+    };
+    static constexpr size_t kCap = size_t(1) << 14;
+    std::mutex mu_;
+    std::unordered_map<cudaStream_t, Hist> hist_;
+};
+LaunchTracker g_order;
 
 __global__ void qa_reset_kernel(int32_t *lens, int n_lens, uint32_t *seq_cnt, int n_seq) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_lens; i += gridDim.x * blockDim.x)
@@ -232,6 +304,7 @@ qa_status run_k1(qa_cache *c, int layer, int batch, const int32_t *lens, const v
         p.T = p.cu[n];
         if (p.T > 0) {
             if (qa::launch_k1(p, D, s) != cudaSuccess) return QA_ERR_CUDA;
+            g_order.barrier(s);
             c->launches[QA_KERNEL_NORM_ROPE_APPEND]++;
         }
         row0 += p.T;
@@ -307,7 +380,12 @@ qa_status run_multi(qa_cache *c, int layer, int batch, const int32_t *lens, int 
         row += lens[b];
     }
     flush();
-    for (const auto &l : launches) {
+    const int resident_max = qa::k3_max_resident_ctas();
+    for (auto &l : launches) {
+        int tm = 0;
+        for (int z = 0; z < l.first.B; ++z) tm = std::max(tm, l.second.ntok[z]);
+        l.first.guard = g_order.admit(s, c, layer, l.first.S * g.n_kv_heads * l.first.HG * l.first.B,
+                                      tm, true, resident_max);
         if (qa::launch_k3_multi(l.first, l.second, g.head_dim, HPC, s) != cudaSuccess)
             return QA_ERR_CUDA;
         c->launches[QA_KERNEL_DECODE_ATTN]++;
@@ -411,6 +489,7 @@ QA_API qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out) {
 QA_API qa_status qa_cache_free(qa_cache *c) {
     if (!c) return QA_OK;
     cudaDeviceSynchronize();
+    g_order.clear();
     free_all(c);
     delete c;
     return QA_OK;
@@ -423,6 +502,7 @@ QA_API qa_status qa_cache_reset(qa_cache *c, void *stream) {
     qa_reset_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(c->lens_dev, n_lens,
                                                                        c->seq_cnt, g.max_batch);
     if (cudaGetLastError() != cudaSuccess) return QA_ERR_CUDA;
+    g_order.barrier(static_cast<cudaStream_t>(stream));
     c->launches[QA_KERNEL_RESET]++;
     std::fill(c->lens_host.begin(), c->lens_host.end(), 0);
     return QA_OK;
@@ -518,6 +598,7 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
     if (st != QA_OK) return st;
     for (size_t i = 0; i < k2s.size(); ++i) {
         if (qa::launch_k2(k2s[i], D, k2_items[i], s) != cudaSuccess) return QA_ERR_CUDA;
+        g_order.barrier(s);
         c->launches[QA_KERNEL_PREFILL_ATTN]++;
     }
     for (int b = 0; b < batch; ++b)
@@ -569,6 +650,9 @@ qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const vo
         p.b0 = b0;
         p.B = nb;
         p.S = choose_splits(c, nb, pos_max);
+        p.guard = g_order.admit(static_cast<cudaStream_t>(stream), c, layer,
+                                p.S * g.n_kv_heads * c->HG * nb, 1, !dev_pos,
+                                qa::k3_max_resident_ctas());
         if (qa::launch_k3(p, g.head_dim, c->HPC, static_cast<cudaStream_t>(stream)) != cudaSuccess)
             return QA_ERR_CUDA;
         c->launches[QA_KERNEL_DECODE_ATTN]++;
@@ -606,6 +690,7 @@ QA_API qa_status qa_cache_sync_lengths(qa_cache *c, int layer, void *stream) {
                         sizeof(int32_t) * g.max_batch, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return QA_ERR_CUDA;
+    g_order.barrier(s);
     return QA_OK;
 }
 
@@ -636,6 +721,7 @@ QA_API qa_status qa_cache_set_lengths(qa_cache *c, int layer, const int32_t *len
                         sizeof(int32_t) * g.max_batch, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return QA_ERR_CUDA;
+    g_order.barrier(s);
     std::copy(lens_host, lens_host + g.max_batch,
               c->lens_host.begin() + static_cast<size_t>(layer) * g.max_batch);
     return QA_OK;
@@ -655,6 +741,7 @@ QA_API qa_status qa_get_device_error(qa_cache *c, uint32_t *detail) {
         cudaMemcpy(&word, c->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
         cudaMemset(c->err, 0, sizeof(word)) != cudaSuccess)
         return QA_ERR_CUDA;
+    g_order.clear();
     if (detail) *detail = word;
     switch (word & 0xffu) {
         case 0: return QA_OK;

@@ -66,6 +66,8 @@ constexpr int kK3MaxSeqPerLaunch = 64;  // positions carried in one launch's par
 // New tokens per sequence of one launch of the decode kernel family (1 for a
 // decode step, up to this many for a short chunk such as a verify step).
 constexpr int kK3MaxTokens = 8;
+// guard value meaning "every cache row may still be written: load all after the wait"
+constexpr int kK3GuardAll = 1 << 30;
 
 struct K3Params {
     const CUtensorMap *tm_k, *tm_v;  // (D, capacity, max_batch * Hkv) over this layer's K / V
@@ -82,6 +84,8 @@ struct K3Params {
     int b0;                          // first sequence of this launch (blockIdx.z = b - b0)
     int window;                      // attention window in keys (0: the whole cache)
     int dev_pos;                     // 1: positions are the device lengths (pos unused)
+    int guard;                       // rows just below each sequence's first new slot that
+                                     // a launch still running may write (loaded after the wait)
     uint32_t *seq_cnt;               // [max_batch] groups done per sequence (dev_pos only)
     int pos[kK3MaxSeqPerLaunch];     // slot of each launched sequence's (first) new token
 };
@@ -118,4 +122,7 @@ int k3_cluster_capacity(int D, int HPC, int S, bool multi);
 // Largest split count (<= kK3MaxSplits, <= chunks) whose `groups` clusters all
 // fit on the device at once.
 int k3_choose_splits(int D, int HPC, int groups, int pos_max, bool multi);
+// Upper bound on the CTAs of the decode kernel family resident at once on the
+// current device (SMs x the largest per-SM occupancy of any of its kernels).
+int k3_max_resident_ctas();
 }  // namespace qa

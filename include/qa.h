@@ -138,11 +138,15 @@ qa_status qa_prefill(qa_cache *cache, int layer, int batch, const int32_t *promp
  * previous kernel on the stream (programmatic dependent launch): the step
  * reads q, k, v and the weights before that kernel has finished, so they must
  * not be written by the immediately preceding decode step or short chunk (its
- * out buffer in particular must not be this step's q, k or v).  Each launch
- * lets the next one start only after its own wait for the previous kernel, so
- * at most that one kernel is still running; the cache rows it can be writing
- * (at most 8 per sequence, just below this step's position) are read only
- * after this step's wait.
+ * out buffer in particular must not be this step's q, k or v).  A launch
+ * lets the next one start at once, and each of its thread blocks waits for
+ * the previous kernel before it exits; the library tracks, per stream, the
+ * launches that can still be running when a new one starts (bounded by the
+ * thread blocks the device holds at once) and makes the new launch read the
+ * cache rows they append to its layer only after its wait.  Kernels of other
+ * code enqueued between these calls on the same stream must not let their
+ * successors start before they themselves have waited for their predecessor
+ * (the usual use of programmatic dependent launch).
  * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (a sequence already holds
  * `capacity` tokens; nothing is evicted or wrapped). */
 qa_status qa_decode_step(qa_cache *cache, int layer, int batch,
