@@ -11,14 +11,15 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
-#include <deque>
 #include <mutex>
 #include <new>
-#include <unordered_map>
 #include <vector>
 
+#include "launch_order.h"
 #include "qa.h"
 #include "qa_internal.h"
+
+static_assert(qa::LaunchOrder::kGuardAll == qa::kK3GuardAll, "one guard value for 'all rows'");
 
 #define QA_API extern "C" __attribute__((visibility("default")))
 
@@ -46,75 +47,9 @@ struct qa_cache {
 
 namespace {
 
-// ---------------------------------------------------------------- launch ordering
-// Decode-family launches with host positions (qa_decode_step, short chunks of
-// qa_prefill) signal their dependents at kernel start (programmatic dependent
-// launch), and every one of their CTAs waits for the previous kernel before it
-// exits, so a launch that has finished implies that its predecessor has.  When
-// launch X starts, the launches that may still run are N, N-1, ..., N-k (N
-// the one just before X) where all CTAs of N-k+1..N were resident together
-// with a CTA of N-k: the walk back stops where that would exceed the CTAs the
-// device can hold, at a launch that signals only after its wait (device
-// positions: nothing before it still runs), or at a kernel that never signals
-// (the prefill kernels, reset, the allocation-free step; the stream
-// synchronised: nothing before the next launch still runs).  X loads only
-// after its own wait the cache rows such launches append to its layer: at
-// most the sum of their new tokens per sequence, just below X's first slot.
-class LaunchTracker {
-  public:
-    int admit(cudaStream_t s, const qa_cache *cache, int layer, int ctas, int tmax, bool early,
-              int resident_max) {
-        std::lock_guard<std::mutex> lock(mu_);
-        Hist &h = hist_[s];
-        int64_t guard = 0, resident = 0;
-        bool bounded = false;
-        for (auto it = h.recs.rbegin(); it != h.recs.rend(); ++it) {
-            if (it->cache == cache && it->layer == layer) guard += it->tmax;
-            if (!it->early) {
-                bounded = true;
-                break;
-            }
-            resident += it->ctas;
-            if (resident + 1 > resident_max) {
-                bounded = true;
-                break;
-            }
-        }
-        if (!bounded && h.truncated) guard = qa::kK3GuardAll;  // older launches unknown
-        h.recs.push_back({cache, layer, ctas, tmax, early});
-        if (h.recs.size() > kCap) {
-            h.recs.pop_front();
-            h.truncated = true;
-        }
-        return static_cast<int>(std::min<int64_t>(guard, qa::kK3GuardAll));
-    }
-    // A kernel that never signals early was enqueued on s, or s was synchronised.
-    void barrier(cudaStream_t s) {
-        std::lock_guard<std::mutex> lock(mu_);
-        auto it = hist_.find(s);
-        if (it != hist_.end()) hist_.erase(it);
-    }
-    // The device was synchronised.
-    void clear() {
-        std::lock_guard<std::mutex> lock(mu_);
-        hist_.clear();
-    }
-
-  private:
-    struct Rec {
-        const qa_cache *cache;
-        int layer, ctas, tmax;
-        bool early;
-    };
-    struct Hist {
-        std::deque<Rec> recs;
-        bool truncated = false;
-    };
-    static constexpr size_t kCap = size_t(1) << 14;
-    std::mutex mu_;
-    std::unordered_map<cudaStream_t, Hist> hist_;
-};
-LaunchTracker g_order;
+// Launch ordering of the decode kernel family (launch_order.h): one record of
+// recent launches per stream, shared by every cache of the process.
+qa::LaunchOrder g_order;
 
 __global__ void qa_reset_kernel(int32_t *lens, int n_lens, uint32_t *seq_cnt, int n_seq) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_lens; i += gridDim.x * blockDim.x)
