@@ -399,8 +399,8 @@ def kernel_source_digest(kernel: str) -> str:
     device headers it includes."""
     import hashlib
     csrc = os.path.join(ROOT, "gqa_attention_preallocated_qa_gb300", "csrc")
-    src = {"k3_decode": "k3_decode_splitkv.cu", "k2_prefill": "k2_prefill_tcgen05.cu",
-           "k1_norm": "k1_norm_rope_append.cu"}[kernel]
+    src = {"k3_decode": "k3_decode_splitkv.cu", "k3_multi": "k3_decode_splitkv.cu",
+           "k2_prefill": "k2_prefill_tcgen05.cu", "k1_norm": "k1_norm_rope_append.cu"}[kernel]
     h = hashlib.sha256()
     for name in (src, "qa_device.cuh", "qa_internal.h"):
         with open(os.path.join(csrc, name), "rb") as fh:
@@ -738,8 +738,10 @@ def run_window(args):
 
 
 def run_profile_case(args):
-    """A short program for ncu: one reset + prefill and four decode steps of the
-    benchmark workload (B=4, prompt 2048), nothing else on the device."""
+    """A short program for ncu: one reset + prefill, four decode steps and one
+    verify call of four tokens per sequence (the decode kernel's multi-token
+    form) on the benchmark workload (B=4, prompt 2048), nothing else on the
+    device; all of it twice."""
     import numpy as np
     import torch
 
@@ -759,6 +761,11 @@ def run_profile_case(args):
             dq, dk, dv = dev(inp.dq[s]), dev(inp.dk[s]), dev(inp.dv[s])
             o = torch.empty_like(dq)
             qa.qa_decode_step(h, 0, w.B, dq, dk, dv, wq, wk, o)
+        # tokens 4..7 of every sequence in one call, packed sequence by sequence
+        vq, vk, vv = (dev(np.ascontiguousarray(a[4:8].transpose(1, 0, 2, 3)).reshape(
+            w.B * 4, *a.shape[2:])) for a in (inp.dq, inp.dk, inp.dv))
+        vo = torch.empty_like(vq)
+        qa.qa_prefill(h, 0, [4] * w.B, vq, vk, vv, wq, wk, vo)
     torch.cuda.synchronize()
     st, word = qa.qa_get_device_error(h)
     qa.qa_cache_free(h)
