@@ -54,6 +54,7 @@ SIGNATURES = {
                                                      _vp, _vp, _vp, _vp]),
     "qa_cache_sync_lengths": (ctypes.c_int, [_vp, ctypes.c_int, _vp]),
     "qa_cache_set_window": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int]),
+    "qa_cache_set_decode_overlap": (ctypes.c_int, [_vp, ctypes.c_int]),
     "qa_cache_view": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                      ctypes.POINTER(_vp), _i64p]),
     "qa_cache_set_lengths": (ctypes.c_int, [_vp, ctypes.c_int, _i32p, _vp]),
@@ -168,6 +169,10 @@ def qa_decode_step_device_lengths(cache, layer, batch, q, k, v, q_norm_w, k_norm
 
 def qa_cache_set_window(cache, layer, window) -> None:
     _check(lib.qa_cache_set_window(cache, layer, window), "qa_cache_set_window")
+
+
+def qa_cache_set_decode_overlap(cache, launches) -> None:
+    _check(lib.qa_cache_set_decode_overlap(cache, launches), "qa_cache_set_decode_overlap")
 
 
 def qa_cache_sync_lengths(cache, layer, stream=None) -> None:

@@ -854,11 +854,12 @@ int k3_max_resident_ctas() {
     return cache[dev];
 }
 
-int k3_choose_splits(int D, int HPC, int groups, int pos_max, bool multi) {
+int k3_choose_splits(int D, int HPC, int groups, int pos_max, bool multi, int overlap) {
     const int nchunks = (pos_max + kK3Chunk - 1) / kK3Chunk;
+    const int64_t need = static_cast<int64_t>(std::max(overlap, 1)) * groups;
     int best = 1;
     for (int S = 2; S <= std::min(kK3MaxSplits, std::max(1, nchunks)); ++S)
-        if (k3_cluster_capacity(D, HPC, S, multi) >= groups) best = S;
+        if (k3_cluster_capacity(D, HPC, S, multi) >= need) best = S;
     return best;
 }
 
@@ -1068,7 +1069,8 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     if (st != QA_OK) return st;
 
     // Split plan as in qa_decode_step (the variant has the same resources).
-    const int S = k3_choose_splits(D, HPC, groups, pos_max, false);
+    // (launched without overlap: the clusters of one step are enough)
+    const int S = k3_choose_splits(D, HPC, groups, pos_max, false, 1);
 
     K3NoAllocParams p{};
     if (!encode_decode_map(&p.tmk, k_cache, D, g.capacity, g.max_batch * g.n_kv_heads) ||

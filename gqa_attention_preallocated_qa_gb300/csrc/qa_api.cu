@@ -39,6 +39,7 @@ struct qa_cache {
     uint32_t *err = nullptr;
     uint32_t *seq_cnt = nullptr;  // decode with device lengths: groups done per sequence
     std::vector<int> window;      // per layer: attention window in keys (0: full)
+    int overlap = 2;              // decode launches whose clusters the split plan fits at once
     CUtensorMap *dmaps = nullptr;  // device: [layer][K, V] decode tensor maps
     std::vector<int32_t> lens_host;
     uint64_t kv_bytes = 0, scratch_bytes = 0;
@@ -159,9 +160,10 @@ bool qa::encode_decode_map(CUtensorMap *m, void *base, int D, int capacity, int 
 
 namespace {
 
-int choose_splits(const qa_cache *c, int batch, int pos_max) {
+// overlap: launches whose clusters should fit at once (see qa_cache_set_decode_overlap).
+int choose_splits(const qa_cache *c, int batch, int pos_max, int overlap) {
     return qa::k3_choose_splits(c->cfg.head_dim, c->HPC, batch * c->cfg.n_kv_heads * c->HG,
-                                pos_max, false);
+                                pos_max, false, overlap);
 }
 
 // Validation shared by qa_prefill and qa_prefill_transform.
@@ -298,7 +300,8 @@ qa_status run_multi(qa_cache *c, int layer, int batch, const int32_t *lens, int 
     auto flush = [&]() {
         if (nz == 0) return;
         p.B = nz;
-        p.S = qa::k3_choose_splits(g.head_dim, HPC, nz * g.n_kv_heads * p.HG, pos_max, true);
+        p.S = qa::k3_choose_splits(g.head_dim, HPC, nz * g.n_kv_heads * p.HG, pos_max, true,
+                                   c->overlap);
         launches.emplace_back(p, m);
         nz = 0;
         pos_max = 0;
@@ -547,7 +550,7 @@ QA_API int qa_decode_splits(qa_cache *c, int layer, int batch) {
     int pos_max = 0;
     for (int b = 0; b < batch; ++b)
         pos_max = std::max(pos_max, c->lens_host[static_cast<size_t>(layer) * c->cfg.max_batch + b]);
-    return choose_splits(c, batch, pos_max);
+    return choose_splits(c, batch, pos_max, c->overlap);
 }
 
 namespace {
@@ -584,7 +587,9 @@ qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const vo
         }
         p.b0 = b0;
         p.B = nb;
-        p.S = choose_splits(c, nb, pos_max);
+        // With device positions a launch waits for its predecessor before it
+        // streams anything, so nothing overlaps: plan for one launch.
+        p.S = choose_splits(c, nb, pos_max, dev_pos ? 1 : c->overlap);
         p.guard = g_order.admit(static_cast<cudaStream_t>(stream), c, layer,
                                 p.S * g.n_kv_heads * c->HG * nb, 1, !dev_pos,
                                 qa::k3_max_resident_ctas());
@@ -608,6 +613,12 @@ QA_API qa_status qa_decode_step_device_lengths(qa_cache *c, int layer, int batch
                                                const void *k, const void *v, const void *q_norm_w,
                                                const void *k_norm_w, void *out, void *stream) {
     return decode_step(c, layer, batch, q, k, v, q_norm_w, k_norm_w, out, stream, true);
+}
+
+QA_API qa_status qa_cache_set_decode_overlap(qa_cache *c, int launches) {
+    if (!c || launches < 1 || launches > 8) return QA_ERR_INVALID_ARG;
+    c->overlap = launches;
+    return QA_OK;
 }
 
 QA_API qa_status qa_cache_set_window(qa_cache *c, int layer, int window) {

@@ -193,8 +193,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // before it are visible to all CTAs of the cluster after it.
 // Split cluster barrier: arrive (releasing this thread's earlier writes, e.g.
 // mbarrier initialisation) and, later, wait for every thread of the cluster.
+// Relaxed: the only state peers need before they push into this CTA is its
+// mbarrier initialisation, which fence.mbarrier_init.release.cluster orders
+// before this arrive.
 __device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");

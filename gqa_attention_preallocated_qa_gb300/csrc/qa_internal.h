@@ -119,9 +119,9 @@ cudaError_t launch_k3_multi(const K3Params &p, const K3Multi &m, int D, int HPC,
 // be resident at once on the current device (cached per device, head_dim,
 // form, heads per CTA and S); 0 on error.
 int k3_cluster_capacity(int D, int HPC, int S, bool multi);
-// Largest split count (<= kK3MaxSplits, <= chunks) whose `groups` clusters all
-// fit on the device at once.
-int k3_choose_splits(int D, int HPC, int groups, int pos_max, bool multi);
+// Largest split count (<= kK3MaxSplits, <= chunks) such that the clusters of
+// `overlap` launches of `groups` clusters each fit on the device at once.
+int k3_choose_splits(int D, int HPC, int groups, int pos_max, bool multi, int overlap);
 // Upper bound on the CTAs of the decode kernel family resident at once on the
 // current device (SMs x the largest per-SM occupancy of any of its kernels).
 int k3_max_resident_ctas();

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define QA_ABI_VERSION 2
+#define QA_ABI_VERSION 3
 
 typedef enum {
     QA_OK = 0,
@@ -185,6 +185,20 @@ qa_status qa_decode_step_device_lengths(qa_cache *cache, int layer, int batch,
  * Host-side only, takes effect for launches after the call.
  * Errors: INVALID_ARG (no such layer, window < 0). */
 qa_status qa_cache_set_window(qa_cache *cache, int layer, int window);
+
+/* How many consecutive decode-kernel launches (decode steps, short chunks)
+ * the split plan lets run on the device at once.  A launch's split count S
+ * is the largest (<= 16) for which `launches` launches' thread-block
+ * clusters fit together, so that each launch streams its cache while the
+ * next one starts (programmatic dependent launch).  2 (the default) suits
+ * attention launched back to back (a decode loop of attention layers); 1
+ * gives an isolated launch, e.g. one between other kernels, the most splits.
+ * Any value gives the same result up to the summation order of the split
+ * merge.  qa_decode_step_device_lengths, whose launches cannot overlap (they
+ * wait for the previous kernel before reading their positions), always plans
+ * for 1.  Host-side only, takes effect for launches after the call.
+ * Errors: INVALID_ARG (launches outside 1..8). */
+qa_status qa_cache_set_decode_overlap(qa_cache *cache, int launches);
 
 /* Copy one layer's device lengths into the host copy (synchronises `stream`),
  * after decode steps that advanced them on the device. */

@@ -202,3 +202,53 @@ def test_back_to_back_steps_equal_synchronised_steps(qa):
         np.testing.assert_array_equal(a, b, err_msg=f"call {i} ({plan[i]})")
     np.testing.assert_array_equal(Ka, Kb)
     np.testing.assert_array_equal(Va, Vb)
+
+
+def test_decode_overlap_changes_splits_not_results(qa, oracle_mod):
+    """qa_cache_set_decode_overlap only sets how many launches the split plan
+    fits on the device at once: fewer splits for more overlap, and the same
+    attention (every setting within the parity bar of the oracle)."""
+    Hq, Hkv, D, B = 32, 8, 128, 4
+    prompt = (600, 700, 520, 650)
+    steps, cap = 3, 720
+    inp = layer_inputs(167, prompt, Hq, Hkv, D, steps)
+    wq, wk = dev(inp.wq), dev(inp.wk)
+    splits, outs = {}, {}
+    for overlap in (1, 2, 4):
+        c = GpuCache(qa, 1, B, Hq, Hkv, D, cap)
+        try:
+            qa.qa_cache_set_decode_overlap(c.h, overlap)
+            q, k, v = dev(inp.q), dev(inp.k), dev(inp.v)
+            out = torch.empty_like(q)
+            qa.qa_prefill(c.h, 0, list(prompt), q, k, v, wq, wk, out)
+            splits[overlap] = qa.qa_decode_splits(c.h, 0, B)
+            res = []
+            for s in range(steps):
+                o = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+                qa.qa_decode_step(c.h, 0, B, dev(inp.dq[s]), dev(inp.dk[s]), dev(inp.dv[s]), wq, wk, o)
+                res.append(o)
+            torch.cuda.synchronize()
+            outs[overlap] = np.stack([f64(o) for o in res])
+            with pytest.raises(qa.QaError):
+                qa.qa_cache_set_decode_overlap(c.h, 0)
+            with pytest.raises(qa.QaError):
+                qa.qa_cache_set_decode_overlap(c.h, 9)
+            assert c.device_error() == (0, 0)
+        finally:
+            c.free()
+    assert splits[1] > splits[4] >= 1 and splits[1] >= splits[2] >= splits[4]
+    orc = ChunkOracle(oracle_mod, B, Hq, Hkv, D, cap, inp.wq, inp.wk)
+    t0 = 0
+    for b, L in enumerate(prompt):
+        orc.append(b, F(inp.k[t0:t0 + L]), F(inp.v[t0:t0 + L]))
+        t0 += L
+    want = []
+    for s in range(steps):
+        row = []
+        for b in range(B):
+            orc.append(b, F(inp.dk[s][b][None]), F(inp.dv[s][b][None]))
+            row.append([orc.out_row(b, orc.lens[b] - 1, h, F(inp.dq[s][b, h])) for h in (0, 9, 22, 31)])
+        want.append(row)
+    want = np.array(want)
+    for overlap, got in outs.items():
+        assert_parity(got[:, :, (0, 9, 22, 31)], want, f"overlap {overlap}")
