@@ -35,6 +35,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -772,30 +773,46 @@ static int cluster_capacity_t(int S, bool multi) {
     return cluster_capacity_k(k3_multi_kernel<D, HPC, 8 / HPC>, K3Shape<D, 8>::kSmemBytes, S);
 }
 
-int k3_cluster_capacity(int D, int HPC, int S, bool multi) {
+// Per device, head_dim, form and heads per CTA: the capacity for every S,
+// queried once ([S], 0 = query failed).  The table is filled under the lock and
+// never changes afterwards, so callers read it without locking.
+static const int *capacity_table(int D, int HPC, bool multi) {
     constexpr int kDev = 16;
-    // [device][D == 128][multi][HPC 1/2/4][S]: 0 = not queried yet, -1 = query failed
-    static int cache[kDev][2][2][3][kK3MaxSplits + 1] = {};
+    struct Table {
+        std::atomic<bool> ready{false};
+        int cap[kK3MaxSplits + 1] = {};
+    };
+    static Table tables[kDev][2][2][3];
     static std::mutex mu;
     int dev = 0;
-    if (S < 1 || S > kK3MaxSplits || cudaGetDevice(&dev) != cudaSuccess || dev >= kDev) return 0;
-    if ((D != 64 && D != 128) || (HPC != 1 && HPC != 2 && HPC != 4)) return 0;
-    const int di = D == 128 ? 1 : 0, hi = HPC == 4 ? 2 : (HPC == 2 ? 1 : 0);
-    std::lock_guard<std::mutex> lock(mu);
-    int &slot = cache[dev][di][multi ? 1 : 0][hi][S];
-    if (slot == 0) {
-        int n = 0;
-        if (D == 128)
-            n = HPC == 4 ? cluster_capacity_t<128, 4>(S, multi)
-                         : (HPC == 2 ? cluster_capacity_t<128, 2>(S, multi)
-                                     : cluster_capacity_t<128, 1>(S, multi));
-        else
-            n = HPC == 4 ? cluster_capacity_t<64, 4>(S, multi)
-                         : (HPC == 2 ? cluster_capacity_t<64, 2>(S, multi)
-                                     : cluster_capacity_t<64, 1>(S, multi));
-        slot = n > 0 ? n : -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDev) return nullptr;
+    if ((D != 64 && D != 128) || (HPC != 1 && HPC != 2 && HPC != 4)) return nullptr;
+    Table &t = tables[dev][D == 128 ? 1 : 0][multi ? 1 : 0][HPC == 4 ? 2 : (HPC == 2 ? 1 : 0)];
+    if (!t.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!t.ready.load(std::memory_order_relaxed)) {
+            for (int S = 1; S <= kK3MaxSplits; ++S) {
+                int n = 0;
+                if (D == 128)
+                    n = HPC == 4 ? cluster_capacity_t<128, 4>(S, multi)
+                                 : (HPC == 2 ? cluster_capacity_t<128, 2>(S, multi)
+                                             : cluster_capacity_t<128, 1>(S, multi));
+                else
+                    n = HPC == 4 ? cluster_capacity_t<64, 4>(S, multi)
+                                 : (HPC == 2 ? cluster_capacity_t<64, 2>(S, multi)
+                                             : cluster_capacity_t<64, 1>(S, multi));
+                t.cap[S] = n > 0 ? n : 0;
+            }
+            t.ready.store(true, std::memory_order_release);
+        }
     }
-    return slot > 0 ? slot : 0;
+    return t.cap;
+}
+
+int k3_cluster_capacity(int D, int HPC, int S, bool multi) {
+    if (S < 1 || S > kK3MaxSplits) return 0;
+    const int *cap = capacity_table(D, HPC, multi);
+    return cap ? cap[S] : 0;
 }
 
 template <typename Kern>
@@ -832,12 +849,19 @@ static int max_occupancy_d() {
 
 int k3_max_resident_ctas() {
     constexpr int kDev = 64;
-    static int cache[kDev] = {};
+    static std::atomic<int> cache[kDev] = {};
     static std::mutex mu;
     int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return 1 << 20;
+    }
+    if (dev < kDev) {
+        const int known = cache[dev].load(std::memory_order_acquire);
+        if (known > 0) return known;
+    }
     int sms = 0, per_sm_limit = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&per_sm_limit, cudaDevAttrMaxBlocksPerMultiprocessor, dev) !=
             cudaSuccess) {
         cudaGetLastError();
@@ -845,21 +869,23 @@ int k3_max_resident_ctas() {
     }
     if (dev >= kDev) return sms * per_sm_limit;
     std::lock_guard<std::mutex> lock(mu);
-    if (cache[dev] == 0) {
+    if (cache[dev].load(std::memory_order_relaxed) == 0) {
         const int a = max_occupancy_d<64>(), b = max_occupancy_d<128>();
         // a failed query falls back to the architectural limit of CTAs per SM
         const int per_sm = (a < 0 || b < 0) ? per_sm_limit : std::max(std::max(a, b), 1);
-        cache[dev] = sms * per_sm;
+        cache[dev].store(sms * per_sm, std::memory_order_release);
     }
-    return cache[dev];
+    return cache[dev].load(std::memory_order_relaxed);
 }
 
 int k3_choose_splits(int D, int HPC, int groups, int pos_max, bool multi, int overlap) {
     const int nchunks = (pos_max + kK3Chunk - 1) / kK3Chunk;
     const int64_t need = static_cast<int64_t>(std::max(overlap, 1)) * groups;
+    const int *cap = capacity_table(D, HPC, multi);
     int best = 1;
+    if (!cap) return best;
     for (int S = 2; S <= std::min(kK3MaxSplits, std::max(1, nchunks)); ++S)
-        if (k3_cluster_capacity(D, HPC, S, multi) >= need) best = S;
+        if (cap[S] >= need) best = S;
     return best;
 }
 
