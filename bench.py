@@ -341,14 +341,17 @@ def run_e2e(args, qa, h, w, inp, stream):
     inputs (prompt q/k/v, norm weights, the 128 decode tokens' q/k/v) from
     pinned host memory to the device and reads its results (prefill output and
     the 128 decode outputs) back, all inside the timed events.  As a caller
-    would, the step overlaps copies with compute on a second stream: the decode
-    tokens' inputs go up while the prefill runs, and the prefill output comes
-    back while the decode steps run; both streams join before the step ends."""
+    would, the step overlaps copies with compute: the prompt goes up one
+    sequence at a time on an upload stream and each sequence is prefilled (a
+    chunked qa_prefill call for that sequence alone) as soon as its rows have
+    arrived, the decode tokens' inputs follow, and the prefill output comes
+    back on a download stream while the decode steps run; all streams join
+    before the step's end event."""
     import numpy as np
     import torch
     lib = qa.lib
     sh = stream.cuda_stream
-    side = torch.cuda.Stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
 
     def flat(*arrays):
         return np.concatenate([np.ascontiguousarray(a).reshape(-1) for a in arrays])
@@ -357,9 +360,8 @@ def run_e2e(args, qa, h, w, inp, stream):
     host_in = torch.from_numpy(flat(*parts).view(np.int16)).view(torch.bfloat16).pin_memory()
     dev_in = torch.empty_like(host_in, device="cuda")
     sizes = [a.size for a in parts]
-    offs = np.concatenate([[0], np.cumsum(sizes)])
-    n_pre = int(offs[5])  # prompt q, k, v and the weights; then the decode tokens
-    ptr = [dev_in.data_ptr() + 2 * int(o) for o in offs[:-1]]
+    offs = [int(o) for o in np.concatenate([[0], np.cumsum(sizes)])]
+    ptr = [dev_in.data_ptr() + 2 * o for o in offs[:-1]]
     q_p, k_p, v_p, wq_p, wk_p, dq_p, dk_p, dv_p = ptr
     step_q, step_kv = w.B * w.Hq * w.D * 2, w.B * w.Hkv * w.D * 2
     T = w.T
@@ -369,29 +371,55 @@ def run_e2e(args, qa, h, w, inp, stream):
     host_out = torch.empty(dev_out.shape, dtype=torch.bfloat16).pin_memory()
     out_p = dev_out.data_ptr()
     dout_p = out_p + n_out_pre * 2
-    lens_arr = qa._i32(w.prompt_lens)
+    cu = [0]
+    for L in w.prompt_lens:
+        cu.append(cu[-1] + L)
+    qrow, kvrow = w.Hq * w.D, w.Hkv * w.D  # elements per token
+    lens_one = []
+    for b in range(w.B):
+        lens_one.append(qa._i32([w.prompt_lens[i] if i == b else 0 for i in range(w.B)]))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
+    def copy_rows(dst, src, base, row, a, b):
+        dst[base + a * row:base + b * row].copy_(src[base + a * row:base + b * row], non_blocking=True)
+
     def step():
-        side.wait_stream(stream)  # nothing of this step starts before the step's start event
-        with torch.cuda.stream(side):
-            dev_in[n_pre:].copy_(host_in[n_pre:], non_blocking=True)
+        up.wait_stream(stream)  # nothing of this step starts before the step's start event
+        down.wait_stream(stream)
+        arrived = []
+        with torch.cuda.stream(up):
+            copy_rows(dev_in, host_in, offs[3], 1, 0, offs[5] - offs[3])  # norm weights
+            for b in range(w.B):
+                a, e = cu[b], cu[b + 1]
+                copy_rows(dev_in, host_in, offs[0], qrow, a, e)
+                copy_rows(dev_in, host_in, offs[1], kvrow, a, e)
+                copy_rows(dev_in, host_in, offs[2], kvrow, a, e)
+                ev = torch.cuda.Event()
+                ev.record(up)
+                arrived.append(ev)
+            dev_in[offs[5]:].copy_(host_in[offs[5]:], non_blocking=True)  # decode tokens
             dec_in = torch.cuda.Event()
-            dec_in.record(side)
-        dev_in[:n_pre].copy_(host_in[:n_pre], non_blocking=True)
+            dec_in.record(up)
         st = lib.qa_cache_reset(h, sh)
-        st |= lib.qa_prefill(h, 0, w.B, lens_arr, q_p, k_p, v_p, wq_p, wk_p, out_p, sh)
-        pre_done = torch.cuda.Event()
-        pre_done.record(stream)
-        with torch.cuda.stream(side):
-            side.wait_event(pre_done)
+        for b in range(w.B):
+            a = cu[b]
+            stream.wait_event(arrived[b])
+            st |= lib.qa_prefill(h, 0, w.B, lens_one[b], q_p + 2 * a * qrow, k_p + 2 * a * kvrow,
+                                 v_p + 2 * a * kvrow, wq_p, wk_p, out_p + 2 * a * qrow, sh)
+        # the prefill output goes down once the uploads are done (the two directions
+        # share the link's bandwidth), while the decode steps run
+        done = torch.cuda.Event()
+        done.record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(done)
             host_out[:n_out_pre].copy_(dev_out[:n_out_pre], non_blocking=True)
         stream.wait_event(dec_in)
         for s in range(w.steps):
             st |= lib.qa_decode_step(h, 0, w.B, dq_p + s * step_q, dk_p + s * step_kv,
                                      dv_p + s * step_kv, wq_p, wk_p, dout_p + s * step_q, sh)
         host_out[n_out_pre:].copy_(dev_out[n_out_pre:], non_blocking=True)
-        stream.wait_stream(side)  # the prefill output is back before the step's end event
+        stream.wait_stream(up)
+        stream.wait_stream(down)  # every prefill output is back before the step's end event
         if st:
             raise RuntimeError(f"qa call failed with status {st}")
 
@@ -410,7 +438,8 @@ def run_e2e(args, qa, h, w, inp, stream):
     ms = sum(a.elapsed_time(b) for a, b in evs) / n
     return {"value": round(ms * 1e3, 2), "unit": UNIT, "h2d_bytes_per_step": host_in.numel() * 2,
             "d2h_bytes_per_step": host_out.numel() * 2, "steps": n, "host_buffers": "pinned",
-            "copies": "decode inputs up during the prefill, prefill output down during the decode steps"}
+            "copies": "prompt up one sequence at a time, each prefilled as it arrives; prefill "
+                      "output down during the decode steps"}
 
 
 def kernel_source_digest(kernel: str) -> str:
