@@ -444,15 +444,20 @@ def run_e2e(args, qa, h, w, inp, stream):
 
 def kernel_source_digest(kernel: str) -> str:
     """sha256 (first 16 hex digits) over the kernel's source file and the
-    device headers it includes."""
+    device headers it includes, with comments and whitespace removed (a
+    comment edit does not change the kernel the counters were taken on)."""
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "gqa_attention_preallocated_qa_gb300", "csrc")
     src = {"k3_decode": "k3_decode_splitkv.cu", "k3_multi": "k3_decode_splitkv.cu",
            "k2_prefill": "k2_prefill_tcgen05.cu", "k1_norm": "k1_norm_rope_append.cu"}[kernel]
     h = hashlib.sha256()
     for name in (src, "qa_device.cuh", "qa_internal.h"):
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, name)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

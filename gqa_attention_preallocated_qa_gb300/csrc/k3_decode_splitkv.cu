@@ -1,34 +1,40 @@
-// k3_decode_splitkv.cu -- K3: one fused launch per decode step of one layer.
+// k3_decode_splitkv.cu -- K3: one fused launch per decode step of one layer
+// (and, in its multi-token form, per short chunk of up to 8 new tokens per
+// sequence, such as the verify step of speculative decoding).
 //
 // For every (sequence b, kv head, head group, split) CTA:
-//   1. take pos, the slot of the new token: from the launch parameters (the
-//      cache's exact host copy of the lengths), or, in the variant built for
-//      CUDA-graph capture, from the device lengths,
-//   2. RMSNorm + RoPE the HPC (<= 4) query heads of the group at pos, rounded
-//      to bf16 like the prefill path, staged in shared memory,
-//   3. the CTA owning the last split also norms + rotates k, appends k' and v
-//      to cache slot pos and attends to that new key in registers,
+//   1. take pos, the slot of the (first) new token: from the launch parameters
+//      (the cache's exact host copy of the lengths), or, in the variant built
+//      for CUDA-graph capture, from the device lengths,
+//   2. RMSNorm + RoPE the CTA's query rows (HPC <= 4 heads of the group, times
+//      the new tokens in the multi-token form; at most 8 rows) at their
+//      positions, rounded to bf16 like the prefill path, staged in shared memory,
+//   3. the CTA owning the last split also norms + rotates the new tokens' k,
+//      appends k' and v to their cache slots and attends to those new keys in
+//      registers (token t sees new tokens 0..t),
 //   4. stream its share of cache keys [0, pos) (or the attention window's part
 //      of them) in 32-key chunks through a ring of shared-memory stages filled
 //      by TMA tensor copies (128-byte swizzle, evict-first L2 policy), one
-//      stage per consumer warp; all query heads of the group share every load,
+//      stage per consumer warp; all query rows of the CTA share every load,
 //   5. per chunk and warp: S = q' K^T and O += P V as warp-level bf16 MMAs
-//      (m16n8k16, fp32 accumulate; the 4 heads of a group fill rows 0-3 of the
-//      16-row tile, so the tile's unused rows cost tensor time, not memory),
-//      online softmax in fp32 on the score fragments, P reused in registers as
-//      the A operand of P V,
+//      (m16n8k16, fp32 accumulate; the query rows fill rows 0-7 of the 16-row
+//      tile, so the tile's unused rows cost tensor time, not memory), online
+//      softmax in fp32 on the score fragments, P reused in registers as the A
+//      operand of P V,
 //   6. the S split CTAs of a group form one thread-block cluster: each CTA
 //      combines its consumer warps' partials in shared memory and pushes the
 //      result (m, l, o) with st.async straight into the shared memory of the
 //      CTA that owns each run of outputs, counted on that CTA's receive
 //      mbarrier; each owner merges the S partials of its run in a fixed order
-//      (deterministic) and writes out[b][h] in bf16; the
-//      length of b becomes pos + 1 (written by one CTA, or, with device
-//      lengths, by the last group of the sequence through a counter).
-// With programmatic dependent launch the step overlaps the previous kernel on
-// the stream: it waits for it only before loading the chunk holding row
-// pos - 1 (the only cache row a previous decode step of the layer writes) and
-// before its global writes.
+//      (deterministic) and writes the outputs in bf16; the length of b grows by
+//      the new tokens (written by one CTA, or, with device lengths, by the last
+//      group of the sequence through a counter).
+// With programmatic dependent launch consecutive launches run side by side:
+// a launch signals the next at its start and waits for the previous kernel
+// only before loading the cache rows that a launch possibly still running
+// appends to its layer (the host passes their number) and before its global
+// writes.  The host plans the split count so that two launches' clusters fit
+// on the device at once.
 // This serves the decode step of the dryft-flash-infer agent guide ("Where the
 // wins are": per-step overhead is the largest cost at batch 1 and 4, so the
 // step is one launch) against the preallocated cache of the same section.
