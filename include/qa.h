@@ -242,9 +242,10 @@ qa_status qa_stats(qa_cache *cache, uint64_t launches[QA_NUM_KERNELS]);
  * rotary table, error word). */
 qa_status qa_memory_info(qa_cache *cache, uint64_t *kv_bytes, uint64_t *scratch_bytes);
 
-/* Number of key-range splits the decode kernel will use for the current
- * lengths of `layer` and `batch` sequences (a pure host computation; a step
- * launches one kernel per 64 sequences, and this is the first one's count). */
+/* Number of key-range splits qa_decode_step will use for the current
+ * lengths of `layer` and `batch` sequences under the cache's overlap setting
+ * (qa_cache_set_decode_overlap; a pure host computation; a step launches one
+ * kernel per 64 sequences, and this is the first one's count). */
 int qa_decode_splits(qa_cache *cache, int layer, int batch);
 
 /* ---- allocation-free decode step ----------------------------------------
