@@ -252,3 +252,23 @@ def test_decode_overlap_changes_splits_not_results(qa, oracle_mod):
     want = np.array(want)
     for overlap, got in outs.items():
         assert_parity(got[:, :, (0, 9, 22, 31)], want, f"overlap {overlap}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,chunks", [
+    (16, 2, 128, [(40, 9), (3, 8), (2, 1), (1, 4)]),    # G = 8: two head groups per kv head
+    (4, 2, 64, [(20, 33), (5, 3), (8, 8), (2, 0)]),     # G = 2
+])
+def test_short_chunks_other_groupings(qa, oracle_mod, Hq, Hkv, D, chunks):
+    run_chunks(qa, oracle_mod, chunks, Hq, Hkv, D, 80, seed=173 + Hq, decode_steps=2,
+               heads=tuple(range(Hq)), rows_per_chunk=8)
+
+
+def test_short_chunks_over_64_sequences(qa, oracle_mod):
+    """More sequences than one launch carries: several multi-token launches in
+    one call (and sequences without new tokens skipped)."""
+    B = 80
+    rng = np.random.default_rng(179)
+    prompt = tuple(int(x) for x in rng.integers(1, 40, size=B))
+    short = tuple(0 if i % 10 == 3 else 1 + i % 3 for i in range(B))  # 72 sequences with tokens
+    run_chunks(qa, oracle_mod, [prompt, short], 2, 1, 64, 48, seed=181, decode_steps=1,
+               heads=(0, 1), rows_per_chunk=3)
