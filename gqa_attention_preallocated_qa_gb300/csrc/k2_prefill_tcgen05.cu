@@ -31,6 +31,8 @@
 // block at its window's first tile.
 // Every mbarrier wait is bounded (qa_device.cuh): a stuck pipeline records a
 // timeout in the error word and the CTA still frees its TMEM and exits.
+#include <atomic>
+
 #include "qa_device.cuh"
 
 namespace qa {
@@ -434,14 +436,14 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 template <int D, bool kWindow>
 static cudaError_t launch_k2_t(const K2Params &p, int nitems, cudaStream_t stream) {
     constexpr int smem = K2Layout<D>::kSmemBytes;
-    static int configured_mask = 0;  // one bit per device
+    static std::atomic<unsigned> configured{0u};  // devices 0..31 set up (one bit each)
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 31 && !(configured_mask & (1 << dev))) {
+    if (dev >= 32 || !((configured.load(std::memory_order_acquire) >> dev) & 1u)) {
         cudaError_t e = cudaFuncSetAttribute(k2_prefill_kernel<D, kWindow>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        configured_mask |= 1 << dev;
+        if (dev < 32) configured.fetch_or(1u << dev, std::memory_order_release);
     }
     k2_prefill_kernel<D, kWindow><<<nitems, kK2Threads, smem, stream>>>(p);
     return cudaGetLastError();

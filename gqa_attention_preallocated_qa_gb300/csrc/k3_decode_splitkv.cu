@@ -716,17 +716,17 @@ __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
 template <int D, int HPC, bool kDevPos>
 static cudaError_t launch_k3_t(const K3Params &p, cudaStream_t stream) {
     constexpr int smem = K3Shape<D, HPC>::kSmemBytes;
-    static int configured_mask = 0;  // one bit per device
+    static std::atomic<unsigned> configured{0u};  // devices 0..31 set up (one bit each)
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 31 && !(configured_mask & (1 << dev))) {
+    if (dev >= 32 || !((configured.load(std::memory_order_acquire) >> dev) & 1u)) {
         cudaError_t e = cudaFuncSetAttribute(k3_decode_kernel<D, HPC, kDevPos>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k3_decode_kernel<D, HPC, kDevPos>,
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
-        configured_mask |= 1 << dev;
+        if (dev < 32) configured.fetch_or(1u << dev, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.S, p.Hkv * p.HG, p.B);
@@ -918,14 +918,14 @@ static cudaError_t launch_k3_multi_t(const K3MultiParams &p, cudaStream_t stream
     constexpr int TPS = 8 / HPC;
     constexpr int smem = K3Shape<D, 8>::kSmemBytes;
     auto kern = k3_multi_kernel<D, HPC, TPS>;
-    static int configured_mask = 0;  // one bit per device
+    static std::atomic<unsigned> configured{0u};  // devices 0..31 set up (one bit each)
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 31 && !(configured_mask & (1 << dev))) {
+    if (dev >= 32 || !((configured.load(std::memory_order_acquire) >> dev) & 1u)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
-        configured_mask |= 1 << dev;
+        if (dev < 32) configured.fetch_or(1u << dev, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.base.S, p.base.Hkv * p.base.HG, p.base.B);
