@@ -8,14 +8,17 @@
 // affordable", same guide, "Numerics").
 //
 // One CTA = one 128-row block of a sequence's new tokens (a whole prompt, or a
-// chunk appended after the tokens the layer already holds) for TWO query heads
-// of the same kv head (GQA: both share every K/V tile).  Warp roles (320 threads):
-//   warps 0-3  softmax warpgroup 0 (query head h0): thread r owns row r
-//   warps 4-7  softmax warpgroup 1 (query head h1)
-//   warp  8    TMA producer: Q0/Q1 once, then K_j, V_j tiles into a ring
-//   warp  9    tcgen05 issuer (one thread) and TMEM owner
-// Tensor memory (512 columns x 128 lanes, fp32):
-//   [0,128) S0/P0   [128,256) S1/P1   [256,256+D) O0   [256+D,256+2D) O1
+// chunk appended after the tokens the layer already holds) for NT query heads
+// of one kv head (kK2HeadsPerCta: 1 by default, so that two CTAs share an SM
+// and one's prologue and epilogue overlap the other's main loop; with 2, both
+// heads share every K/V tile).  Warp roles (NT * 128 + 64 threads):
+//   warps 0-3        softmax warpgroup 0 (query head h0): thread r owns row r
+//   warps 4-7        softmax warpgroup 1 (query head h1; NT = 2 only)
+//   warp  4*NT       TMA producer: Q once, then K_j, V_j tiles into a ring
+//   warp  4*NT + 1   tcgen05 issuer (one thread) and TMEM owner
+// Tensor memory (NT * 256 columns x 128 lanes, fp32):
+//   NT = 1: [0,128) S0/P0   [128,128+D) O0
+//   NT = 2: [0,128) S0/P0   [128,256) S1/P1   [256,256+D) O0   [256+D,256+2D) O1
 // S_t = Q_t K_j^T (both operands K-major, 128-byte swizzled smem); the softmax
 // threads read their row of S_t with tcgen05.ld, compute p = 2^(s*c - m*c) in
 // fp32, write P as bf16 over the first 64 columns of S_t, rescale O_t when the
@@ -37,16 +40,20 @@
 
 namespace qa {
 
-template <int D>
+// NT = query heads (128-row tiles) per CTA.
+template <int D, int NT>
 struct K2Layout {
     static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 64 bf16
     static constexpr int kBoxes = D / 64;
     static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D
-    static constexpr int kStages = (D == 128) ? 4 : 6;
-    static constexpr int kQBytes = 2 * kTileBytes;
+    // two CTAs per SM with one tile each: Q + 2 K/V stages fit twice
+    static constexpr int kStages = NT == 2 ? ((D == 128) ? 4 : 6) : ((D == 128) ? 2 : 4);
+    static constexpr int kQBytes = NT * kTileBytes;
     static constexpr int kSmemBytes = kQBytes + kStages * kTileBytes + 1024;  // + alignment slack
-    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
-    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = NT * 128, kColO1 = NT * 128 + D;
+    static constexpr uint32_t kTmemCols = NT == 2 ? 512 : 256;
+    static constexpr int kThreads = NT * 128 + 64;  // softmax warpgroups, TMA warp, MMA warp
+    static constexpr int kTmaWarp = 4 * NT, kMmaWarp = 4 * NT + 1;
 };
 
 // max(a, b, c) in one instruction (NaN inputs are ignored, as by fmaxf).
@@ -97,10 +104,10 @@ __device__ __forceinline__ bool k2_decode_item(const K2Params &p, int idx, int &
     return false;
 }
 
-template <int D, bool kWindow>
-__global__ void __launch_bounds__(kK2Threads, 1)
+template <int D, bool kWindow, int NT>
+__global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
     k2_prefill_kernel(const __grid_constant__ K2Params p) {
-    using Lay = K2Layout<D>;
+    using Lay = K2Layout<D, NT>;
     constexpr int NS = Lay::kStages;
     const unsigned FULL = 0xffffffffu;
 
@@ -118,8 +125,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int b = 0, kvh = 0, pair = 0, qb = 0;
     if (!k2_decode_item(p, blockIdx.x, b, kvh, pair, qb)) return;  // uniform per CTA
-    const bool two = 2 * pair + 1 < p.G;
-    const int h0 = kvh * p.G + 2 * pair;
+    const bool two = NT == 2 && 2 * pair + 1 < p.G;
+    const int h0 = kvh * p.G + NT * pair;
     const int L = p.len[b];
     // Query row r of the block is new token qb*128 + r at position qmin + r; it
     // sees keys 0..qmin + r, or with an attention window of W keys
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             mbar_init(smem_u32(&bar_kv_full[s]), 1);
             mbar_init(smem_u32(&bar_kv_empty[s]), 1);
         }
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < NT; ++t) {
             mbar_init(smem_u32(&bar_s[t]), 1);
             mbar_init(smem_u32(&bar_p[t]), 128);
             mbar_init(smem_u32(&bar_pv[t]), 1);
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         s_abort = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == Lay::kMmaWarp) {
         tmem_alloc(smem_u32(&s_tmem), Lay::kTmemCols);
         tmem_relinquish();
     }
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (warp == 8) {
+    if (warp == Lay::kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&p.tm_q);
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 mbar_wait(smem_u32(&bar_kv_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2, 2);
             mbar_wait(bq, 0, &dummy, p.err, kKernK2, 3);
         }
-    } else if (warp == 9) {
+    } else if (warp == Lay::kMmaWarp) {
         // ------------------------------------------------------------ tcgen05 issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
@@ -207,7 +214,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 return (base & 0xFFFFFFFF00000000ull) |
                        static_cast<uint32_t>(static_cast<uint32_t>(base) + (byte_off >> 4));
             };
-            const uint64_t dQ[2] = {sdesc_sw128(sQ, 16, 1024), sdesc_sw128(sQ + Lay::kTileBytes, 16, 1024)};
+            const uint64_t dQ[2] = {sdesc_sw128(sQ, 16, 1024),
+                                    sdesc_sw128(sQ + (NT - 1) * Lay::kTileBytes, 16, 1024)};
             auto issue_s = [&](int t, int st) {
                 const uint64_t dK = sdesc_sw128(sKV + st * Lay::kTileBytes, 16, 1024);
 #pragma unroll
@@ -427,7 +435,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == Lay::kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, Lay::kTmemCols);
     }
@@ -435,17 +443,19 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 
 template <int D, bool kWindow>
 static cudaError_t launch_k2_t(const K2Params &p, int nitems, cudaStream_t stream) {
-    constexpr int smem = K2Layout<D>::kSmemBytes;
+    constexpr int NT = kK2HeadsPerCta;
+    using Lay = K2Layout<D, NT>;
+    constexpr int smem = Lay::kSmemBytes;
     static std::atomic<unsigned> configured{0u};  // devices 0..31 set up (one bit each)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 32 || !((configured.load(std::memory_order_acquire) >> dev) & 1u)) {
-        cudaError_t e = cudaFuncSetAttribute(k2_prefill_kernel<D, kWindow>,
+        cudaError_t e = cudaFuncSetAttribute(k2_prefill_kernel<D, kWindow, NT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (dev < 32) configured.fetch_or(1u << dev, std::memory_order_release);
     }
-    k2_prefill_kernel<D, kWindow><<<nitems, kK2Threads, smem, stream>>>(p);
+    k2_prefill_kernel<D, kWindow, NT><<<nitems, Lay::kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

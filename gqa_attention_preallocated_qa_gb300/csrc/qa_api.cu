@@ -518,7 +518,7 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
             p.Hq = g.n_q_heads;
             p.Hkv = g.n_kv_heads;
             p.G = c->G;
-            p.npairs = (c->G + 1) / 2;
+            p.npairs = (c->G + qa::kK2HeadsPerCta - 1) / qa::kK2HeadsPerCta;
             p.max_qblocks = maxqb;
             p.window = c->window[layer];
             p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));

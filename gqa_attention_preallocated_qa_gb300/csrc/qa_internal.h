@@ -39,7 +39,15 @@ struct K1Params {
 };
 
 // ---------------------------------------------------------------- K2
-constexpr int kK2Threads = 320;   // 2 softmax warpgroups, 1 TMA warp, 1 MMA warp
+// Query heads (128-row tiles) per prefill CTA: 1 (two CTAs per SM, each with
+// one softmax warpgroup, a TMA warp and an MMA warp; the default: one CTA's
+// per-block prologue and epilogue overlap the other's main loop) or 2 (one CTA
+// per SM; the two heads share every K/V tile).
+#ifndef QA_K2_HEADS_PER_CTA
+#define QA_K2_HEADS_PER_CTA 1
+#endif
+constexpr int kK2HeadsPerCta = QA_K2_HEADS_PER_CTA;
+static_assert(kK2HeadsPerCta == 1 || kK2HeadsPerCta == 2, "one or two query heads per CTA");
 constexpr int kK2BlockM = 128;    // query rows per tile
 constexpr int kK2BlockN = 128;    // keys per tile
 
@@ -49,7 +57,7 @@ struct alignas(64) K2Params {
     CUtensorMap tm_v[kMaxSeqPerLaunch];
     __nv_bfloat16 *out;                       // [T][Hq][D]
     uint32_t *err;
-    int nseq, Hq, Hkv, G, npairs;             // npairs: query-head pairs per kv head
+    int nseq, Hq, Hkv, G, npairs;             // npairs: CTAs (head tiles) per kv head and block
     int len[kMaxSeqPerLaunch];                // new tokens of each sequence
     int start[kMaxSeqPerLaunch];              // position of each sequence's first new token
     int cu[kMaxSeqPerLaunch];                 // first row of each sequence in q'/out
