@@ -86,6 +86,13 @@ def test_null_cache_is_rejected_everywhere(qa):
     assert qa.lib.qa_stats(None, None) == 1
     assert qa.lib.qa_memory_info(None, None, None) == 1
     assert qa.lib.qa_decode_splits(None, 0, 1) == 0
+    assert qa.lib.qa_decode_step_device_lengths(None, 0, 1, 16, 16, 16, 16, 16, 16, None) == 1
+    assert qa.lib.qa_cache_sync_lengths(None, 0, None) == 1
+    assert qa.lib.qa_cache_set_window(None, 0, 16) == 1
+    assert qa.lib.qa_cache_set_decode_overlap(None, 2) == 1
+    assert qa.lib.qa_cache_view(None, 0, None, None, None, None) == 1
+    pos = (ctypes.c_int32 * 1)(0)
+    assert qa.lib.qa_decode_step_noalloc(None, 1, pos, 16, 16, 16, 16, 16, 16, 16, 16, None) == 1
 
 
 def test_valid_alloc_without_a_device_reports_cuda_error(qa):
