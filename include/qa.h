@@ -2,9 +2,10 @@
  * qa.h -- C ABI of the GB300 (sm_103a) attention hot path of a greedy
  * Qwen3-style decoder: per-head QK-RMSNorm + rotary embedding + KV-cache
  * append, causal grouped-query prefill attention (whole prompts or chunks
- * appended to what a layer holds, which also serves multi-token verify
- * queries) and single-token decode attention against a preallocated bf16 KV
- * cache, with an optional per-layer attention window.
+ * appended to what a layer holds; chunks of up to 8 tokens per sequence, such
+ * as multi-token verify queries, run in the decode kernel's multi-token form)
+ * and decode attention against a preallocated bf16 KV cache, with an optional
+ * per-layer attention window.
  *
  * The arguments follow the pages' statement of the problem: a batch of
  * prompts with their lengths, one new token per sequence per decode step,
@@ -57,7 +58,8 @@ typedef enum {
 enum {
     QA_KERNEL_NORM_ROPE_APPEND = 0, /* K1: fused QK-RMSNorm + RoPE + cache append (prefill rows) */
     QA_KERNEL_PREFILL_ATTN = 1,     /* K2: causal GQA flash attention, TMA + tcgen05 */
-    QA_KERNEL_DECODE_ATTN = 2,      /* K3: fused norm/RoPE/append + split-KV decode + LSE merge */
+    QA_KERNEL_DECODE_ATTN = 2,      /* K3: fused norm/RoPE/append + split-KV decode + LSE merge
+                                       (decode steps and short-chunk prefills) */
     QA_KERNEL_RESET = 3,            /* cache-length reset */
     QA_NUM_KERNELS = 4
 };
