@@ -282,20 +282,60 @@ def run_ours(args):
     dec_gbs = dec_bytes / w.steps / (dec_us_per_step * 1e-6) / 1e9
     dec_share = sum(dec_ms) / total_ms
 
+    # K1 and K2 alone (the two halves of a prefill call), L2 flushed before each
+    k1_us, k2_us = time_prefill_halves(args, qa, h, w, P, lens_arr, flush, stream)
+    k1_bytes = w.T * (w.Hq + 2 * w.Hkv) * w.D * 2 * 2  # each row read once, written once
+    k1_gbs = k1_bytes / (k1_us * 1e-6) / 1e9
+    k2_tflops = flops / (k2_us * 1e-6) / 1e12
+
     # e2e through the public API with host buffers (pinned), copies inside the timed region
     e2e = run_e2e(args, qa, h, w, inp, stream)
+    qa.qa_cache_free(h)
 
-    roof_dec = {"bound": "hbm", "kernel": "k3_decode_kernel<128,4>", "achieved": round(dec_gbs, 1),
-                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(dec_gbs / pk["hbm_gbs"], 4),
-                "traffic": traffic_for("k3_decode", dec_bytes / w.steps),
-                "per_launch_bytes": round(dec_bytes / w.steps),
-                "duration": "decode span / 128 launches (includes inter-launch gaps)"}
+    # the decode sweep: every step reads its K/V from HBM (layers cycled)
+    with ClockSampler(local) as sweep_clocks:
+        sweep, isolated = decode_sweep(args, pk, args.sweep_steps)
+    cold = next(p for p in sweep if (p["B"], p["L"]) == (4, 2048))
+
+    roof_cold = {"bound": "hbm", "kernel": "k3_decode_kernel<128,4>",
+                 "workload": "decode step, B=4, cache length 2048 (+ growth), HBM-cold: "
+                             f"{cold['layers']} layer caches cycled, {cold['steps']} steps",
+                 "achieved": cold["hbm_gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                 "frac": cold["frac_of_measured_hbm"],
+                 "traffic": traffic_for("k3_decode", cold["kv_bytes_per_step"]),
+                 "traffic_regime": "cold launch, nothing of the cache in L2 (ncu)",
+                 "per_launch_bytes": cold["kv_bytes_per_step"],
+                 "duration": "events around the whole loop / steps (launch gaps included)"}
+    roof_iso = {"bound": "hbm", "kernel": "k3_decode_kernel<128,4>",
+                "workload": "one isolated decode step, B=4, L=2048, HBM-cold",
+                "achieved": isolated["hbm_gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": isolated["frac_of_measured_hbm"], "traffic": None,
+                "per_launch_bytes": isolated["kv_bytes_per_step"],
+                "duration": isolated["how"]}
+    roof_l2 = {"bound": "hbm", "kernel": "k3_decode_kernel<128,4>",
+               "workload": "decode steps of the generate call above, one layer: its 35.7 MB "
+                           "cache stays in the 129 MB L2 (L2-resident, not an HBM figure)",
+               "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+               "frac": round(dec_gbs / pk["hbm_gbs"], 4), "traffic": None,
+               "per_launch_bytes": round(dec_bytes / w.steps),
+               "duration": "decode span / 128 launches (includes inter-launch gaps)"}
+    roof_k1 = {"bound": "hbm", "kernel": "k1_norm_rope_append_kernel<128>",
+               "workload": "qa_prefill_transform, B=4 x 2048 prompt rows",
+               "achieved": round(k1_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+               "frac": round(k1_gbs / pk["hbm_gbs"], 4),
+               "traffic": traffic_for("k1_norm", k1_bytes), "per_launch_bytes": k1_bytes,
+               "duration": "median over launches, L2 flushed before each"}
+    roof_k2 = {"bound": "tensor", "kernel": "k2_prefill_kernel<128>",
+               "workload": "qa_prefill_attend, B=4 x 2048 causal",
+               "achieved": round(k2_tflops, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+               "frac": round(k2_tflops / pk["bf16_tflops"], 4),
+               "traffic": traffic_for("k2_prefill", None), "per_launch_flops": flops,
+               "duration": "median over launches, L2 flushed before each"}
     roof_pre = {"bound": "tensor", "kernel": "k1 + k2_prefill_kernel<128>",
+                "workload": "qa_prefill call (K1 + K2), B=4 x 2048",
                 "achieved": round(pre_tflops, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(pre_tflops / pk["bf16_tflops"], 4),
-                "traffic": traffic_for("k2_prefill", None), "per_launch_flops": flops,
-                "duration": "prefill call (K1 + K2) span"}
-    dominant = roof_dec if dec_share >= 0.5 else roof_pre
+                "frac": round(pre_tflops / pk["bf16_tflops"], 4), "traffic": None,
+                "per_launch_flops": flops, "duration": "prefill call (K1 + K2) span"}
     rev, dirty = git_rev()
     line = {
         "metric": METRIC, "value": round(job_us, 2), "unit": UNIT,
@@ -313,13 +353,22 @@ def run_ours(args):
             "prefill_attn_us": round(pre_us, 2),
             "prefill_attn_tflops": round(pre_tflops, 1),
             "prefill_frac_of_measured_bf16": round(pre_tflops / pk["bf16_tflops"], 4),
+            "decode_l2_resident": "the single-layer decode figures above: the layer's 35.7 MB "
+                                  "cache stays in L2 (see decode_sweep for HBM-cold steps)",
+            "k1_append_us": round(k1_us, 2), "k1_append_hbm_gbs": round(k1_gbs, 1),
+            "k1_frac_of_measured_hbm": round(k1_gbs / pk["hbm_gbs"], 4),
+            "k2_prefill_attn_us": round(k2_us, 2), "k2_prefill_attn_tflops": round(k2_tflops, 1),
+            "k2_frac_of_measured_bf16": round(k2_tflops / pk["bf16_tflops"], 4),
             "decode_time_share": round(dec_share, 4),
             "step_ms_p50": round(statistics.median(step_ms), 4),
             "step_ms_spread": round((max(step_ms) - min(step_ms)) / statistics.median(step_ms), 4),
+            "decode_sweep": sweep,
+            "decode_sweep_clocks": sweep_clocks.summary(),
+            "decode_isolated": isolated,
             "peaks": pk["source"],
         },
-        "roofline": dominant,
-        "roofline_all": [roof_dec, roof_pre],
+        "roofline": roof_cold,
+        "roofline_all": [roof_cold, roof_iso, roof_l2, roof_k1, roof_k2, roof_pre],
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
@@ -336,12 +385,45 @@ def run_ours(args):
                                 "cores": 1, "kind": "oracle",
                                 "sample": model.desc + f"; {len(ests)} samples, {spent:.1f} s",
                                 "host_cpus": os.cpu_count()}
-    qa.qa_cache_free(h)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def time_prefill_halves(args, qa, h, w, P, lens_arr, flush, stream, reps=10):
+    """Median µs of K1 alone (qa_prefill_transform) and of K2 alone
+    (qa_prefill_attend over the rows K1 just appended), each launch after an
+    L2 flush, on the generate call's prompt."""
+    import torch
+    lib = qa.lib
+    sh = stream.cuda_stream
+    qp = torch.empty((w.T, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    out2 = torch.empty_like(qp)
+    t1, t2 = [], []
+    for i in range(reps + 3):
+        lib.qa_cache_reset(h, sh)
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        st = lib.qa_prefill_transform(h, 0, w.B, lens_arr, P["q"], P["k"], P["v"], P["wq"],
+                                      P["wk"], qp.data_ptr(), sh)
+        b.record(stream)
+        flush.zero_()
+        c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c.record(stream)
+        st |= lib.qa_prefill_attend(h, 0, w.B, lens_arr, qp.data_ptr(), out2.data_ptr(), sh)
+        d.record(stream)
+        torch.cuda.synchronize()
+        if st:
+            raise RuntimeError(f"prefill halves failed with status {st}")
+        if i >= 3:
+            t1.append(a.elapsed_time(b) * 1e3)
+            t2.append(c.elapsed_time(d) * 1e3)
+    if qa.qa_get_device_error(h)[0]:
+        raise RuntimeError("device error while timing the prefill halves")
+    return statistics.median(t1), statistics.median(t2)
 
 
 def run_e2e(args, qa, h, w, inp, stream):
@@ -484,35 +566,39 @@ def traffic_for(kernel: str, algorithmic_bytes):
 
 
 # ---------------------------------------------------------------- decode sweep
-def run_sweep(args):
+def decode_sweep(args, pk, steps, isolated_steps=200):
     """Decode-only sweep (batch 1 and 4, cache lengths 512 to 16384).  Each
     point allocates NL layer caches, NL large enough that together they hold
     at least 3x the L2 (129 MB), every one filled with L raw N(0,1) keys/values
-    per sequence; the timed `--sweep-steps` decode steps cycle through the
-    layers (step s decodes layer s mod NL, as a model's layer loop does), so
-    each step reads its layer's K/V from HBM, not from L2.  The length of a
-    layer grows by one per visit; bytes are counted exactly.  One JSON line per
-    point: mean µs per step, K/V bytes per step and HBM GB/s (events around the
-    whole loop: launch gaps included); `same_layer_us_per_step` repeats the
-    measurement on a single layer (its cache can stay in L2 when small)."""
+    per sequence; the `steps` timed decode steps cycle through the layers (step
+    s decodes layer s mod NL, as a model's layer loop does), so each step reads
+    its layer's K/V from HBM, not from L2.  The length of a layer grows by one
+    per visit; bytes are counted exactly.  Per point: mean µs per step, K/V
+    bytes per step and HBM GB/s (events around the whole loop: launch gaps
+    included); `same_layer_us_per_step` repeats the measurement on a single
+    layer (its cache can stay in L2 when small).  At B = 4, L = 2048 the point
+    also times `isolated_steps` steps one by one: split plan for one launch at
+    a time, a spacer kernel before each (so no launch overlaps the previous
+    decode launch) and events around each launch."""
     import numpy as np
     import torch
 
     from gqa_attention_preallocated_qa_gb300 import binding as qa
     from gqa_attention_preallocated_qa_gb300.configs import DECODE_SWEEP
 
-    pk = peaks()
     l2_bytes = 129 * 1000 * 1000
-    steps = args.sweep_steps
 
     def dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
 
+    points = []
+    isolated = None
     for pt in DECODE_SWEEP:
         inp = pt.inputs()
         layer_bytes = pt.B * pt.Hkv * pt.L * pt.D * 4
         NL = max(1, min(256, -(-3 * l2_bytes // layer_bytes)))
-        visits = -(-(steps + args.warmup) // NL) + args.warmup + 1
+        iso = isolated_steps if (pt.B, pt.L) == (4, 2048) else 0
+        visits = -(-(steps + args.warmup + iso) // NL) + args.warmup + 1
         same_steps = 200
         cap = pt.L + visits + same_steps
         h = qa.qa_cache_alloc(NL, pt.B, pt.Hq, pt.Hkv, pt.D, cap, pt.theta, pt.eps)
@@ -522,6 +608,7 @@ def run_sweep(args):
             K[:, :, :pt.L] = ck
             V[:, :, :pt.L] = cv
             qa.qa_cache_set_lengths(h, layer, [pt.L] * pt.B)
+        del ck, cv
         q, k, v, wq, wk = (dev(a) for a in (inp.dq[0], inp.dk[0], inp.dv[0], inp.wq, inp.wk))
         out = torch.empty_like(q)
         stream = torch.cuda.current_stream()
@@ -551,6 +638,33 @@ def run_sweep(args):
         us = e0.elapsed_time(e1) * 1e3 / steps
         byts /= steps
         gbs = byts / (us * 1e-6) / 1e9
+        if iso:
+            qa.qa_cache_set_decode_overlap(h, 1)
+            iso_splits = qa.qa_decode_splits(h, 0, pt.B)
+            spacer = torch.zeros(1, device="cuda")
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(iso)]
+            ib = 0
+            for i in range(iso):
+                layer = (args.warmup + steps + i) % NL
+                spacer.add_(1.0)  # a plain kernel: this launch cannot overlap a decode launch
+                evs[i][0].record(stream)
+                st |= lib.qa_decode_step(h, layer, pt.B, *args_c, sh)
+                evs[i][1].record(stream)
+                lens[layer] += 1
+                ib += pt.B * pt.Hkv * lens[layer] * pt.D * 4
+            torch.cuda.synchronize()
+            if st or qa.qa_get_device_error(h)[0]:
+                raise RuntimeError("isolated decode steps failed")
+            iso_us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+            iso_gbs = ib / iso / (iso_us * 1e-6) / 1e9
+            isolated = {"B": pt.B, "L": pt.L, "steps": iso, "splits": iso_splits,
+                        "us_per_step": round(iso_us, 3), "hbm_gbs": round(iso_gbs, 1),
+                        "frac_of_measured_hbm": round(iso_gbs / pk["hbm_gbs"], 4),
+                        "kv_bytes_per_step": round(ib / iso),
+                        "how": "median of per-launch events; a spacer kernel before each launch, "
+                               "layers cycled (HBM-cold), split plan for one launch"}
+            qa.qa_cache_set_decode_overlap(h, 2)
         # the same on one layer, for reference (its K/V may stay in L2)
         n1 = same_steps
         e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -561,13 +675,26 @@ def run_sweep(args):
         torch.cuda.synchronize()
         if st or qa.qa_get_device_error(h)[0]:
             raise RuntimeError(f"decode sweep point {pt.name} failed")
-        print(json.dumps({"sweep": pt.name, "B": pt.B, "L": pt.L, "steps": steps, "layers": NL,
-                          "splits": splits, "us_per_step": round(us, 3),
-                          "kv_bytes_per_step": round(byts), "hbm_gbs": round(gbs, 1),
-                          "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
-                          "same_layer_us_per_step": round(e2.elapsed_time(e3) * 1e3 / max(1, n1), 3),
-                          "same_layer_steps": n1}), flush=True)
+        points.append({"sweep": pt.name, "B": pt.B, "L": pt.L, "steps": steps, "layers": NL,
+                       "splits": splits, "us_per_step": round(us, 3),
+                       "kv_bytes_per_step": round(byts), "hbm_gbs": round(gbs, 1),
+                       "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
+                       "same_layer_us_per_step": round(e2.elapsed_time(e3) * 1e3 / max(1, n1), 3)})
         qa.qa_cache_free(h)
+        del inp
+    return points, isolated
+
+
+def run_sweep(args):
+    """`--sweep`: the decode sweep alone, one JSON line per point (and one for
+    the isolated step), with the clocks seen while it ran."""
+    pk = peaks()
+    with ClockSampler(0) as clocks:
+        points, isolated = decode_sweep(args, pk, args.sweep_steps)
+    for p in points:
+        print(json.dumps(p), flush=True)
+    print(json.dumps({"isolated_decode": isolated}), flush=True)
+    print(json.dumps({"clocks": clocks.summary()}), flush=True)
 
 
 def run_verify(args):
@@ -844,23 +971,31 @@ def run_reference(args):
         return
     from gqa_attention_preallocated_qa_gb300.configs import QWEN3_4B_B4 as w
     inp = w.inputs()
-    model = OracleStepModel(w, inp, frac_rows=2048)
+    model = OracleStepModel(w, inp, frac_rows=512)
     for _ in range(args.warmup):
         model.sample()
-    ests, spent = [], 0.0
+    ests, spents = [], []
     for _ in range(args.steps):
         est, sp = model.sample()
         ests.append(est)
-        spent += sp
+        spents.append(sp)
     value = statistics.median(ests) * 1e6
+    # Each timed step runs a bounded sample of the generate call; ms_per_step is
+    # the wall time of the sample actually run, `value` the full call it stands
+    # for (the sample scaled up row for row, as the description says).
+    sample_ms = statistics.mean(spents) * 1e3
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value / 1e3, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sample_ms, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": "qwen3_4b_b4_p2048_d128", "step": STEP_DEF, "batch": w.B,
                        "prompt": w.prompt_lens[0], "decode_steps": w.steps, "layers": 1},
+            "extrapolated": {"value_is": "the full generate call, scaled up from each step's "
+                                         "sample", "sample_ms_per_step": round(sample_ms, 3),
+                             "scale": round(value / 1e3 / sample_ms, 1)},
             "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": model.desc + f"; {len(ests)} samples, {spent:.1f} s"},
+                             "sample": model.desc + f"; {len(ests)} samples, "
+                                                    f"{sum(spents):.1f} s"},
             "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

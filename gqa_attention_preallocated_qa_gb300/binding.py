@@ -67,6 +67,9 @@ SIGNATURES = {
     "qa_decode_splits": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int]),
     "qa_decode_step_noalloc": (ctypes.c_int, [ctypes.POINTER(qa_config), ctypes.c_int, _i32p, _vp,
                                               _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "qa_noalloc_get_device_error": (ctypes.c_int, [_u32p, _vp]),
+    "qa_prefill_attend": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, _i32p, _vp, _vp, _vp]),
+    "qa_debug_arm_wait_timeout": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint32]),
     "qa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "qa_abi_version": (ctypes.c_int, []),
 }
@@ -186,6 +189,23 @@ def qa_decode_step_noalloc(cfg: qa_config, positions, k_cache, v_cache, q, k, v,
                                       _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(k), _ptr(v),
                                       _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out), _stream(stream)),
            "qa_decode_step_noalloc")
+
+
+def qa_noalloc_get_device_error(stream=None):
+    """(status, raw error word) of the allocation-free step; reading clears the word."""
+    w = ctypes.c_uint32()
+    st = lib.qa_noalloc_get_device_error(ctypes.byref(w), _stream(stream))
+    return st, w.value
+
+
+def qa_prefill_attend(cache, layer, prompt_lens, qprime, out, stream=None) -> None:
+    _check(lib.qa_prefill_attend(cache, layer, len(prompt_lens), _i32(prompt_lens), _ptr(qprime),
+                                 _ptr(out), _stream(stream)),
+           "qa_prefill_attend")
+
+
+def qa_debug_arm_wait_timeout(kernel: int, wait_us: int) -> None:
+    _check(lib.qa_debug_arm_wait_timeout(kernel, wait_us), "qa_debug_arm_wait_timeout")
 
 
 def qa_cache_view(cache, layer):

@@ -174,13 +174,17 @@ __global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
                 for (int x = 0; x < Lay::kBoxes; ++x)
                     tma_load_3d(sQ + t * Lay::kTileBytes + x * Lay::kBoxBytes, &p.tm_q, x * 64,
                                 h0 + t, row0, bq);
+            // Test hook: CTA 0 withholds the copy of V tile 0 (nothing will complete
+            // that stage's phase), so the MMA warp's wait for it runs out.
+            const int withheld = (p.fault && blockIdx.x == 0) ? 1 : -1;
             int issued = 0;
             for (int idx = 0; idx < 2 * nkv; ++idx, ++issued) {
                 const int st = idx % NS;
                 if (idx >= NS &&
                     !mbar_wait(smem_u32(&bar_kv_empty[st]), ((idx / NS) - 1) & 1, &s_abort, p.err,
-                               kKernK2, 1))
+                               kKernK2, 1, p.wait_ns))
                     break;
+                if (idx == withheld) continue;
                 const uint32_t fb = smem_u32(&bar_kv_full[st]);
                 mbar_expect_tx(fb, Lay::kTileBytes);
                 const CUtensorMap *tm = (idx & 1) ? &p.tm_v[b] : &p.tm_k[b];
@@ -191,8 +195,10 @@ __global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
             // Never leave a copy in flight: bounded wait for the last ones and Q.
             int dummy = 0;
             for (int i = max(0, issued - NS); i < issued; ++i)
-                mbar_wait(smem_u32(&bar_kv_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2, 2);
-            mbar_wait(bq, 0, &dummy, p.err, kKernK2, 3);
+                if (i != withheld)
+                    mbar_wait(smem_u32(&bar_kv_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2,
+                              2, p.wait_ns);
+            mbar_wait(bq, 0, &dummy, p.err, kKernK2, 3, p.wait_ns);
         }
     } else if (warp == Lay::kMmaWarp) {
         // ------------------------------------------------------------ tcgen05 issuer
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
             const uint32_t tS[2] = {tmem + Lay::kColS0, tmem + Lay::kColS1};
             const uint32_t tO[2] = {tmem + Lay::kColO0, tmem + Lay::kColO1};
             const int ntiles = two ? 2 : 1;
-            bool ok = mbar_wait(smem_u32(&bar_q), 0, &s_abort, p.err, kKernK2, 4);
+            bool ok = mbar_wait(smem_u32(&bar_q), 0, &s_abort, p.err, kKernK2, 4, p.wait_ns);
             tc_fence_after();
 
             // S_t = Q_t K^T: K-major A and B, 128-byte swizzle, 8-row groups 1024 B apart;
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
                            (acc || k > 0) ? 1u : 0u);
             };
 
-            if (ok) ok = mbar_wait(smem_u32(&bar_kv_full[0]), 0, &s_abort, p.err, kKernK2, 5);
+            if (ok) ok = mbar_wait(smem_u32(&bar_kv_full[0]), 0, &s_abort, p.err, kKernK2, 5, p.wait_ns);
             if (ok) {
                 tc_fence_after();
                 for (int t = 0; t < ntiles; ++t) {
@@ -256,12 +262,12 @@ __global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
                 const int iv = 2 * j + 1, sv = iv % NS;
                 const int ik = 2 * (j + 1), sk = ik % NS;
                 const bool more = j + 1 < nkv;
-                ok = mbar_wait(smem_u32(&bar_kv_full[sv]), (iv / NS) & 1, &s_abort, p.err, kKernK2, 6);
+                ok = mbar_wait(smem_u32(&bar_kv_full[sv]), (iv / NS) & 1, &s_abort, p.err, kKernK2, 6, p.wait_ns);
                 if (ok && more)
                     ok = mbar_wait(smem_u32(&bar_kv_full[sk]), (ik / NS) & 1, &s_abort, p.err,
-                                   kKernK2, 8);
+                                   kKernK2, 8, p.wait_ns);
                 for (int t = 0; ok && t < ntiles; ++t) {
-                    ok = mbar_wait(smem_u32(&bar_p[t]), j & 1, &s_abort, p.err, kKernK2, 7);
+                    ok = mbar_wait(smem_u32(&bar_p[t]), j & 1, &s_abort, p.err, kKernK2, 7, p.wait_ns);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(t, sv, j > 0);
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
             // Drain: every commit above must have arrived before the CTA exits.
             int dummy = 0;
             for (int i = max(0, committed - NS); i < committed; ++i)
-                mbar_wait(smem_u32(&bar_kv_empty[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2, 10);
+                mbar_wait(smem_u32(&bar_kv_empty[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2, 10, p.wait_ns);
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroups
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
             float mref = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j < nkv; ++j) {
-                ok = mbar_wait(smem_u32(&bar_s[t]), j & 1, &s_abort, p.err, kKernK2, 11);
+                ok = mbar_wait(smem_u32(&bar_s[t]), j & 1, &s_abort, p.err, kKernK2, 11, p.wait_ns);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -403,7 +409,7 @@ __global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
                 mbar_arrive(smem_u32(&bar_p[t]));
             }
             if (ok) {
-                ok = mbar_wait(smem_u32(&bar_pv[t]), 0, &s_abort, p.err, kKernK2, 12);
+                ok = mbar_wait(smem_u32(&bar_pv[t]), 0, &s_abort, p.err, kKernK2, 12, p.wait_ns);
                 ok = __all_sync(FULL, ok);
             }
             if (ok) {

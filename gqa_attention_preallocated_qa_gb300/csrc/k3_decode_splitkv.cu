@@ -311,7 +311,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     // splits in shares that differ by one at most: split `split` streams chunks
     // [c_begin, c_end) and the last split also attends to the new tokens.
     bool pos_ok = false;
-    int c_begin = 0, my_chunks = 0, c_safe = 0, first_round = 0, key_lo = 0;
+    int c_begin = 0, my_chunks = 0, c_safe = 0, first_round = 0, key_lo = 0, withheld = -1;
     auto plan = [&]() {
         pos_ok = pos >= 0 && ntok >= 1 && ntok <= TPS && pos + ntok <= p.cap;
         const int nchunks = pos_ok ? (pos + kK3Chunk - 1) / kK3Chunk : 0;
@@ -327,6 +327,9 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         // chunks wholly below row pos - guard (all of them without a guard)
         c_safe = p.guard <= 0 ? nchunks : (pos > p.guard ? (pos - p.guard) / kK3Chunk : 0);
         first_round = min(NS, my_chunks);
+        // Test hook: the first CTA withholds its first chunk's copy (FaultPlan).
+        withheld = (p.fault && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
+                    my_chunks > 0) ? 0 : -1;
     };
     if (!kDevPos) plan();
     const bool owner = split == S - 1;
@@ -337,6 +340,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     uint64_t policy = 0;
     // Stage `st` receives chunk c: K then V, each D/64 boxes of 32 rows.
     auto issue = [&](int c, int st) {
+        if (c - c_begin == withheld) return;  // nothing completes this stage's phase
         const uint32_t fb = smem_u32(&bar_full[st]);
         mbar_expect_tx(fb, Sh::kStageBytes);
         const uint32_t dk = sRing + st * Sh::kStageBytes;
@@ -445,7 +449,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
                 const int st = issued % NS;
                 if (issued >= NS &&
                     !mbar_wait(smem_u32(&bar_empty[st]), ((issued / NS) - 1) & 1, &s_abort, p.err,
-                               kKernK3, 2))
+                               kKernK3, 2, p.wait_ns))
                     break;
                 if (!waited && c_begin + issued >= c_safe) {  // may hold a previous step's rows
                     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -455,8 +459,9 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             }
             // No copy may land after the CTA exits: wait (bounded) for the last ones.
             for (int i = max(0, issued - NS); i < issued; ++i) {
+                if (i == withheld) continue;
                 int dummy = 0;
-                mbar_wait(smem_u32(&bar_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK3, 3);
+                mbar_wait(smem_u32(&bar_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK3, 3, p.wait_ns);
             }
         }
 
@@ -483,7 +488,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
 
         for (int c = c_begin + warp, i = warp; i < my_chunks; c += NW, i += NW) {
             const int st = i % NS;
-            bool ok = mbar_wait(smem_u32(&bar_full[st]), (i / NS) & 1, &s_abort, p.err, kKernK3, 4);
+            bool ok = mbar_wait(smem_u32(&bar_full[st]), (i / NS) & 1, &s_abort, p.err, kKernK3, 4, p.wait_ns);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             const int base = c * kK3Chunk;
@@ -635,7 +640,14 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + ntok;
     }
     if (E_me > 0) {
-        bool ok = mbar_wait_cluster(smem_u32(&bar_recv), 0, &s_abort, p.err, kKernK3, 5);
+        bool ok = mbar_wait_cluster(smem_u32(&bar_recv), 0, &s_abort, p.err, kKernK3, 5, p.wait_ns);
+        if (!ok) {
+            // Given up (this CTA timed out somewhere): the peers still push their
+            // partials here, so every inbound st.async must land before this CTA
+            // exits and its shared memory goes away.  Bounded like every wait.
+            int dummy = 0;
+            mbar_wait_cluster(smem_u32(&bar_recv), 0, &dummy, p.err, kKernK3, 6, p.wait_ns);
+        }
         ok = __syncthreads_and(ok);
         if (!ok) return;
         if (kDevPos && split == 0 && threadIdx.x == 0) {
@@ -1148,10 +1160,38 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     bp.S = S;
     bp.eps = g.rms_eps;
     bp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    const FaultPlan f = take_fault(QA_KERNEL_DECODE_ATTN);
+    bp.fault = f.fault;
+    bp.wait_ns = f.wait_ns;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: the error word starts at zero.
-    if (cudaMemsetAsync(scr, 0, kNoAllocScratchBytes, s) != cudaSuccess) return QA_ERR_CUDA;
-    if (launch_noalloc(p, D, HPC, s) != cudaSuccess) return QA_ERR_CUDA;
+    // The error word is zero when the library loads and after every read
+    // through qa_noalloc_get_device_error; a call does not clear it, so the
+    // first error of any call since the last read is kept for the caller.
+    if (launch_noalloc(p, D, HPC, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return QA_ERR_CUDA;
     return QA_OK;
+}
+
+extern "C" __attribute__((visibility("default"))) qa_status qa_noalloc_get_device_error(
+    uint32_t *detail, void *stream) {
+    using namespace qa;
+    NoAllocDevice *dev = nullptr;
+    qa_status st = noalloc_setup(dev);
+    if (st != QA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    // A copy into this stack word and a 4-byte memset: neither allocates.
+    if (cudaMemcpyAsync(&word, dev->scratch, sizeof(word), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return QA_ERR_CUDA;
+    if (word != 0 && (cudaMemsetAsync(dev->scratch, 0, sizeof(word), s) != cudaSuccess ||
+                      cudaStreamSynchronize(s) != cudaSuccess))
+        return QA_ERR_CUDA;
+    if (detail) *detail = word;
+    switch (word & 0xffu) {
+        case 0: return QA_OK;
+        case kErrTimeout: return QA_ERR_DEVICE_TIMEOUT;
+        default: return QA_ERR_DEVICE_BOUNDS;
+    }
 }

@@ -52,6 +52,11 @@ namespace {
 // recent launches per stream, shared by every cache of the process.
 qa::LaunchOrder g_order;
 
+// Failure-detection test hook (qa_debug_arm_wait_timeout): the kernel index
+// whose next launch withholds a copy (-1: none) and that launch's wait limit.
+std::atomic<int> g_fault_kernel{-1};
+std::atomic<uint64_t> g_fault_wait_ns{qa::kWaitTimeoutNs};
+
 __global__ void qa_reset_kernel(int32_t *lens, int n_lens, uint32_t *seq_cnt, int n_seq) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_lens; i += gridDim.x * blockDim.x)
         lens[i] = 0;
@@ -143,6 +148,17 @@ bool encode_q_map(CUtensorMap *m, void *base, int D, int Hq, int T) {
 }
 
 }  // namespace
+
+qa::FaultPlan qa::take_fault(int kernel) {
+    FaultPlan f;
+    int armed = kernel;
+    if (g_fault_kernel.load(std::memory_order_acquire) == kernel &&
+        g_fault_kernel.compare_exchange_strong(armed, -1, std::memory_order_acq_rel)) {
+        f.fault = 1;
+        f.wait_ns = g_fault_wait_ns.load(std::memory_order_acquire);
+    }
+    return f;
+}
 
 bool qa::encode_decode_map(CUtensorMap *m, void *base, int D, int capacity, int rows_z) {
     auto enc = get_encode_fn();
@@ -278,6 +294,8 @@ K3Params make_k3(qa_cache *c, int layer, const void *q, const void *k, const voi
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.head_dim)));
     p.seq_cnt = c->seq_cnt;
     p.window = c->window[layer];
+    p.fault = 0;
+    p.wait_ns = qa::kWaitTimeoutNs;
     return p;
 }
 
@@ -324,9 +342,91 @@ qa_status run_multi(qa_cache *c, int layer, int batch, const int32_t *lens, int 
         for (int z = 0; z < l.first.B; ++z) tm = std::max(tm, l.second.ntok[z]);
         l.first.guard = g_order.admit(s, c, layer, l.first.S * g.n_kv_heads * l.first.HG * l.first.B,
                                       tm, true, resident_max);
+        const qa::FaultPlan f = qa::take_fault(QA_KERNEL_DECODE_ATTN);
+        l.first.fault = f.fault;
+        l.first.wait_ns = f.wait_ns;
         if (qa::launch_k3_multi(l.first, l.second, g.head_dim, HPC, s) != cudaSuccess)
             return QA_ERR_CUDA;
         c->launches[QA_KERNEL_DECODE_ATTN]++;
+    }
+    return QA_OK;
+}
+
+// One prefill-attention launch (up to kMaxSeqPerLaunch sequences) and its work items.
+struct PrefillLaunch {
+    K2Params p;
+    int items;
+};
+
+// K2 launches for the L_b = lens[b] new tokens of each sequence, at positions
+// start[b] .. start[b] + L_b - 1 of `layer` (already in the cache when the
+// launches run); q' rows are read from `qprime` and the outputs written to
+// `out` (both packed [T][Hq][D]; they may be the same buffer).  Builds every
+// tensor map first, so a failure leaves nothing enqueued.
+qa_status plan_k2(qa_cache *c, int layer, int batch, const int32_t *lens, const int32_t *start,
+                  const void *qprime, void *out, std::vector<PrefillLaunch> &launches) {
+    const qa_config &g = c->cfg;
+    const int D = g.head_dim;
+    int64_t row0 = 0;
+    for (int s0 = 0; s0 < batch; s0 += qa::kMaxSeqPerLaunch) {
+        const int n = std::min(qa::kMaxSeqPerLaunch, batch - s0);
+        K2Params p{};
+        int nseq = 0, rows = 0, maxqb = 0;
+        for (int i = 0; i < n; ++i) {
+            const int L = lens[s0 + i];
+            const int P = start[s0 + i];
+            if (L > 0) {
+                __nv_bfloat16 *kb = c->K + layer * c->layer_elems +
+                                    static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
+                __nv_bfloat16 *vb = c->V + layer * c->layer_elems +
+                                    static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
+                if (!encode_kv_map(&p.tm_k[nseq], kb, D, P + L, g.n_kv_heads, g.capacity) ||
+                    !encode_kv_map(&p.tm_v[nseq], vb, D, P + L, g.n_kv_heads, g.capacity))
+                    return QA_ERR_CUDA;
+                p.len[nseq] = L;
+                p.start[nseq] = P;
+                p.cu[nseq] = rows;
+                maxqb = std::max(maxqb, (L + 127) / 128);
+                ++nseq;
+            }
+            rows += L;
+        }
+        if (nseq > 0) {
+            if (!encode_q_map(&p.tm_q,
+                              const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(qprime)) +
+                                  row0 * g.n_q_heads * D,
+                              D, g.n_q_heads, rows))
+                return QA_ERR_CUDA;
+            p.out = static_cast<__nv_bfloat16 *>(out) + row0 * g.n_q_heads * D;
+            p.err = c->err;
+            p.nseq = nseq;
+            p.Hq = g.n_q_heads;
+            p.Hkv = g.n_kv_heads;
+            p.G = c->G;
+            p.npairs = (c->G + qa::kK2HeadsPerCta - 1) / qa::kK2HeadsPerCta;
+            p.max_qblocks = maxqb;
+            p.window = c->window[layer];
+            p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+            p.fault = 0;
+            p.wait_ns = qa::kWaitTimeoutNs;
+            int items = 0;
+            for (int i = 0; i < nseq; ++i) items += (p.len[i] + 127) / 128;
+            items *= g.n_kv_heads * p.npairs;
+            launches.push_back({p, items});
+        }
+        row0 += rows;
+    }
+    return QA_OK;
+}
+
+qa_status launch_k2s(qa_cache *c, std::vector<PrefillLaunch> &launches, cudaStream_t s) {
+    for (auto &l : launches) {
+        const qa::FaultPlan f = qa::take_fault(QA_KERNEL_PREFILL_ATTN);
+        l.p.fault = f.fault;
+        l.p.wait_ns = f.wait_ns;
+        if (qa::launch_k2(l.p, c->cfg.head_dim, l.items, s) != cudaSuccess) return QA_ERR_CUDA;
+        g_order.barrier(s);
+        c->launches[QA_KERNEL_PREFILL_ATTN]++;
     }
     return QA_OK;
 }
@@ -470,7 +570,6 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
         check_prefill(c, layer, batch, prompt_lens, q, k, v, q_norm_w, k_norm_w, out, &T);
     if (st != QA_OK) return st;
     const qa_config &g = c->cfg;
-    const int D = g.head_dim;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int tmax = 0;
     for (int b = 0; b < batch; ++b) tmax = std::max(tmax, static_cast<int>(prompt_lens[b]));
@@ -482,66 +581,44 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
         return QA_OK;
     }
     // Build all tensor maps before the first launch so a failure enqueues nothing.
-    std::vector<K2Params> k2s;
-    std::vector<int> k2_items;
-    int64_t row0 = 0;
-    for (int s0 = 0; s0 < batch; s0 += qa::kMaxSeqPerLaunch) {
-        const int n = std::min(qa::kMaxSeqPerLaunch, batch - s0);
-        K2Params p{};
-        int nseq = 0, rows = 0, maxqb = 0;
-        for (int i = 0; i < n; ++i) {
-            const int L = prompt_lens[s0 + i];
-            const int P = c->lens_host[static_cast<size_t>(layer) * g.max_batch + s0 + i];
-            if (L > 0) {
-                __nv_bfloat16 *kb = c->K + layer * c->layer_elems +
-                                    static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
-                __nv_bfloat16 *vb = c->V + layer * c->layer_elems +
-                                    static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
-                if (!encode_kv_map(&p.tm_k[nseq], kb, D, P + L, g.n_kv_heads, g.capacity) ||
-                    !encode_kv_map(&p.tm_v[nseq], vb, D, P + L, g.n_kv_heads, g.capacity))
-                    return QA_ERR_CUDA;
-                p.len[nseq] = L;
-                p.start[nseq] = P;
-                p.cu[nseq] = rows;
-                maxqb = std::max(maxqb, (L + 127) / 128);
-                ++nseq;
-            }
-            rows += L;
-        }
-        if (nseq > 0) {
-            if (!encode_q_map(&p.tm_q, static_cast<__nv_bfloat16 *>(out) + row0 * g.n_q_heads * D,
-                              D, g.n_q_heads, rows))
-                return QA_ERR_CUDA;
-            p.out = static_cast<__nv_bfloat16 *>(out) + row0 * g.n_q_heads * D;
-            p.err = c->err;
-            p.nseq = nseq;
-            p.Hq = g.n_q_heads;
-            p.Hkv = g.n_kv_heads;
-            p.G = c->G;
-            p.npairs = (c->G + qa::kK2HeadsPerCta - 1) / qa::kK2HeadsPerCta;
-            p.max_qblocks = maxqb;
-            p.window = c->window[layer];
-            p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-            int items = 0;
-            for (int i = 0; i < nseq; ++i) items += (p.len[i] + 127) / 128;
-            items *= g.n_kv_heads * p.npairs;
-            k2s.push_back(p);
-            k2_items.push_back(items);
-        }
-        row0 += rows;
-    }
+    std::vector<PrefillLaunch> k2s;
+    const int32_t *cur = c->lens_host.data() + static_cast<size_t>(layer) * g.max_batch;
+    st = plan_k2(c, layer, batch, prompt_lens, cur, out, out, k2s);
+    if (st != QA_OK) return st;
     // K1 stages the normed, rotated queries in `out`; K2 reads them back and
     // overwrites every row with its attention output (each CTA owns its rows).
     st = run_k1(c, layer, batch, prompt_lens, q, k, v, q_norm_w, k_norm_w, out, s);
     if (st != QA_OK) return st;
-    for (size_t i = 0; i < k2s.size(); ++i) {
-        if (qa::launch_k2(k2s[i], D, k2_items[i], s) != cudaSuccess) return QA_ERR_CUDA;
-        g_order.barrier(s);
-        c->launches[QA_KERNEL_PREFILL_ATTN]++;
-    }
+    st = launch_k2s(c, k2s, s);
+    if (st != QA_OK) return st;
     for (int b = 0; b < batch; ++b)
         c->lens_host[static_cast<size_t>(layer) * g.max_batch + b] += prompt_lens[b];
     return QA_OK;
+}
+
+QA_API qa_status qa_prefill_attend(qa_cache *c, int layer, int batch, const int32_t *prompt_lens,
+                                   const void *qprime, void *out, void *stream) {
+    qa_status st = check_layer(c, layer, batch);
+    if (st != QA_OK) return st;
+    if (!prompt_lens) return QA_ERR_INVALID_ARG;
+    const qa_config &g = c->cfg;
+    // The new tokens are the last prompt_lens[b] positions sequence b holds.
+    const int32_t *held = c->lens_host.data() + static_cast<size_t>(layer) * g.max_batch;
+    std::vector<int32_t> start(static_cast<size_t>(batch));
+    int64_t T = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (prompt_lens[b] < 0 || prompt_lens[b] > held[b]) return QA_ERR_INVALID_ARG;
+        start[b] = held[b] - prompt_lens[b];
+        T += prompt_lens[b];
+    }
+    if (T == 0) return QA_OK;
+    if (!qprime || !out) return QA_ERR_INVALID_ARG;
+    if (!aligned16(qprime) || !aligned16(out)) return QA_ERR_ALIGNMENT;
+    if (T > (int64_t(1) << 26)) return QA_ERR_INVALID_ARG;
+    std::vector<PrefillLaunch> k2s;
+    st = plan_k2(c, layer, batch, prompt_lens, start.data(), qprime, out, k2s);
+    if (st != QA_OK) return st;
+    return launch_k2s(c, k2s, static_cast<cudaStream_t>(stream));
 }
 
 QA_API int qa_decode_splits(qa_cache *c, int layer, int batch) {
@@ -593,6 +670,9 @@ qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const vo
         p.guard = g_order.admit(static_cast<cudaStream_t>(stream), c, layer,
                                 p.S * g.n_kv_heads * c->HG * nb, 1, !dev_pos,
                                 qa::k3_max_resident_ctas());
+        const qa::FaultPlan f = qa::take_fault(QA_KERNEL_DECODE_ATTN);
+        p.fault = f.fault;
+        p.wait_ns = f.wait_ns;
         if (qa::launch_k3(p, g.head_dim, c->HPC, static_cast<cudaStream_t>(stream)) != cudaSuccess)
             return QA_ERR_CUDA;
         c->launches[QA_KERNEL_DECODE_ATTN]++;
@@ -694,6 +774,18 @@ QA_API qa_status qa_get_device_error(qa_cache *c, uint32_t *detail) {
         case qa::kErrTimeout: return QA_ERR_DEVICE_TIMEOUT;
         default: return QA_ERR_DEVICE_BOUNDS;
     }
+}
+
+QA_API qa_status qa_debug_arm_wait_timeout(int kernel, uint32_t wait_us) {
+    if (kernel == -1) {
+        g_fault_kernel.store(-1, std::memory_order_release);
+        return QA_OK;
+    }
+    if (kernel != QA_KERNEL_PREFILL_ATTN && kernel != QA_KERNEL_DECODE_ATTN) return QA_ERR_INVALID_ARG;
+    if (wait_us < 1 || wait_us > 2000000) return QA_ERR_INVALID_ARG;
+    g_fault_wait_ns.store(static_cast<uint64_t>(wait_us) * 1000ull, std::memory_order_release);
+    g_fault_kernel.store(kernel, std::memory_order_release);
+    return QA_OK;
 }
 
 QA_API qa_status qa_stats(qa_cache *c, uint64_t launches[QA_NUM_KERNELS]) {

@@ -67,17 +67,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, but never forever:
-// after kWaitTimeoutNs, or once another thread of the CTA raised *abort, give
-// up, record a timeout in the error word and return false.
+// after limit_ns (kWaitTimeoutNs unless a launch asks for less), or once
+// another thread of the CTA raised *abort, give up, record a timeout in the
+// error word and return false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          uint32_t *err, uint32_t kernel, uint32_t site) {
+                                          uint32_t *err, uint32_t kernel, uint32_t site,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((spin & 63u) == 0u) {
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort = 1;
                 set_error(err, kErrTimeout, kernel, site);
                 return false;
@@ -89,7 +91,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Bounded wait with cluster-scope acquire: for data that other CTAs of the
 // cluster wrote into this CTA's shared memory with st.async.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort,
-                                                  uint32_t *err, uint32_t kernel, uint32_t site) {
+                                                  uint32_t *err, uint32_t kernel, uint32_t site,
+                                                  uint64_t limit_ns = kWaitTimeoutNs) {
     const uint64_t t0 = globaltimer();
     for (uint32_t spin = 0;; ++spin) {
         uint32_t ok;
@@ -102,7 +105,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
         if (ok) return true;
         if ((spin & 63u) == 63u) {
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort = 1;
                 set_error(err, kErrTimeout, kernel, site);
                 return false;

@@ -17,6 +17,17 @@ constexpr uint32_t kKernK1 = 1, kKernK2 = 2, kKernK3 = 3;
 // kernel here takes well under a millisecond).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
+// Failure-detection test hook (qa_debug_arm_wait_timeout): a launch whose
+// `fault` field is set withholds the first tile copy of its first thread
+// block, so a consumer of that tile waits for an mbarrier no copy will ever
+// complete, and its waits give up after `wait_ns`.  Nothing else changes.
+struct FaultPlan {
+    uint64_t wait_ns = kWaitTimeoutNs;
+    int fault = 0;
+};
+// Takes (and disarms) the armed fault for `kernel` (QA_KERNEL_* index), if any.
+FaultPlan take_fault(int kernel);
+
 // ---------------------------------------------------------------- K1
 // Sequences per prefill launch (K1 and K2 take their per-sequence data as
 // kernel parameters; longer batches are split into several launches).
@@ -64,6 +75,8 @@ struct alignas(64) K2Params {
     int max_qblocks;
     int window;                               // attention window in keys (0: all earlier keys)
     float scale_log2;                         // log2(e) / sqrt(D)
+    int fault;                                // test hook: withhold a copy in CTA 0 (FaultPlan)
+    uint64_t wait_ns;                         // limit of every bounded wait
 };
 
 // ---------------------------------------------------------------- K3
@@ -95,6 +108,8 @@ struct K3Params {
     int guard;                       // rows just below each sequence's first new slot that
                                      // a launch still running may write (loaded after the wait)
     uint32_t *seq_cnt;               // [max_batch] groups done per sequence (dev_pos only)
+    int fault;                       // test hook: withhold a copy in CTA (0,0,0) (FaultPlan)
+    uint64_t wait_ns;                // limit of every bounded wait
     int pos[kK3MaxSeqPerLaunch];     // slot of each launched sequence's (first) new token
 };
 

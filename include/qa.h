@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define QA_ABI_VERSION 3
+#define QA_ABI_VERSION 4
 
 typedef enum {
     QA_OK = 0,
@@ -230,11 +230,39 @@ qa_status qa_prefill_transform(qa_cache *cache, int layer, int batch, const int3
                                const void *q_norm_w, const void *k_norm_w, void *qprime_out,
                                void *stream);
 
+/* Run only the attention of a prefill (K2): for sequence b, the last
+ * prompt_lens[b] positions the layer holds (appended earlier, e.g. by
+ * qa_prefill_transform) attend causally to keys 0..own position (and the
+ * layer's window), exactly as in qa_prefill.  qprime: [T][Hq][D] normed,
+ * rotated queries of those tokens (qa_prefill_transform's output); out:
+ * [T][Hq][D]; out may be qprime (in place, as qa_prefill does).  Always the
+ * prefill kernel, whatever the lengths.  Splitting qa_prefill this way lets
+ * each kernel be timed on its own.  The lengths are not changed.
+ * Errors: INVALID_ARG (a prompt_lens[b] above what sequence b holds),
+ * ALIGNMENT. */
+qa_status qa_prefill_attend(qa_cache *cache, int layer, int batch, const int32_t *prompt_lens,
+                            const void *qprime, void *out, void *stream);
+
 /* Synchronise the device, read and clear the error word the kernels set when
  * a bounded wait expired or a position fell outside the cache.  Returns
  * QA_OK, QA_ERR_DEVICE_TIMEOUT or QA_ERR_DEVICE_BOUNDS; *detail (may be NULL)
  * receives the raw word: bits 0-7 kind, 8-15 kernel, 16-31 site. */
 qa_status qa_get_device_error(qa_cache *cache, uint32_t *detail);
+
+/* Failure-detection test hook.  Arms the next launch of `kernel`
+ * (QA_KERNEL_PREFILL_ATTN, or QA_KERNEL_DECODE_ATTN: decode steps, short
+ * chunks and qa_decode_step_noalloc), process-wide: in that launch the first
+ * thread block withholds one of its tile copies, so a wait for that tile can
+ * never succeed, and every bounded wait of the launch gives up after wait_us
+ * microseconds (1 .. 2000000) instead of 2 s.  The waiting thread records
+ * QA_ERR_DEVICE_TIMEOUT (kernel and site in the detail word) in the error
+ * word that qa_get_device_error / qa_noalloc_get_device_error read, the block
+ * waits (bounded) for its own copies in flight and for what its cluster peers
+ * send it, frees its tensor memory and exits; that launch's outputs and the
+ * cache slots it appends are undefined, everything else stays usable.
+ * kernel = -1 disarms.  Nothing faults or hangs: every wait is bounded.
+ * Errors: INVALID_ARG (another kernel index, wait_us out of range). */
+qa_status qa_debug_arm_wait_timeout(int kernel, uint32_t wait_us);
 
 /* Successful-launch counters per kernel (QA_KERNEL_*), proving which native
  * kernels ran (the launch-counter check of the pegainfer PR #862 review). */
@@ -251,15 +279,13 @@ qa_status qa_memory_info(qa_cache *cache, uint64_t *kv_bytes, uint64_t *scratch_
 int qa_decode_splits(qa_cache *cache, int layer, int batch);
 
 /* ---- allocation-free decode step ----------------------------------------
- * The pages have no counterpart of this entry point; it exists for callers
- * that must not allocate device memory at all: code that runs while a CUDA
- * graph is being captured (an allocation there is illegal or breaks the
- * capture), engines that hand out every byte of the GPU from their own arena
- * and forbid any other allocation, and plug-ins embedded in a host framework
- * that owns the device allocator.  Such a caller owns the cache memory and the
- * lengths itself and passes them in.
+ * The pages have no counterpart of this entry point.  It is for callers that
+ * may not allocate device memory at all: engines that hand out every byte of
+ * the GPU from their own arena and forbid any other allocation, and plug-ins
+ * embedded in a host framework that owns the device allocator.  Such a caller
+ * owns the cache memory and the lengths itself and passes them in.
  *
- * One decode step of one layer, computed by the same kernel as
+ * One decode step of one layer, computed by the same kernel body as
  * qa_decode_step: for each of sequences 0..batch-1 the new token's q and k are
  * RMS-normed and rotated at position positions[b], k' and v are written to
  * cache slot positions[b], and every query head attends over slots
@@ -267,18 +293,22 @@ int qa_decode_splits(qa_cache *cache, int layer, int batch);
  *   cfg         geometry (num_layers is ignored; one layer is passed).
  *   positions   HOST int32 [batch]: current length of each sequence, which is
  *               the slot of its new token; each must be < capacity.  The
- *               caller advances its own lengths after the call.
+ *               caller advances its own lengths after the call.  The
+ *               positions and their rotary values are copied into the
+ *               launch's parameters at this call.
  *   k_cache, v_cache  DEVICE bf16 [max_batch][n_kv_heads][capacity][head_dim]
  *               of this layer, caller-owned, read and appended to.
  *   q, k, v, q_norm_w, k_norm_w, out: as in qa_decode_step.
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
- * The kernel's global scratch (its error word; the key-range splits are
- * merged in distributed shared memory) is a fixed 256-byte array in the
- * library's device code, created on every GPU that loads the library and held
- * until the process exits; each call clears it first.  The first call on a
- * device looks up that array's address (no allocation); make that first call
- * before any stream capture.  Every call shares the array: calls that may
- * overlap on the GPU (different streams without ordering) race on it.
+ * The kernel's only global scratch is its error word (the key-range splits
+ * are merged in distributed shared memory), kept in a fixed 256-byte array in
+ * the library's device code that every GPU loading the library holds until
+ * the process exits.  The first call on a device looks up that array's
+ * address (no allocation); make that first call before any stream capture.
+ * Every call shares the array: calls that may overlap on the GPU (different
+ * streams without ordering) race on it.  The error word is zero at load and
+ * is cleared only by qa_noalloc_get_device_error, so it keeps the first error
+ * of any call since the last read.
  * Limits: batch <= 16 (the per-sequence positions and rotary values travel in
  * the kernel parameters), else QA_ERR_UNSUPPORTED_SHAPE.  Errors:
  * INVALID_ARG, UNSUPPORTED_SHAPE, ALIGNMENT, CAPACITY (a position >=
@@ -287,6 +317,15 @@ qa_status qa_decode_step_noalloc(const qa_config *cfg, int batch, const int32_t 
                                  void *k_cache, void *v_cache, const void *q, const void *k,
                                  const void *v, const void *q_norm_w, const void *k_norm_w,
                                  void *out, void *stream);
+
+/* Read and clear the error word of qa_decode_step_noalloc on the current
+ * device, after synchronising `stream` (the stream the steps ran on; calls on
+ * other streams must have finished too).  Returns QA_OK,
+ * QA_ERR_DEVICE_TIMEOUT or QA_ERR_DEVICE_BOUNDS; *detail (may be NULL)
+ * receives the raw word (bits 0-7 kind, 8-15 kernel, 16-31 site).  Allocates
+ * nothing: a 4-byte copy into host memory and a 4-byte memset.
+ * Errors: CUDA. */
+qa_status qa_noalloc_get_device_error(uint32_t *detail, void *stream);
 
 /* Static description of a status code. */
 const char *qa_status_str(qa_status status);

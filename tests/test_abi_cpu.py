@@ -102,3 +102,21 @@ def test_valid_alloc_without_a_device_reports_cuda_error(qa):
     with pytest.raises(qa.QaError) as e:
         qa.qa_cache_alloc(1, 1, 2, 1, 64, 72)
     assert e.value.status == 6
+
+
+def test_new_hooks_validate_before_touching_the_device(qa):
+    lens = (ctypes.c_int32 * 1)(4)
+    assert qa.lib.qa_prefill_attend(None, 0, 1, lens, 16, 16, None) == 1
+    # the failure-detection hook: only the two tiled kernels, a bounded limit
+    for kernel, us in ((0, 100), (3, 100), (7, 100), (1, 0), (2, 2000001)):
+        assert qa.lib.qa_debug_arm_wait_timeout(kernel, us) == 1
+    assert qa.lib.qa_debug_arm_wait_timeout(2, 1000) == 0
+    assert qa.lib.qa_debug_arm_wait_timeout(-1, 0) == 0   # disarm
+
+
+def test_noalloc_error_read_without_a_device_reports_cuda_error(qa):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    w = ctypes.c_uint32(123)
+    assert qa.lib.qa_noalloc_get_device_error(ctypes.byref(w), None) == 6

@@ -6,7 +6,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import GpuCache, bits, dev, f64
+from gpu_util import GpuCache, assert_parity, bits, dev, f64
+from gqa_attention_preallocated_qa_gb300.inputs import bf16_bits_to_f64 as F
 from gqa_attention_preallocated_qa_gb300.inputs import layer_inputs
 
 pytestmark = pytest.mark.gpu
@@ -34,12 +35,14 @@ def prefilled(qa, layers, prompt, cap, inps):
     return c
 
 
-def test_device_lengths_step_equals_host_position_step(qa):
+def test_device_lengths_step_equals_host_position_step(qa, oracle_mod):
     prompt, steps, cap = (300, 129, 1, 512), 5, 600
     inp = layer_inputs(81, prompt, HQ, HKV, D, steps)
     wq, wk = dev(inp.wq), dev(inp.wk)
     a = prefilled(qa, 1, prompt, cap, [inp])
     b = prefilled(qa, 1, prompt, cap, [inp])
+    lay = oracle_mod.OracleLayer(oracle_mod.Geometry(4, HQ, HKV, D, cap))
+    lay.prefill(prompt, F(inp.q), F(inp.k), F(inp.v), F(inp.wq), F(inp.wk))
     # device-length steps plan their splits for one launch at a time; the same
     # plan on the host-position side makes the two sums bit-comparable
     qa.qa_cache_set_decode_overlap(a.h, 1)
@@ -51,6 +54,8 @@ def test_device_lengths_step_equals_host_position_step(qa):
             qa.qa_decode_step_device_lengths(b.h, 0, 4, dq, dk, dv, wq, wk, ob)
             torch.cuda.synchronize()
             np.testing.assert_array_equal(bits(oa), bits(ob))
+            _, want = lay.decode(F(inp.dq[s]), F(inp.dk[s]), F(inp.dv[s]), F(inp.wq), F(inp.wk))
+            assert_parity(f64(ob), want, f"device-length step {s}")
         final = [n + steps for n in prompt]
         assert list(b.views()[2].cpu().numpy()) == final
         assert qa.qa_cache_lengths(b.h, 0, 4) == list(prompt)  # host copy not advanced
@@ -74,12 +79,22 @@ def test_device_lengths_step_equals_host_position_step(qa):
         b.free()
 
 
-def test_cuda_graph_of_a_two_layer_decode_step_replays_at_every_position(qa):
+def test_cuda_graph_of_a_two_layer_decode_step_replays_at_every_position(qa, oracle_mod):
     prompt, cap, replays = (200, 77, 512, 129), 560, 4
     inps = [layer_inputs(83 + l, prompt, HQ, HKV, D, replays) for l in range(2)]
     ws = [(dev(i.wq), dev(i.wk)) for i in inps]
     g_cache = prefilled(qa, 2, prompt, cap, inps)
     e_cache = prefilled(qa, 2, prompt, cap, inps)
+    # the oracle follows both layers step by step: every replay is judged by it
+    lays = []
+    for inp in inps:
+        lay = oracle_mod.OracleLayer(oracle_mod.Geometry(4, HQ, HKV, D, cap))
+        lay.prefill(prompt, F(inp.q), F(inp.k), F(inp.v), F(inp.wq), F(inp.wk))
+        lays.append(lay)
+
+    def oracle_step(s):
+        return [lays[l].decode(F(inps[l].dq[s]), F(inps[l].dk[s]), F(inps[l].dv[s]),
+                               F(inps[l].wq), F(inps[l].wk))[1] for l in range(2)]
     try:
         # static buffers of the captured step
         sq = [torch.empty((4, HQ, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
@@ -102,6 +117,9 @@ def test_cuda_graph_of_a_two_layer_decode_step_replays_at_every_position(qa):
         step(g_cache.h)
         torch.cuda.synchronize()
         want = [[f64(so[l])] for l in range(2)]
+        orc = oracle_step(0)
+        for l in range(2):
+            assert_parity(want[l][0], orc[l], f"eager device-length step 0, layer {l}")
         step(e_cache.h)
         torch.cuda.synchronize()
         for l in range(2):
@@ -121,8 +139,10 @@ def test_cuda_graph_of_a_two_layer_decode_step_replays_at_every_position(qa):
             load(s)
             graph.replay()
             torch.cuda.synchronize()
+            orc = oracle_step(s)
             for l in range(2):
                 np.testing.assert_array_equal(f64(so[l]), ref[l], err_msg=f"replay {s} layer {l}")
+                assert_parity(f64(so[l]), orc[l], f"graph replay {s}, layer {l}")
         final = [n + replays for n in prompt]
         for l in range(2):
             assert list(g_cache.views(l)[2].cpu().numpy()) == final

@@ -108,7 +108,7 @@ def test_decode_on_prefilled_cache(qa, oracle_mod, B, L, Hq, Hkv, D):
 # ------------------------------------------------------------------ prefill + decode, small
 @pytest.mark.parametrize("lens,Hq,Hkv,D,steps,cap", [
     (TINY.prompt_lens, TINY.Hq, TINY.Hkv, TINY.D, TINY.steps, TINY.cap),
-    (QWEN3_4B_B1.prompt_lens, 32, 8, 128, 4, QWEN3_4B_B1.cap),
+    (QWEN3_4B_B1.prompt_lens, 32, 8, 128, QWEN3_4B_B1.steps, QWEN3_4B_B1.cap),  # all 32 steps
     ((200, 77, 300, 1, 129), 32, 8, 128, 3, 310),      # ragged, tails of 1 and 127 rows
     ((130, 5), 16, 2, 64, 2, 140),                      # group 8 (two head groups per kv head)
     ((100, 256), 4, 4, 128, 2, 260),                    # group 1 (multi-head)

@@ -5,7 +5,9 @@ any size.
 - B=4, prompts of 2048, 128 decode steps, capacity 2176 (the benchmark's
   launch configuration), run three times with a cache reset in between.
 - B=4 ragged prompts (512, 1024, 1536, 2048), 64 decode steps, 36 independent
-  layer caches; layers 0, 17 and 35 are tracked by the oracle.
+  layer caches: every layer's decode steps 0 and 63 on one head per kv group,
+  and layers 0, 17 and 35 in full (every prompt row on one head plus sampled
+  rows on two more, every decode step on every head, the cache slots).
 - Decode sweep: B in {1, 4} x cache length in {512, 2048, 8192, 16384}, cache
   filled with raw N(0,1) keys/values, one decode step, every head checked.
 """
@@ -92,24 +94,35 @@ def test_b4_prompt2048_128_steps_with_reset_reruns(qa, oracle_mod):
         qp = lay.prefill_transform(w.prompt_lens, F(inp.q), F(inp.k), F(inp.v), F(inp.wq),
                                    F(inp.wk))
         check_prefill_rows(lay, w, qp, got_pre, w.prompt_lens, rng, heads=(0, 3, 4, 17, 31))
-        checked = (0, 1, 63, 64, 127)
-        for s in range(w.steps):
+        for s in range(w.steps):  # every decode step, every head
             qd = lay.decode_transform(F(inp.dq[s]), F(inp.dk[s]), F(inp.dv[s]), F(inp.wq),
                                       F(inp.wk))
-            if s in checked:
-                want = np.array([[lay.attend_cached(b, h, qd[b, h]) for h in range(w.Hq)]
-                                 for b in range(w.B)])
-                assert_parity(got_dec[s], want, f"decode step {s}")
+            want = np.array([[lay.attend_cached(b, h, qd[b, h]) for h in range(w.Hq)]
+                             for b in range(w.B)])
+            assert_parity(got_dec[s], want, f"decode step {s}")
         check_cache(c, lay, [w.cap] * w.B)
         assert c.device_error() == (0, 0)
     finally:
         c.free()
 
 
+def check_all_prefill_rows(lay, qp, got, lens, head):
+    """Every prompt row of every sequence on one head."""
+    want_rows, got_rows = [], []
+    t0 = 0
+    for b, L in enumerate(lens):
+        for i in range(L):
+            want_rows.append(lay.prefill_row(b, head, i, qp[t0 + i, head]))
+            got_rows.append(got[t0 + i, head])
+        t0 += L
+    assert_parity(np.array(got_rows), np.array(want_rows), f"all prompt rows, head {head}")
+
+
 def test_ragged_prompts_36_layers(qa, oracle_mod):
     w = RAGGED_36L
     rng = np.random.default_rng(7)
     tracked = (0, 17, 35)
+    every_layer_steps = (0, w.steps - 1)
     c = GpuCache(qa, w.layers, w.B, w.Hq, w.Hkv, w.D, w.cap)
     try:
         c.poison(tracked)
@@ -123,36 +136,57 @@ def test_ragged_prompts_36_layers(qa, oracle_mod):
             dec.append((dev(inp.dq), dev(inp.dk), dev(inp.dv), wq, wk))
             if l in tracked:
                 torch.cuda.synchronize()
-                layers[l] = (inp, F(bits(out)))
-            del q, k, v, out
+                layers[l] = F(bits(out))
+            del q, k, v, out, inp
         douts = {l: torch.empty((w.steps, w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
                  for l in tracked}
+        # steps 0 and 63 of every layer
+        souts = torch.empty((len(every_layer_steps), w.layers, w.B, w.Hq, w.D), dtype=torch.bfloat16,
+                            device="cuda")
         scratch = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
         for s in range(w.steps):          # the generate loop: every layer, step by step
             for l in range(w.layers):
                 dq, dk, dv, wq, wk = dec[l]
-                o = douts[l][s] if l in tracked else scratch
+                if l in tracked:
+                    o = douts[l][s]
+                elif s in every_layer_steps:
+                    o = souts[every_layer_steps.index(s), l]
+                else:
+                    o = scratch
                 qa.qa_decode_step(c.h, l, w.B, dq[s], dk[s], dv[s], wq, wk, o)
+                if l in tracked and s in every_layer_steps:
+                    souts[every_layer_steps.index(s), l].copy_(o)
         torch.cuda.synchronize()
         final = [L + w.steps for L in w.prompt_lens]
         for l in range(w.layers):
             assert qa.qa_cache_lengths(c.h, l, w.B) == final
             assert list(c.views(l)[2].cpu().numpy()) == final
-        for l in tracked:
-            inp, got_pre = layers[l]
+        got_steps = f64(souts)
+        G = w.Hq // w.Hkv
+        for l in range(w.layers):
+            inp = w.inputs(l)
             lay = oracle_mod.OracleLayer(oracle_mod.Geometry(w.B, w.Hq, w.Hkv, w.D, w.cap))
             qp = lay.prefill_transform(w.prompt_lens, F(inp.q), F(inp.k), F(inp.v), F(inp.wq),
                                        F(inp.wk))
-            check_prefill_rows(lay, w, qp, got_pre, w.prompt_lens, rng, heads=(1, 30))
-            got_dec = f64(douts[l])
+            if l in tracked:
+                check_all_prefill_rows(lay, qp, layers[l], w.prompt_lens, head=(l % w.Hq))
+                check_prefill_rows(lay, w, qp, layers[l], w.prompt_lens, rng, heads=(1, 30))
+                got_dec = f64(douts[l])
             for s in range(w.steps):
                 qd = lay.decode_transform(F(inp.dq[s]), F(inp.dk[s]), F(inp.dv[s]), F(inp.wq),
                                           F(inp.wk))
-                if s in (0, 31, 63):
+                if l in tracked:  # every step, every head
                     want = np.array([[lay.attend_cached(b, h, qd[b, h]) for h in range(w.Hq)]
                                      for b in range(w.B)])
                     assert_parity(got_dec[s], want, f"layer {l} decode step {s}")
-            check_cache(c, lay, final, layer=l)
+                if s in every_layer_steps:  # one head per kv group, rotating with the layer
+                    heads = [kvh * G + (l + kvh) % G for kvh in range(w.Hkv)]
+                    want = np.array([[lay.attend_cached(b, h, qd[b, h]) for h in heads]
+                                     for b in range(w.B)])
+                    got = got_steps[every_layer_steps.index(s), l][:, heads]
+                    assert_parity(got, want, f"layer {l} decode step {s}")
+            if l in tracked:
+                check_cache(c, lay, final, layer=l)
         assert c.device_error() == (0, 0)
         assert qa.qa_stats(c.h)["decode_attn"] == w.layers * w.steps
     finally:

@@ -296,3 +296,47 @@ def test_reset_then_rerun_is_identical_and_overflow_is_an_error(oracle_mod):
     # a prefill on a non-empty layer is an error too
     with pytest.raises(oracle_mod.OracleError):
         lay.prefill(lens, *args)
+
+
+def test_attend_cached_after_decode_transform_matches_brute_force_and_decode(oracle_mod):
+    # OracleLayer.attend_cached is the expected value of the full-size decode
+    # checks (the cache is appended once by decode_transform, then any head is
+    # attended on its own).  Pinned two ways: (1) against the matrix-form brute
+    # force over each sequence's prompt + decode tokens (decode step s of a
+    # sequence is row L_b + s of that concatenation), and (2) against the
+    # oracle's own fused decode on a second layer.  A head-mapping slip (h % Hkv
+    # instead of h // G) or a length slip (keys :n+1 or :n-1) fails both.
+    prompt_lens, Hq, Hkv, D, steps = (6, 1, 9), 8, 2, 16, 3
+    inp = layer_inputs(37, prompt_lens, Hq, Hkv, D, steps)
+    q, k, v, wq, wk = (_f(a) for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+    dq, dk, dv = _f(inp.dq), _f(inp.dk), _f(inp.dv)
+    B, cap = len(prompt_lens), max(prompt_lens) + steps
+    a = oracle_mod.OracleLayer(_geom(oracle_mod, B, Hq, Hkv, D, cap))
+    b = oracle_mod.OracleLayer(_geom(oracle_mod, B, Hq, Hkv, D, cap))
+    a.prefill(prompt_lens, q, k, v, wq, wk)
+    b.prefill(prompt_lens, q, k, v, wq, wk)
+    # brute force over the concatenated tokens of each sequence
+    cu = np.concatenate([[0], np.cumsum(prompt_lens)])
+    cat = [np.concatenate([x[cu[i]:cu[i + 1]] for i in range(B)] +
+                          [d[s, i:i + 1] for s in range(steps) for i in range(B)])
+           for x, d in ((q, dq), (k, dk), (v, dv))]
+    # reorder into sequence-major packing: sequence i's prompt rows, then its steps
+    rows = []
+    off = int(cu[-1])
+    for i in range(B):
+        rows.extend(range(cu[i], cu[i + 1]))
+        rows.extend(off + s * B + i for s in range(steps))
+    qb, kb, vb = (c[rows] for c in cat)
+    brute = _brute_force_layer([L + steps for L in prompt_lens], qb, kb, vb, wq, wk, Hq, Hkv,
+                               1e6, 1e-6)
+    bcu = np.concatenate([[0], np.cumsum([L + steps for L in prompt_lens])])
+    for s in range(steps):
+        qp = a.decode_transform(dq[s], dk[s], dv[s], wq, wk)
+        _, fused = b.decode(dq[s], dk[s], dv[s], wq, wk)
+        for i in range(B):
+            for h in range(Hq):
+                got = a.attend_cached(i, h, qp[i, h])
+                np.testing.assert_allclose(got, fused[i, h], rtol=1e-12, atol=1e-14)
+                np.testing.assert_allclose(got, brute[bcu[i] + prompt_lens[i] + s, h],
+                                           rtol=1e-9, atol=1e-12)
+    assert list(a.lens) == [L + steps for L in prompt_lens]
