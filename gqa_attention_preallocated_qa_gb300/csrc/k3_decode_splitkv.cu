@@ -327,9 +327,9 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         // chunks wholly below row pos - guard (all of them without a guard)
         c_safe = p.guard <= 0 ? nchunks : (pos > p.guard ? (pos - p.guard) / kK3Chunk : 0);
         first_round = min(NS, my_chunks);
-        // Test hook: the first CTA withholds its first chunk's copy (FaultPlan).
-        withheld = (p.fault && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
-                    my_chunks > 0) ? 0 : -1;
+        // Test hook (FaultPlan): every CTA of the first (sequence, kv head, head
+        // group) cluster that streams cache chunks withholds its first one.
+        withheld = (p.fault && blockIdx.y == 0 && blockIdx.z == 0 && my_chunks > 0) ? 0 : -1;
     };
     if (!kDevPos) plan();
     const bool owner = split == S - 1;

@@ -18,9 +18,11 @@ constexpr uint32_t kKernK1 = 1, kKernK2 = 2, kKernK3 = 3;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 // Failure-detection test hook (qa_debug_arm_wait_timeout): a launch whose
-// `fault` field is set withholds the first tile copy of its first thread
-// block, so a consumer of that tile waits for an mbarrier no copy will ever
-// complete, and its waits give up after `wait_ns`.  Nothing else changes.
+// `fault` field is set withholds one tile copy (prefill: V tile 0 of its first
+// thread block; decode: the first cache chunk of every block of the first
+// cluster that streams any), so a consumer of that tile waits for an mbarrier
+// no copy will ever complete, and the launch's waits give up after `wait_ns`.
+// Nothing else changes.
 struct FaultPlan {
     uint64_t wait_ns = kWaitTimeoutNs;
     int fault = 0;
