@@ -56,10 +56,18 @@ struct K1Params {
 // one softmax warpgroup, a TMA warp and an MMA warp; the default: one CTA's
 // per-block prologue and epilogue overlap the other's main loop) or 2 (one CTA
 // per SM; the two heads share every K/V tile).
+// QA_K2_FORM selects the prefill kernel: 1 (default) the persistent form (one
+// CTA per SM walking a fixed share of the work items, two query heads of one kv
+// head per item sharing every K/V tile, the next item's loads and first S
+// overlapping the current item's end); 0 the per-block form (one CTA per work
+// item, QA_K2_HEADS_PER_CTA query heads each).
+#ifndef QA_K2_FORM
+#define QA_K2_FORM 1
+#endif
 #ifndef QA_K2_HEADS_PER_CTA
 #define QA_K2_HEADS_PER_CTA 1
 #endif
-constexpr int kK2HeadsPerCta = QA_K2_HEADS_PER_CTA;
+constexpr int kK2HeadsPerCta = QA_K2_FORM == 1 ? 2 : QA_K2_HEADS_PER_CTA;
 static_assert(kK2HeadsPerCta == 1 || kK2HeadsPerCta == 2, "one or two query heads per CTA");
 constexpr int kK2BlockM = 128;    // query rows per tile
 constexpr int kK2BlockN = 128;    // keys per tile
@@ -78,6 +86,7 @@ struct alignas(64) K2Params {
     int window;                               // attention window in keys (0: all earlier keys)
     float scale_log2;                         // log2(e) / sqrt(D)
     int fault;                                // test hook: withhold a copy in CTA 0 (FaultPlan)
+    int nitems;                               // work items (query block x head tile(s))
     uint64_t wait_ns;                         // limit of every bounded wait
 };
 
