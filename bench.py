@@ -566,6 +566,15 @@ def traffic_for(kernel: str, algorithmic_bytes):
 
 
 # ---------------------------------------------------------------- decode sweep
+def host_ahead(launches: int, us_per_launch: float = 6.0):
+    """Put the device behind the host: a GPU sleep long enough for the host to
+    enqueue `launches` calls first, so that events around a loop of short
+    launches time the device, not the host's launch rate (which the caller
+    measures and reports separately)."""
+    import torch
+    torch.cuda._sleep(int(launches * us_per_launch * 2.5e3))  # ~2.5 GHz upper bound on cycles/us
+
+
 def decode_sweep(args, pk, steps, isolated_steps=200):
     """Decode-only sweep (batch 1 and 4, cache lengths 512 to 16384).  Each
     point allocates NL layer caches, NL large enough that together they hold
@@ -573,9 +582,11 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
     per sequence; the `steps` timed decode steps cycle through the layers (step
     s decodes layer s mod NL, as a model's layer loop does), so each step reads
     its layer's K/V from HBM, not from L2.  The length of a layer grows by one
-    per visit; bytes are counted exactly.  Per point: mean µs per step, K/V
-    bytes per step and HBM GB/s (events around the whole loop: launch gaps
-    included); `same_layer_us_per_step` repeats the measurement on a single
+    per visit; bytes are counted exactly.  A GPU sleep before the loop lets the
+    host enqueue the launches ahead of the device, so the events time the
+    device (the host's own µs per call is reported beside it).  Per point: mean
+    µs per step, K/V bytes per step and HBM GB/s (events around the whole loop:
+    launch gaps included); `same_layer_us_per_step` repeats the measurement on a single
     layer (its cache can stay in L2 when small).  At B = 4, L = 2048 the point
     also times `isolated_steps` steps one by one: split plan for one launch at
     a time, a spacer kernel before each (so no launch overlaps the previous
@@ -625,13 +636,16 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         byts = 0
         torch.cuda.synchronize()
+        host_ahead(steps)
         e0.record(stream)
+        t_host = time.perf_counter()
         for i in range(steps):
             layer = (args.warmup + i) % NL
             st |= lib.qa_decode_step(h, layer, pt.B, *args_c, sh)
             lens[layer] += 1
             byts += pt.B * pt.Hkv * lens[layer] * pt.D * 4  # keys 0..pos, K and V
         e1.record(stream)
+        host_us = (time.perf_counter() - t_host) * 1e6 / steps
         torch.cuda.synchronize()
         if st or qa.qa_get_device_error(h)[0]:
             raise RuntimeError(f"decode sweep point {pt.name} failed")
@@ -645,6 +659,8 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(iso)]
             ib = 0
+            torch.cuda.synchronize()
+            host_ahead(3 * iso)
             for i in range(iso):
                 layer = (args.warmup + steps + i) % NL
                 spacer.add_(1.0)  # a plain kernel: this launch cannot overlap a decode launch
@@ -663,7 +679,8 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
                         "frac_of_measured_hbm": round(iso_gbs / pk["hbm_gbs"], 4),
                         "kv_bytes_per_step": round(ib / iso),
                         "how": "median of per-launch events; a spacer kernel before each launch, "
-                               "layers cycled (HBM-cold), split plan for one launch"}
+                               "layers cycled (HBM-cold), split plan for one launch, the host "
+                               "ahead of the device"}
             qa.qa_cache_set_decode_overlap(h, 2)
         # the same on one layer, for reference (its K/V may stay in L2)
         n1 = same_steps
@@ -677,6 +694,7 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
             raise RuntimeError(f"decode sweep point {pt.name} failed")
         points.append({"sweep": pt.name, "B": pt.B, "L": pt.L, "steps": steps, "layers": NL,
                        "splits": splits, "us_per_step": round(us, 3),
+                       "host_us_per_call": round(host_us, 3),
                        "kv_bytes_per_step": round(byts), "hbm_gbs": round(gbs, 1),
                        "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
                        "same_layer_us_per_step": round(e2.elapsed_time(e3) * 1e3 / max(1, n1), 3)})

@@ -358,6 +358,8 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
             mbar_init(smem_u32(&bar_empty[s]), 1);
         }
         mbar_init(smem_u32(&bar_recv), 1);
+        prefetch_tmap(tmk);
+        prefetch_tmap(tmv);
         s_abort = 0;
         if (E_me > 0) mbar_expect_tx(smem_u32(&bar_recv), NSRC * (E_me * 4 + nh_me * 8));
         fence_mbar_init();
@@ -424,12 +426,26 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         if constexpr (kTableRope) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         prologue();
     } else {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        pos = p.lens[b];
-        plan();
-        if (warp == NW && lane == 0) {
-            for (; issued_early < first_round; ++issued_early) issue(c_begin + issued_early, issued_early);
+        if (p.dev_pos == 2) {
+            // No launch that may still run writes this layer (the host's launch
+            // record says so): its lengths are settled and the step proceeds as
+            // one with host positions.
+            pos = p.lens[b];
+            plan();
+            if (warp == NW && lane == 0) {
+                for (; issued_early < first_round && c_begin + issued_early < c_safe; ++issued_early)
+                    issue(c_begin + issued_early, issued_early);
+            }
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        } else {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            pos = p.lens[b];
+            plan();
+            if (warp == NW && lane == 0) {
+                for (; issued_early < first_round; ++issued_early)
+                    issue(c_begin + issued_early, issued_early);
+            }
         }
         prologue();
     }
@@ -443,7 +459,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     if (warp == NW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            bool waited = kDevPos;
+            bool waited = kDevPos && p.dev_pos != 2;
             int issued = issued_early;
             for (; issued < my_chunks; ++issued) {
                 const int st = issued % NS;
@@ -710,7 +726,7 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
 template <int D, int HPC, bool kDevPos>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_kernel(const __grid_constant__ K3Params p) {
-    k3_body<D, HPC, 1, true, kDevPos>(p, nullptr, p.tm_k, p.tm_v, nullptr);
+    k3_body<D, HPC, 1, true, kDevPos>(p, nullptr, &p.tmk, &p.tmv, nullptr);
 }
 
 // Up to TPS new tokens per sequence (HPC x TPS = 8 query rows per CTA).
@@ -722,7 +738,7 @@ struct K3MultiParams {
 template <int D, int HPC, int TPS>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_multi_kernel(const __grid_constant__ K3MultiParams p) {
-    k3_body<D, HPC, TPS, true, false>(p.base, nullptr, p.base.tm_k, p.base.tm_v, &p.mt);
+    k3_body<D, HPC, TPS, true, false>(p.base, nullptr, &p.base.tmk, &p.base.tmv, &p.mt);
 }
 
 template <int D, int HPC, bool kDevPos>
@@ -992,15 +1008,15 @@ static_assert(kNoAllocMaxBatch <= kK3MaxSeqPerLaunch, "positions travel in K3Par
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 struct alignas(64) K3NoAllocParams {
-    CUtensorMap tmk, tmv;              // over the caller's K / V of this layer
+    K3Params base;                     // base.tmk / tmv over the caller's K / V of this layer;
+                                       // base.pos[b]: slot of each sequence's new token
     float2 cs[kNoAllocMaxBatch * 64];  // (cos, sin) at pos[b] of the D/2 frequencies, [b][i]
-    K3Params base;                     // base.pos[b]: slot of each sequence's new token
 };
 
 template <int D, int HPC>
 __global__ void __launch_bounds__((kK3ConsumerWarps + 1) * 32, 2)
     k3_decode_noalloc_kernel(const __grid_constant__ K3NoAllocParams p) {
-    k3_body<D, HPC, 1, false, false>(p.base, p.cs, &p.tmk, &p.tmv, nullptr);
+    k3_body<D, HPC, 1, false, false>(p.base, p.cs, &p.base.tmk, &p.base.tmv, nullptr);
 }
 
 template <int D, int HPC>
@@ -1117,8 +1133,8 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     const int S = k3_choose_splits(D, HPC, groups, pos_max, false, 1);
 
     K3NoAllocParams p{};
-    if (!encode_decode_map(&p.tmk, k_cache, D, g.capacity, g.max_batch * g.n_kv_heads) ||
-        !encode_decode_map(&p.tmv, v_cache, D, g.capacity, g.max_batch * g.n_kv_heads))
+    if (!encode_decode_map(&p.base.tmk, k_cache, D, g.capacity, g.max_batch * g.n_kv_heads) ||
+        !encode_decode_map(&p.base.tmv, v_cache, D, g.capacity, g.max_batch * g.n_kv_heads))
         return QA_ERR_CUDA;
     for (int b = 0; b < batch; ++b) {
         p.base.pos[b] = positions[b];
@@ -1131,8 +1147,6 @@ extern "C" __attribute__((visibility("default"))) qa_status qa_decode_step_noall
     }
     unsigned char *scr = dev->scratch;
     K3Params &bp = p.base;
-    bp.tm_k = nullptr;  // the kernel takes the maps from the parameter block
-    bp.tm_v = nullptr;
     bp.q = static_cast<const __nv_bfloat16 *>(q);
     bp.k = static_cast<const __nv_bfloat16 *>(k);
     bp.v = static_cast<const __nv_bfloat16 *>(v);

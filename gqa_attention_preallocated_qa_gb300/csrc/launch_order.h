@@ -67,6 +67,25 @@ class LaunchOrder {
         return static_cast<int>(std::min<int64_t>(guard, kGuardAll));
     }
 
+    // True when no launch that may still run when the next launch on `stream`
+    // starts appends to (cache, layer): the same walk as admit, nothing recorded.
+    // A launch for which this holds may read that layer's device lengths
+    // before its own wait.
+    bool layer_settled(const void *stream, const void *cache, int layer, int64_t resident_max) {
+        std::lock_guard<std::mutex> lock(mu_);
+        auto found = hist_.find(stream);
+        if (found == hist_.end()) return true;
+        const Hist &h = found->second;
+        int64_t resident = 0;
+        for (auto it = h.recs.rbegin(); it != h.recs.rend(); ++it) {
+            if (it->cache == cache && it->layer == layer) return false;
+            if (!it->early) return true;
+            resident += it->ctas;
+            if (resident + 1 > resident_max) return true;
+        }
+        return !h.truncated;
+    }
+
     // A kernel that never signals early was enqueued on `stream`, or the
     // stream was synchronised.
     void barrier(const void *stream) {

@@ -40,7 +40,7 @@ struct qa_cache {
     uint32_t *seq_cnt = nullptr;  // decode with device lengths: groups done per sequence
     std::vector<int> window;      // per layer: attention window in keys (0: full)
     int overlap = 2;              // decode launches whose clusters the split plan fits at once
-    CUtensorMap *dmaps = nullptr;  // device: [layer][K, V] decode tensor maps
+    std::vector<CUtensorMap> maps;  // [layer][K, V] decode tensor maps (copied into each launch)
     std::vector<int32_t> lens_host;
     uint64_t kv_bytes = 0, scratch_bytes = 0;
     std::atomic<uint64_t> launches[QA_NUM_KERNELS];
@@ -94,7 +94,6 @@ void free_all(qa_cache *c) {
     cudaFree(c->rope);
     cudaFree(c->err);
     cudaFree(c->seq_cnt);
-    cudaFree(c->dmaps);
 }
 
 template <typename T>
@@ -270,8 +269,8 @@ K3Params make_k3(qa_cache *c, int layer, const void *q, const void *k, const voi
                  const void *wq, const void *wk, void *out) {
     const qa_config &g = c->cfg;
     K3Params p{};
-    p.tm_k = c->dmaps + 2 * layer;
-    p.tm_v = c->dmaps + 2 * layer + 1;
+    p.tmk = c->maps[2 * layer];
+    p.tmv = c->maps[2 * layer + 1];
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.k = static_cast<const __nv_bfloat16 *>(k);
     p.v = static_cast<const __nv_bfloat16 *>(v);
@@ -498,17 +497,16 @@ QA_API qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out) {
                  cudaSuccess;
     }
     if (ok) {
-        // Decode tensor maps, two per layer, kept in device memory.
+        // Decode tensor maps, two per layer, kept on the host and copied into the
+        // parameters of every decode launch.
         std::vector<CUtensorMap> maps(static_cast<size_t>(2) * g.num_layers);
         for (int l = 0; ok && l < g.num_layers; ++l)
             ok = qa::encode_decode_map(&maps[2 * l], c->K + l * c->layer_elems, D, g.capacity,
                                        g.max_batch * g.n_kv_heads) &&
                  qa::encode_decode_map(&maps[2 * l + 1], c->V + l * c->layer_elems, D, g.capacity,
                                        g.max_batch * g.n_kv_heads);
-        ok = ok && dev_alloc(&c->dmaps, maps.size(), scr) &&
-             cudaMemcpy(c->dmaps, maps.data(), maps.size() * sizeof(CUtensorMap),
-                        cudaMemcpyHostToDevice) == cudaSuccess &&
-             cudaDeviceSynchronize() == cudaSuccess;
+        ok = ok && cudaDeviceSynchronize() == cudaSuccess;
+        if (ok) c->maps = std::move(maps);
     }
     if (!ok) {
         free_all(c);
@@ -654,7 +652,15 @@ qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const vo
         for (int b = 0; b < batch; ++b)
             if (mirror[b] + 1 > g.capacity) return QA_ERR_CAPACITY;
     K3Params p = make_k3(c, layer, q, k, v, q_norm_w, k_norm_w, out);
-    p.dev_pos = dev_pos ? 1 : 0;
+    const int64_t resident_max = qa::k3_max_resident_ctas();
+    // Device positions: when no launch that may still be running writes this
+    // layer (a multi-layer loop, e.g. a captured layer stack), the kernel reads
+    // them at once and overlaps its predecessor like a host-position step;
+    // otherwise it waits for its predecessor before reading them and nothing
+    // overlaps.
+    const bool settled =
+        dev_pos && g_order.layer_settled(static_cast<cudaStream_t>(stream), c, layer, resident_max);
+    p.dev_pos = dev_pos ? (settled ? 2 : 1) : 0;
     for (int b0 = 0; b0 < batch; b0 += qa::kK3MaxSeqPerLaunch) {
         const int nb = std::min(qa::kK3MaxSeqPerLaunch, batch - b0);
         int pos_max = 0;
@@ -662,14 +668,18 @@ qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const vo
             p.pos[i] = mirror[b0 + i];
             pos_max = std::max(pos_max, mirror[b0 + i]);
         }
+        // The host copy lags behind device positions (a captured step runs at
+        // every later position): plan the splits for a full cache.
+        if (dev_pos) pos_max = g.capacity - 1;
         p.b0 = b0;
         p.B = nb;
-        // With device positions a launch waits for its predecessor before it
-        // streams anything, so nothing overlaps: plan for one launch.
-        p.S = choose_splits(c, nb, pos_max, dev_pos ? 1 : c->overlap);
+        // The cache's overlap setting alone sets the plan (not whether this launch
+        // overlaps), so a captured step and the same step run eagerly agree bit
+        // for bit.
+        p.S = choose_splits(c, nb, pos_max, c->overlap);
         p.guard = g_order.admit(static_cast<cudaStream_t>(stream), c, layer,
-                                p.S * g.n_kv_heads * c->HG * nb, 1, !dev_pos,
-                                qa::k3_max_resident_ctas());
+                                p.S * g.n_kv_heads * c->HG * nb, 1, !dev_pos || settled,
+                                resident_max);
         const qa::FaultPlan f = qa::take_fault(QA_KERNEL_DECODE_ATTN);
         p.fault = f.fault;
         p.wait_ns = f.wait_ns;

@@ -101,8 +101,10 @@ constexpr int kK3MaxTokens = 8;
 // guard value meaning "every cache row may still be written: load all after the wait"
 constexpr int kK3GuardAll = 1 << 30;
 
-struct K3Params {
-    const CUtensorMap *tm_k, *tm_v;  // (D, capacity, max_batch * Hkv) over this layer's K / V
+struct alignas(64) K3Params {
+    // (D, capacity, max_batch * Hkv) over this layer's K / V, in the launch
+    // parameters (no descriptor fetch from global memory before the first copy)
+    CUtensorMap tmk, tmv;
     const __nv_bfloat16 *q, *k, *v;  // [batch][Hq][D], [batch][Hkv][D] (whole call)
     const __nv_bfloat16 *wq, *wk;
     __nv_bfloat16 *kc, *vc;          // layer base
@@ -115,7 +117,9 @@ struct K3Params {
     float eps, scale_log2;
     int b0;                          // first sequence of this launch (blockIdx.z = b - b0)
     int window;                      // attention window in keys (0: the whole cache)
-    int dev_pos;                     // 1: positions are the device lengths (pos unused)
+    int dev_pos;                     // 0: positions from pos[]; 1: the device lengths, read
+                                     // after the launch wait; 2: the device lengths, read at
+                                     // once (no launch still running writes this layer)
     int guard;                       // rows just below each sequence's first new slot that
                                      // a launch still running may write (loaded after the wait)
     uint32_t *seq_cnt;               // [max_batch] groups done per sequence (dev_pos only)

@@ -85,9 +85,9 @@ typedef struct qa_cache qa_cache; /* opaque */
 /* Allocate a cache on the current CUDA device: K and V as bf16
  * [num_layers][max_batch][n_kv_heads][capacity][head_dim] (zero-filled),
  * int32 lengths [num_layers][max_batch] (all zero), an fp32 rotary table
- * [capacity][head_dim/2] of (cos, sin) built on the host in fp64, the decode
- * kernel's TMA tensor maps (two per layer) and per-sequence counters, and an
- * error word.  Synchronous.
+ * [capacity][head_dim/2] of (cos, sin) built on the host in fp64,
+ * per-sequence counters and an error word; the decode kernel's TMA tensor
+ * maps (two per layer) are kept on the host.  Synchronous.
  * Errors: INVALID_ARG (cfg or out null, non-positive sizes),
  * UNSUPPORTED_SHAPE, CUDA (allocation failed; nothing is leaked). */
 qa_status qa_cache_alloc(const qa_config *cfg, qa_cache **out);
@@ -160,16 +160,22 @@ qa_status qa_decode_step(qa_cache *cache, int layer, int batch,
  * every replay, so one graph serves every position.  (No counterpart in the
  * pages; it serves the NEXT item "CUDA-graph-captured multi-layer decode step".)
  * Arguments, layouts and ownership as qa_decode_step.  Differences:
- *  - the kernel reads lens[b] after the previous kernel on the stream has
- *    finished, and the last kv-head group of each sequence sets lens[b] + 1
- *    (a per-sequence counter, reset by qa_cache_reset);
+ *  - the kernel reads lens[b] from the device: at once when no launch that may
+ *    still be running writes this layer (the library's per-stream launch
+ *    record says so; e.g. each layer of a captured multi-layer step), and
+ *    then it overlaps the previous launch like qa_decode_step; otherwise after
+ *    the previous kernel on the stream has finished.  The last kv-head group
+ *    of each sequence sets lens[b] + 1 (a per-sequence counter, reset by
+ *    qa_cache_reset);
  *  - the host copy of the lengths is not advanced (call qa_cache_sync_lengths
  *    before any call that uses it: qa_prefill, qa_decode_step, the split plan);
  *  - a sequence already at capacity is detected on the device: the step does
  *    nothing for that sequence and qa_get_device_error returns
  *    QA_ERR_DEVICE_BOUNDS;
- *  - the split count is planned from the host copy at capture time (any count
- *    is correct; it only sets the speed).
+ *  - the split count is planned for a full cache (capacity) under the cache's
+ *    overlap setting (qa_cache_set_decode_overlap), so a captured step and the
+ *    same step run eagerly give bit-identical results (any count is correct;
+ *    it only sets the speed).
  * Capture requires that the first call on this device for this geometry ran
  * outside capture (it configures the kernel and caches the occupancy query).
  * Errors: INVALID_ARG, ALIGNMENT (host side); DEVICE_BOUNDS (device side). */
@@ -196,9 +202,7 @@ qa_status qa_cache_set_window(qa_cache *cache, int layer, int window);
  * attention launched back to back (a decode loop of attention layers); 1
  * gives an isolated launch, e.g. one between other kernels, the most splits.
  * Any value gives the same result up to the summation order of the split
- * merge.  qa_decode_step_device_lengths, whose launches cannot overlap (they
- * wait for the previous kernel before reading their positions), always plans
- * for 1.  Host-side only, takes effect for launches after the call.
+ * merge.  Host-side only, takes effect for launches after the call.
  * Errors: INVALID_ARG (launches outside 1..8). */
 qa_status qa_cache_set_decode_overlap(qa_cache *cache, int launches);
 

@@ -43,9 +43,11 @@ def test_device_lengths_step_equals_host_position_step(qa, oracle_mod):
     b = prefilled(qa, 1, prompt, cap, [inp])
     lay = oracle_mod.OracleLayer(oracle_mod.Geometry(4, HQ, HKV, D, cap))
     lay.prefill(prompt, F(inp.q), F(inp.k), F(inp.v), F(inp.wq), F(inp.wk))
-    # device-length steps plan their splits for one launch at a time; the same
-    # plan on the host-position side makes the two sums bit-comparable
+    # the same split plan on both sides makes the two sums bit-comparable:
+    # device-length steps plan for a full cache, host-position steps for the
+    # current lengths, and one launch at a time fits the same split count here
     qa.qa_cache_set_decode_overlap(a.h, 1)
+    qa.qa_cache_set_decode_overlap(b.h, 1)
     try:
         for s in range(steps):
             dq, dk, dv = dev(inp.dq[s]), dev(inp.dk[s]), dev(inp.dv[s])
@@ -171,5 +173,40 @@ def test_device_lengths_capacity_is_checked_on_the_device(qa):
         assert list(c.views()[2].cpu().numpy()) == [42, 64]
         st, word = c.device_error()
         assert st == 8 and word != 0  # QA_ERR_DEVICE_BOUNDS
+    finally:
+        c.free()
+
+
+def test_multi_layer_device_length_loop_reads_settled_positions_early(qa, oracle_mod):
+    # Six layers decoded step by step, as a model's layer loop does: when a step
+    # of layer l is launched, no launch still running writes layer l (the ones in
+    # flight are other layers'), so the kernel reads its positions at once and
+    # overlaps the previous launch.  Every output is judged by the oracle, and
+    # the device lengths advance exactly.
+    layers, prompt, cap, steps = 6, (300, 700), 800, 3
+    inps = [layer_inputs(91 + l, prompt, HQ, HKV, D, steps) for l in range(layers)]
+    c = prefilled(qa, layers, prompt, cap, inps)
+    lays = []
+    for inp in inps:
+        lay = oracle_mod.OracleLayer(oracle_mod.Geometry(2, HQ, HKV, D, cap))
+        lay.prefill(prompt, F(inp.q), F(inp.k), F(inp.v), F(inp.wq), F(inp.wk))
+        lays.append(lay)
+    try:
+        ins = [[(dev(i.dq[s]), dev(i.dk[s]), dev(i.dv[s])) for s in range(steps)] for i in inps]
+        ws = [(dev(i.wq), dev(i.wk)) for i in inps]
+        outs = [[torch.empty((2, HQ, D), dtype=torch.bfloat16, device="cuda")
+                 for _ in range(steps)] for _ in range(layers)]
+        torch.cuda.synchronize()
+        for s in range(steps):
+            for l in range(layers):
+                qa.qa_decode_step_device_lengths(c.h, l, 2, *ins[l][s], *ws[l], outs[l][s])
+        torch.cuda.synchronize()
+        for l in range(layers):
+            for s in range(steps):
+                i = inps[l]
+                _, want = lays[l].decode(F(i.dq[s]), F(i.dk[s]), F(i.dv[s]), F(i.wq), F(i.wk))
+                assert_parity(f64(outs[l][s]), want, f"layer {l} step {s}")
+            assert list(c.views(l)[2].cpu().numpy()) == [n + steps for n in prompt]
+        assert c.device_error() == (0, 0)
     finally:
         c.free()
