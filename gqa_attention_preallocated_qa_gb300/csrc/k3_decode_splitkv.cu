@@ -288,9 +288,11 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     const int b = TPS == 1 ? p.b0 + bl : mt->seq[bl];
     const int ntok = TPS == 1 ? 1 : mt->ntok[bl];
     const int qrow0 = TPS == 1 ? b : mt->row0[bl];  // row of token 0 in q, k, v, out
-    // Host positions travel in the parameters; device positions (dev_pos) are
-    // the lengths the previous kernel left, read after the launch wait.
-    int pos = kDevPos ? 0 : p.pos[bl];
+    // Host positions travel in the parameters; device positions are the lengths
+    // an earlier kernel left: read here at once when they are settled (dev_pos
+    // 2: the load's latency overlaps the set-up below), else after the launch
+    // wait.  Every CTA of the sequence reads them before any writes them back.
+    int pos = kDevPos ? (p.dev_pos == 2 ? p.lens[b] : 0) : p.pos[bl];
     const int S = p.S;
 
     // Merge geometry.  The CTA's R x D outputs are dealt to the S CTAs of the
@@ -428,9 +430,8 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     } else {
         if (p.dev_pos == 2) {
             // No launch that may still run writes this layer (the host's launch
-            // record says so): its lengths are settled and the step proceeds as
-            // one with host positions.
-            pos = p.lens[b];
+            // record says so): its lengths are settled (read above) and the step
+            // proceeds as one with host positions.
             plan();
             if (warp == NW && lane == 0) {
                 for (; issued_early < first_round && c_begin + issued_early < c_safe; ++issued_early)

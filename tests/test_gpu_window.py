@@ -114,3 +114,49 @@ def test_window_longer_than_every_sequence_is_full_attention(qa):
             c.free()
     for a, b in zip(*res):
         np.testing.assert_array_equal(a, b)
+
+
+def test_window_1024_over_2048_prompts_and_decode(qa, oracle_mod):
+    # The sliding window of the A10G reproduction repo's stack (1024 keys) over
+    # prompts of 2048 and 1500 tokens, then decode steps past the prompt: rows
+    # around the tile and window boundaries, on three heads, and every decode
+    # output against attention over exactly the window's keys.
+    window, prompt, steps = 1024, (2048, 1500), 3
+    cap = max(prompt) + steps
+    inp = layer_inputs(107, prompt, HQ, HKV, D, steps)
+    B = len(prompt)
+    c = GpuCache(qa, 1, B, HQ, HKV, D, cap)
+    orc = WindowOracle(oracle_mod, B, HQ, HKV, D, cap, inp.wq, inp.wk, window=window)
+    rng = np.random.default_rng(1024)
+    try:
+        qa.qa_cache_set_window(c.h, 0, window)
+        q, k, v, wq, wk = (dev(a) for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+        out = torch.empty_like(q)
+        qa.qa_prefill(c.h, 0, list(prompt), q, k, v, wq, wk, out)
+        torch.cuda.synchronize()
+        got, qf = f64(out), F(inp.q)
+        want, have, t0 = [], [], 0
+        for b, L in enumerate(prompt):
+            orc.append(b, F(inp.k[t0:t0 + L]), F(inp.v[t0:t0 + L]))
+            rows = {0, 127, 128, 1022, 1023, 1024, 1025, 1151, 1152, L - 129, L - 1}
+            rows |= set(rng.integers(0, L, size=8).tolist())
+            for i in sorted(r for r in rows if r < L):
+                for h in (0, 13, 31):
+                    want.append(orc.out_row(b, i, h, qf[t0 + i, h]))
+                    have.append(got[t0 + i, h])
+            t0 += L
+        assert_parity(np.array(have), np.array(want), "window 1024 prefill")
+        for s in range(steps):
+            dq, dk, dv = dev(inp.dq[s]), dev(inp.dk[s]), dev(inp.dv[s])
+            o = torch.empty_like(dq)
+            qa.qa_decode_step(c.h, 0, B, dq, dk, dv, wq, wk, o)
+            torch.cuda.synchronize()
+            want = []
+            for b in range(B):
+                orc.append(b, F(inp.dk[s][b][None]), F(inp.dv[s][b][None]))
+                want.append([orc.out_row(b, orc.lens[b] - 1, h, F(inp.dq[s][b, h]))
+                             for h in range(HQ)])
+            assert_parity(f64(o), np.array(want), f"window 1024 decode step {s}")
+        assert c.device_error() == (0, 0)
+    finally:
+        c.free()
