@@ -620,6 +620,8 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
             V[:, :, :pt.L] = cv
             qa.qa_cache_set_lengths(h, layer, [pt.L] * pt.B)
         del ck, cv
+        if args.sweep_overlap:
+            qa.qa_cache_set_decode_overlap(h, args.sweep_overlap)
         q, k, v, wq, wk = (dev(a) for a in (inp.dq[0], inp.dk[0], inp.dv[0], inp.wq, inp.wk))
         out = torch.empty_like(q)
         stream = torch.cuda.current_stream()
@@ -681,7 +683,7 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
                         "how": "median of per-launch events; a spacer kernel before each launch, "
                                "layers cycled (HBM-cold), split plan for one launch, the host "
                                "ahead of the device"}
-            qa.qa_cache_set_decode_overlap(h, 2)
+            qa.qa_cache_set_decode_overlap(h, args.sweep_overlap or 4)
         # the same on one layer, for reference (its K/V may stay in L2)
         n1 = same_steps
         e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -693,7 +695,7 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
         if st or qa.qa_get_device_error(h)[0]:
             raise RuntimeError(f"decode sweep point {pt.name} failed")
         points.append({"sweep": pt.name, "B": pt.B, "L": pt.L, "steps": steps, "layers": NL,
-                       "splits": splits, "us_per_step": round(us, 3),
+                       "splits": splits, "overlap": args.sweep_overlap or 4, "us_per_step": round(us, 3),
                        "host_us_per_call": round(host_us, 3),
                        "kv_bytes_per_step": round(byts), "hbm_gbs": round(gbs, 1),
                        "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
@@ -1032,6 +1034,9 @@ def main():
                     help="decode-only sweep over batch 1/4 and cache lengths 512..16384")
     ap.add_argument("--sweep-steps", type=int, default=1000,
                     help="timed decode steps per sweep point")
+    ap.add_argument("--sweep-overlap", type=int, default=0,
+                    help="decode launches the split plan fits at once in the sweep "
+                         "(qa_cache_set_decode_overlap; 0: the library's default)")
     ap.add_argument("--verify", action="store_true",
                     help="k-token verify (chunked prefill) vs k decode steps, B=4, L=2048")
     ap.add_argument("--graph", action="store_true",

@@ -642,7 +642,73 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     // Once every source's bytes have landed: per row of the run (one warp
     // each), w_i = 2^((m_i - M) c) with M = max_i m_i and 1 / sum_i w_i l_i;
     // then each output of the run is sum_i w_i o_i times that, over the sources
-    // in a fixed order (deterministic).
+    // in a fixed order (deterministic).  The merge reads only this cluster's
+    // shared memory, so it runs before the launch wait, and only the global
+    // writes (cache slots, lengths, outputs) follow the wait: the part of a step
+    // that waits for the previous kernel's end is a few stores.
+    constexpr int kThreadsK3 = (NW + 1) * 32;
+    constexpr int kOutPer = (R * D + kThreadsK3 - 1) / kThreadsK3;  // outputs per thread, at most
+    float res[kOutPer];
+    bool merged = E_me > 0;
+    if (E_me > 0) {
+        bool ok = mbar_wait_cluster(smem_u32(&bar_recv), 0, &s_abort, p.err, kKernK3, 5, p.wait_ns);
+        if (!ok) {
+            // Given up (this CTA timed out somewhere): the peers still push their
+            // partials here, so every inbound st.async must land before this CTA
+            // exits and its shared memory goes away.  Bounded like every wait.
+            int dummy = 0;
+            mbar_wait_cluster(smem_u32(&bar_recv), 0, &dummy, p.err, kKernK3, 6, p.wait_ns);
+        }
+        merged = __syncthreads_and(ok);
+        if (merged) {
+            const float c = p.scale_log2;
+            constexpr int kPerLane = (kK3MaxSplits + 31) / 32;
+            for (int hl = warp; hl < nh_me; hl += NW + 1) {
+                const float *ml = rcv_ml + 2 * (g_lo + hl);  // source i: ml[2 * R * i], l after it
+                float mi[kPerLane], M = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < kPerLane; ++k) {
+                    const int i = lane + 32 * k;
+                    mi[k] = i < NSRC ? ml[2 * R * i] : -INFINITY;
+                    M = fmaxf(M, mi[k]);
+                }
+#pragma unroll
+                for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o2));
+                float Ls = 0.f;
+#pragma unroll
+                for (int k = 0; k < kPerLane; ++k) {
+                    const int i = lane + 32 * k;
+                    if (i < NSRC) {
+                        const float w = mi[k] == -INFINITY ? 0.f : ex2((mi[k] - M) * c);
+                        s_w[hl * kK3MaxSplits + i] = w;
+                        Ls = fmaf(w, ml[2 * R * i + 1], Ls);
+                    }
+                }
+#pragma unroll
+                for (int o2 = 16; o2 >= 1; o2 >>= 1) Ls += __shfl_xor_sync(FULL, Ls, o2);
+                if (lane == 0) s_linv[hl] = 1.f / Ls;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < kOutPer; ++j) {
+                const int k = threadIdx.x + j * kThreadsK3;
+                res[j] = 0.f;
+                if (k < E_me) {
+                    const int e = e_lo + k, g = e / D, hl = g - g_lo;
+                    const float *w = s_w + hl * kK3MaxSplits;
+                    const float *src = rcv_o + k;
+                    float O4[4] = {0.f, 0.f, 0.f, 0.f};  // four running sums, in a fixed order
+                    int i = 0;
+                    for (; i + 4 <= NSRC; i += 4) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) O4[u] = fmaf(w[i + u], src[(i + u) * E], O4[u]);
+                    }
+                    for (; i < NSRC; ++i) O4[0] = fmaf(w[i], src[i * E], O4[0]);
+                    res[j] = ((O4[0] + O4[1]) + (O4[2] + O4[3])) * s_linv[hl];
+                }
+            }
+        }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");  // before any global write below
     if (owner && hg == 0 && warp == NW && lane < LPR) {
         // Slots pos.. of the cache, read only by later launches.
@@ -656,70 +722,25 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
     if constexpr (kTableRope && !kDevPos) {
         if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.lens[b] = pos + ntok;
     }
-    if (E_me > 0) {
-        bool ok = mbar_wait_cluster(smem_u32(&bar_recv), 0, &s_abort, p.err, kKernK3, 5, p.wait_ns);
-        if (!ok) {
-            // Given up (this CTA timed out somewhere): the peers still push their
-            // partials here, so every inbound st.async must land before this CTA
-            // exits and its shared memory goes away.  Bounded like every wait.
-            int dummy = 0;
-            mbar_wait_cluster(smem_u32(&bar_recv), 0, &dummy, p.err, kKernK3, 6, p.wait_ns);
+    if (!merged) return;
+    if (kDevPos && split == 0 && threadIdx.x == 0) {
+        // Every CTA of this group has pushed, so it has read lens[b]: count the
+        // group towards sequence b; the last group of the sequence advances it.
+        const uint32_t prev = atomic_inc_acq_rel(p.seq_cnt + b);
+        if (prev == static_cast<uint32_t>(p.Hkv * p.HG) - 1u) {
+            p.lens[b] = pos + 1;
+            p.seq_cnt[b] = 0u;
         }
-        ok = __syncthreads_and(ok);
-        if (!ok) return;
-        if (kDevPos && split == 0 && threadIdx.x == 0) {
-            // Every CTA of this group has pushed, so it has read lens[b]: count the
-            // group towards sequence b; the last group of the sequence advances it.
-            const uint32_t prev = atomic_inc_acq_rel(p.seq_cnt + b);
-            if (prev == static_cast<uint32_t>(p.Hkv * p.HG) - 1u) {
-                p.lens[b] = pos + 1;
-                p.seq_cnt[b] = 0u;
-            }
-        }
-        const float c = p.scale_log2;
-        constexpr int kPerLane = (kK3MaxSplits + 31) / 32;
-        for (int hl = warp; hl < nh_me; hl += NW + 1) {
-            const float *ml = rcv_ml + 2 * (g_lo + hl);  // source i: ml[2 * R * i], l after it
-            float mi[kPerLane], M = -INFINITY;
+    }
 #pragma unroll
-            for (int k = 0; k < kPerLane; ++k) {
-                const int i = lane + 32 * k;
-                mi[k] = i < NSRC ? ml[2 * R * i] : -INFINITY;
-                M = fmaxf(M, mi[k]);
-            }
-#pragma unroll
-            for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o2));
-            float Ls = 0.f;
-#pragma unroll
-            for (int k = 0; k < kPerLane; ++k) {
-                const int i = lane + 32 * k;
-                if (i < NSRC) {
-                    const float w = mi[k] == -INFINITY ? 0.f : ex2((mi[k] - M) * c);
-                    s_w[hl * kK3MaxSplits + i] = w;
-                    Ls = fmaf(w, ml[2 * R * i + 1], Ls);
-                }
-            }
-#pragma unroll
-            for (int o2 = 16; o2 >= 1; o2 >>= 1) Ls += __shfl_xor_sync(FULL, Ls, o2);
-            if (lane == 0) s_linv[hl] = 1.f / Ls;
-        }
-        __syncthreads();
-        for (int k = threadIdx.x; k < E_me; k += blockDim.x) {
-            const int e = e_lo + k, g = e / D, d = e % D, hl = g - g_lo;
+    for (int j = 0; j < kOutPer; ++j) {
+        const int k = threadIdx.x + j * kThreadsK3;
+        if (k < E_me) {
+            const int e = e_lo + k, g = e / D, d = e % D;
             const int t = g / HPC, hh = g % HPC;
-            if (t >= ntok) continue;
-            const float *w = s_w + hl * kK3MaxSplits;
-            const float *src = rcv_o + k;
-            float O4[4] = {0.f, 0.f, 0.f, 0.f};  // four running sums, added in a fixed order
-            int i = 0;
-            for (; i + 4 <= NSRC; i += 4) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) O4[u] = fmaf(w[i + u], src[(i + u) * E], O4[u]);
-            }
-            for (; i < NSRC; ++i) O4[0] = fmaf(w[i], src[i * E], O4[0]);
-            const float O = (O4[0] + O4[1]) + (O4[2] + O4[3]);
-            p.out[(static_cast<int64_t>(qrow0 + t) * p.Hq + h_first + hh) * D + d] =
-                __float2bfloat16_rn(O * s_linv[hl]);
+            if (t < ntok)
+                p.out[(static_cast<int64_t>(qrow0 + t) * p.Hq + h_first + hh) * D + d] =
+                    __float2bfloat16_rn(res[j]);
         }
     }
 }

@@ -86,6 +86,18 @@ class LaunchOrder {
         return !h.truncated;
     }
 
+    // What the next launch on `stream` may run beside: 0 nothing (no launch
+    // recorded since the last barrier), 1 launches of other layers only, 2 a
+    // launch that appends to (cache, layer).
+    int in_flight(const void *stream, const void *cache, int layer, int64_t resident_max) {
+        {
+            std::lock_guard<std::mutex> lock(mu_);
+            auto found = hist_.find(stream);
+            if (found == hist_.end() || found->second.recs.empty()) return 0;
+        }
+        return layer_settled(stream, cache, layer, resident_max) ? 1 : 2;
+    }
+
     // A kernel that never signals early was enqueued on `stream`, or the
     // stream was synchronised.
     void barrier(const void *stream) {

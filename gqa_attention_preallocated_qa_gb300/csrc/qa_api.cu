@@ -39,7 +39,8 @@ struct qa_cache {
     uint32_t *err = nullptr;
     uint32_t *seq_cnt = nullptr;  // decode with device lengths: groups done per sequence
     std::vector<int> window;      // per layer: attention window in keys (0: full)
-    int overlap = 2;              // decode launches whose clusters the split plan fits at once
+    int overlap = 4;              // decode launches whose clusters the split plan fits at once
+    bool overlap_fixed = false;   // set by qa_cache_set_decode_overlap: no per-launch choice
     std::vector<CUtensorMap> maps;  // [layer][K, V] decode tensor maps (copied into each launch)
     std::vector<int32_t> lens_host;
     uint64_t kv_bytes = 0, scratch_bytes = 0;
@@ -174,6 +175,21 @@ bool qa::encode_decode_map(CUtensorMap *m, void *base, int D, int capacity, int 
 }
 
 namespace {
+
+// The launches a host-position decode launch plans room for (unless the caller
+// fixed the number with qa_cache_set_decode_overlap): one when nothing may still
+// run beside it, two when launches on its own layer may (a single-layer loop:
+// the rows they append are read only after the wait, so fewer launches overlap
+// usefully), and the cache's setting when only other layers' launches may (a
+// loop over layers).
+int plan_overlap(const qa_cache *c, cudaStream_t stream, int layer, int64_t resident_max) {
+    if (c->overlap_fixed) return c->overlap;
+    switch (g_order.in_flight(stream, c, layer, resident_max)) {
+        case 0: return 1;
+        case 2: return std::min(2, c->overlap);
+        default: return c->overlap;
+    }
+}
 
 // overlap: launches whose clusters should fit at once (see qa_cache_set_decode_overlap).
 int choose_splits(const qa_cache *c, int batch, int pos_max, int overlap) {
@@ -314,11 +330,13 @@ qa_status run_multi(qa_cache *c, int layer, int batch, const int32_t *lens, int 
     std::vector<std::pair<K3Params, qa::K3Multi>> launches;
     qa::K3Multi m{};
     int nz = 0, row = 0, pos_max = 0;
+    const int resident_max = qa::k3_max_resident_ctas();
+    const int ov = plan_overlap(c, s, layer, resident_max);
     auto flush = [&]() {
         if (nz == 0) return;
         p.B = nz;
         p.S = qa::k3_choose_splits(g.head_dim, HPC, nz * g.n_kv_heads * p.HG, pos_max, true,
-                                   c->overlap);
+                                   launches.empty() ? ov : std::min(2, ov));
         launches.emplace_back(p, m);
         nz = 0;
         pos_max = 0;
@@ -335,7 +353,6 @@ qa_status run_multi(qa_cache *c, int layer, int batch, const int32_t *lens, int 
         row += lens[b];
     }
     flush();
-    const int resident_max = qa::k3_max_resident_ctas();
     for (auto &l : launches) {
         int tm = 0;
         for (int z = 0; z < l.first.B; ++z) tm = std::max(tm, l.second.ntok[z]);
@@ -673,10 +690,13 @@ qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const vo
         if (dev_pos) pos_max = g.capacity - 1;
         p.b0 = b0;
         p.B = nb;
-        // The cache's overlap setting alone sets the plan (not whether this launch
-        // overlaps), so a captured step and the same step run eagerly agree bit
-        // for bit.
-        p.S = choose_splits(c, nb, pos_max, c->overlap);
+        // Device positions: the cache's overlap setting alone sets the plan (not
+        // what runs beside the launch), so a captured step and the same step run
+        // eagerly agree bit for bit.  Host positions: the plan follows the stream.
+        p.S = choose_splits(c, nb, pos_max,
+                            dev_pos ? c->overlap
+                                    : plan_overlap(c, static_cast<cudaStream_t>(stream), layer,
+                                                   resident_max));
         p.guard = g_order.admit(static_cast<cudaStream_t>(stream), c, layer,
                                 p.S * g.n_kv_heads * c->HG * nb, 1, !dev_pos || settled,
                                 resident_max);
@@ -708,6 +728,7 @@ QA_API qa_status qa_decode_step_device_lengths(qa_cache *c, int layer, int batch
 QA_API qa_status qa_cache_set_decode_overlap(qa_cache *c, int launches) {
     if (!c || launches < 1 || launches > 8) return QA_ERR_INVALID_ARG;
     c->overlap = launches;
+    c->overlap_fixed = true;
     return QA_OK;
 }
 

@@ -4,6 +4,8 @@
 //   barrier <stream>
 //   clear
 //   fill <stream> <cache> <layer> <n>   (n admits of one block each, outputs nothing)
+//   settled <stream> <cache> <layer> <resident_max>  -> 0 | 1
+//   inflight <stream> <cache> <layer> <resident_max> -> 0 | 1 | 2
 #include <cstdint>
 #include <iostream>
 #include <sstream>
@@ -30,6 +32,15 @@ int main() {
             uintptr_t s;
             in >> s;
             order.barrier(reinterpret_cast<const void *>(s));
+        } else if (cmd == "settled" || cmd == "inflight") {
+            uintptr_t s, c;
+            int layer;
+            long long rmax;
+            in >> s >> c >> layer >> rmax;
+            const void *sp = reinterpret_cast<const void *>(s), *cp = reinterpret_cast<const void *>(c);
+            std::cout << (cmd == "settled" ? int(order.layer_settled(sp, cp, layer, rmax))
+                                           : order.in_flight(sp, cp, layer, rmax))
+                      << "\n";
         } else if (cmd == "clear") {
             order.clear();
         } else if (cmd == "fill") {

@@ -91,3 +91,32 @@ def test_unknown_history_loads_everything_after_the_wait(driver):
     assert driver(lines) == [GUARD_ALL]
     lines = [f"fill 1 7 1 {CAP + 5}", "barrier 1", admit(0, 1, rmax=1 << 40)]
     assert driver(lines) == [0]
+
+
+def settled(layer, rmax=304, stream=1, cache=7):
+    return f"settled {stream} {cache} {layer} {rmax}"
+
+
+def inflight(layer, rmax=304, stream=1, cache=7):
+    return f"inflight {stream} {cache} {layer} {rmax}"
+
+
+def test_settled_layers_may_read_device_lengths_early(driver):
+    # nothing recorded: settled; the layer's own launch possibly running: not
+    assert driver([settled(0), admit(0, 100), settled(0), settled(1)]) == [1, 0, 0, 1]
+    # a loop over layers: layer 0's previous launch is beyond the resident bound
+    # once 304 blocks of later launches sit in between
+    lines = [admit(l, 128) for l in range(4)] + [settled(0), settled(2), settled(3)]
+    assert driver(lines) == [0, 0, 0, 0, 1, 0, 0]
+    # a launch that signals only after its own wait may still run, nothing before it
+    lines = [admit(0, 10), admit(1, 10, early=0), settled(0), settled(1)]
+    assert driver(lines) == [0, 0, 1, 0]
+    # a barrier settles everything; an unknown (truncated) history settles nothing
+    assert driver([admit(0, 10), "barrier 1", settled(0)]) == [0, 1]
+    assert driver([f"fill 1 7 1 {CAP + 5}", settled(0, rmax=1 << 40)]) == [0]
+
+
+def test_in_flight_classifies_what_may_run_beside_the_next_launch(driver):
+    lines = [inflight(0), admit(0, 100), inflight(0), inflight(1), "barrier 1", inflight(0),
+             admit(1, 100, stream=2), inflight(0), inflight(0, stream=2)]
+    assert driver(lines) == [0, 0, 2, 1, 0, 0, 0, 1]
