@@ -793,79 +793,89 @@ def run_verify(args):
 
 
 def run_graph(args):
-    """The multi-layer decode step of the 36-layer ragged workload (B = 4,
-    prompt lengths 512/1024/1536/2048, cache capacity 2112): 36 layer decode
-    steps per generated token, eager through qa_decode_step (host positions),
-    and captured once as a CUDA graph of qa_decode_step_device_lengths calls
-    and replayed (positions advance on the device).  The caches hold seeded
-    N(0,1) keys/values (timing only; parity of this path is in the tests); at
-    1.25 GB they do not fit in L2, so every layer reads its K/V from HBM.  One
-    JSON line: µs per 36-layer step each way and per layer."""
+    """The multi-layer decode step: 36 attention layers, one decode step each per
+    generated token, three ways: eager through qa_decode_step as a caller runs
+    it (the host issues every call, so the slower of host and device sets the
+    pace), the same with the host ahead of the device (device time), and one CUDA
+    graph of 36 qa_decode_step_device_lengths calls replayed once per token
+    (positions advance on the device; no host work per layer).  Two workloads:
+    the 36-layer ragged one (B = 4, prompts 512/1024/1536/2048, capacity 2112,
+    1.25 GB of caches) and B = 1 with a 1024-token prompt (capacity 1088).  The
+    caches hold seeded N(0,1) keys/values (timing only; parity of this path is
+    in the tests) and are far larger than L2 or cycled through 36 layers, so
+    every layer reads its K/V from HBM.  One JSON line per workload."""
     import torch
 
     from gqa_attention_preallocated_qa_gb300 import binding as qa
-    from gqa_attention_preallocated_qa_gb300.configs import RAGGED_36L as w
+    from gqa_attention_preallocated_qa_gb300.configs import RAGGED_36L, Workload
 
     steps = 20
     stream = torch.cuda.current_stream()
-    res = {}
-    for mode in ("eager", "graph"):
-        h = qa.qa_cache_alloc(w.layers, w.B, w.Hq, w.Hkv, w.D, w.cap, w.theta, w.eps)
-        gen = torch.Generator(device="cuda").manual_seed(w.seed)
-        bufs = []
-        for l in range(w.layers):  # caches hold the prompts' lengths of N(0,1) keys/values
-            K, V, _ = qa.cache_tensors(h, l, w.B, w.Hkv, w.cap, w.D)
-            K.normal_(generator=gen)
-            V.normal_(generator=gen)
-            qa.qa_cache_set_lengths(h, l, list(w.prompt_lens))
+    b1 = Workload("qwen3_4b_b1_p1024_36layers", B=1, Hq=32, Hkv=8, D=128, prompt_lens=(1024,),
+                  steps=64, cap=1088, layers=36, seed=6)
+    for w in (RAGGED_36L, b1):
+        res = {}
+        for mode in ("eager_host_paced", "eager", "eager_device_lengths", "graph"):
+            h = qa.qa_cache_alloc(w.layers, w.B, w.Hq, w.Hkv, w.D, w.cap, w.theta, w.eps)
+            gen = torch.Generator(device="cuda").manual_seed(w.seed)
+            bufs = []
+            for l in range(w.layers):  # caches hold the prompts' lengths of N(0,1) keys/values
+                K, V, _ = qa.cache_tensors(h, l, w.B, w.Hkv, w.cap, w.D)
+                K.normal_(generator=gen)
+                V.normal_(generator=gen)
+                qa.qa_cache_set_lengths(h, l, list(w.prompt_lens))
 
-            def rnd(*shape):
-                return torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
-            bufs.append((rnd(w.B, w.Hq, w.D), rnd(w.B, w.Hkv, w.D), rnd(w.B, w.Hkv, w.D),
-                         (1 + 0.1 * rnd(w.D).float()).to(torch.bfloat16),
-                         (1 + 0.1 * rnd(w.D).float()).to(torch.bfloat16),
-                         torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")))
-        torch.cuda.synchronize()
-        lib = qa.lib
-        ptrs = [[t.data_ptr() for t in b] for b in bufs]
-        fn = lib.qa_decode_step if mode == "eager" else lib.qa_decode_step_device_lengths
+                def rnd(*shape):
+                    return torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+                bufs.append((rnd(w.B, w.Hq, w.D), rnd(w.B, w.Hkv, w.D), rnd(w.B, w.Hkv, w.D),
+                             (1 + 0.1 * rnd(w.D).float()).to(torch.bfloat16),
+                             (1 + 0.1 * rnd(w.D).float()).to(torch.bfloat16),
+                             torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")))
+            torch.cuda.synchronize()
+            lib = qa.lib
+            ptrs = [[t.data_ptr() for t in b] for b in bufs]
+            fn = (lib.qa_decode_step if mode in ("eager_host_paced", "eager")
+                  else lib.qa_decode_step_device_lengths)
 
-        def step(sh):
-            st = 0
-            for l in range(w.layers):
-                st |= fn(h, l, w.B, *ptrs[l], sh)
-            return st
-        st = step(stream.cuda_stream)  # warm-up (configures the kernels outside capture)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if mode == "eager":
-            e0.record(stream)
-            for _ in range(steps):
-                st |= step(stream.cuda_stream)
-            e1.record(stream)
-        else:
-            g = torch.cuda.CUDAGraph()
-            side = torch.cuda.Stream()
-            side.wait_stream(stream)
-            with torch.cuda.stream(side):
-                with torch.cuda.graph(g):
-                    st |= step(torch.cuda.current_stream().cuda_stream)
-            stream.wait_stream(side)
-            g.replay()  # first replay outside the timing
-            e0.record(stream)
-            for _ in range(steps):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if st or qa.qa_get_device_error(h)[0]:
-            raise RuntimeError(f"graph bench ({mode}) failed")
-        res[mode] = e0.elapsed_time(e1) * 1e3 / steps
-        qa.qa_cache_free(h)
-    print(json.dumps({"graph": "ragged_36l_b4", "layers": w.layers, "batch": w.B,
-                      "eager_us_per_step": round(res["eager"], 1),
-                      "graph_us_per_step": round(res["graph"], 1),
-                      "eager_us_per_layer": round(res["eager"] / w.layers, 2),
-                      "graph_us_per_layer": round(res["graph"] / w.layers, 2)}), flush=True)
+            def step(sh):
+                st = 0
+                for l in range(w.layers):
+                    st |= fn(h, l, w.B, *ptrs[l], sh)
+                return st
+            st = step(stream.cuda_stream)  # warm-up (configures the kernels outside capture)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if mode != "graph":
+                if mode != "eager_host_paced":
+                    host_ahead(steps * w.layers)
+                e0.record(stream)
+                for _ in range(steps):
+                    st |= step(stream.cuda_stream)
+                e1.record(stream)
+            else:
+                g = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream()
+                side.wait_stream(stream)
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(g):
+                        st |= step(torch.cuda.current_stream().cuda_stream)
+                stream.wait_stream(side)
+                g.replay()  # first replay outside the timing
+                e0.record(stream)
+                for _ in range(steps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            if st or qa.qa_get_device_error(h)[0]:
+                raise RuntimeError(f"graph bench ({mode}) failed")
+            res[mode] = e0.elapsed_time(e1) * 1e3 / steps
+            qa.qa_cache_free(h)
+        print(json.dumps({"graph": w.name, "layers": w.layers, "batch": w.B,
+                          **{f"{m}_us_per_token": round(v, 1) for m, v in res.items()},
+                          "graph_us_per_layer": round(res["graph"] / w.layers, 2),
+                          "timing": "eager_host_paced: as a caller runs it; eager and "
+                                    "eager_device_lengths: the host ahead of the device "
+                                    "(device time); graph: replays back to back"}), flush=True)
 
 
 def run_window(args):

@@ -431,13 +431,14 @@ __device__ __forceinline__ void k3_body(const K3Params &p, const float2 *cs_arr,
         if (p.dev_pos == 2) {
             // No launch that may still run writes this layer (the host's launch
             // record says so): its lengths are settled (read above) and the step
-            // proceeds as one with host positions.
+            // proceeds as one with host positions, signalling the next launch at
+            // once.
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             plan();
             if (warp == NW && lane == 0) {
                 for (; issued_early < first_round && c_begin + issued_early < c_safe; ++issued_early)
                     issue(c_begin + issued_early, issued_early);
             }
-            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         } else {
             asm volatile("griddepcontrol.wait;" ::: "memory");
             asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
