@@ -16,9 +16,14 @@
 // section points at: the normalised vector is rounded to bf16 before the
 // weight multiply, and the product is rounded to bf16 again.  RoPE is then
 // computed in fp32 from an fp64-derived (cos, sin) table and rounded once.
+#include <algorithm>
+#include <atomic>
+
 #include "qa_device.cuh"
 
 namespace qa {
+
+cudaError_t launch_k1_rows(const K1Params &p, int D, cudaStream_t stream);
 
 // Head rows handled by one row group (LPR lanes): all their loads are issued
 // before any arithmetic, so each lane keeps kRowsPerGroup 16-byte loads in flight.
@@ -143,7 +148,213 @@ __global__ void __launch_bounds__(256, 4) k1_norm_rope_append_kernel(const __gri
     }
 }
 
+// ==================================================================== token-tiled form
+// Every warp owns a two-stage ring in shared memory and walks its own share of
+// the tokens (token t goes to warp t mod (CTAs x warps)).  Lane 0 copies a
+// token's q, k and v rows (three contiguous runs of the packed input) into the
+// next stage with bulk copies completing on the stage's mbarrier while the
+// warp transforms the current stage in place (RMSNorm + RoPE of the q and k
+// rows, the cast placement of the per-block form); the normed, rotated
+// queries go out in one bulk store, and the k' and v rows to their cache
+// slots with 16-byte stores (one row of 256 bytes per 16 lanes).  A stage is
+// refilled only after the bulk store of its previous token has read it.
+// Bytes in flight: a token (12 KB at the Qwen3-4B geometry) per warp, eight
+// warps per SM.
+__device__ __forceinline__ uint4 k1_norm_rope16(uint4 xv, uint4 wv, const float4 (&cs)[4], float eps,
+                                               int sub, int lpr) {
+    const unsigned FULL = 0xffffffffu;
+    const int half = lpr / 2;
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    float x[8], wf[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = bf16lo(xw[e]);
+        x[2 * e + 1] = bf16hi(xw[e]);
+        wf[2 * e] = bf16lo(ww[e]);
+        wf[2 * e + 1] = bf16hi(ww[e]);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+    for (int o = half; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+    const float rr = rsqrtf(ss * (1.0f / static_cast<float>(lpr * 8)) + eps);
+    uint32_t yw[4], pw[4], ow[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        yw[e] = pack_bf16(wf[2 * e] * round_bf16(x[2 * e] * rr),
+                          wf[2 * e + 1] * round_bf16(x[2 * e + 1] * rr));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pw[e] = __shfl_xor_sync(FULL, yw[e], half);
+    const bool lower = (sub % lpr) < half;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float y0 = bf16lo(yw[e]), y1 = bf16hi(yw[e]);
+        const float q0 = bf16lo(pw[e]), q1 = bf16hi(pw[e]);
+        const float r0 = lower ? y0 * cs[e].x - q0 * cs[e].y : y0 * cs[e].x + q0 * cs[e].y;
+        const float r1 = lower ? y1 * cs[e].z - q1 * cs[e].w : y1 * cs[e].z + q1 * cs[e].w;
+        ow[e] = pack_bf16(r0, r1);
+    }
+    return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
+constexpr int kK1TWarps = 8;  // warps per CTA, one CTA per SM
+
+template <int D>
+__global__ void __launch_bounds__(kK1TWarps * 32, 1)
+    k1t_norm_rope_append_kernel(const __grid_constant__ K1Params p) {
+    constexpr int LPR = D / 8;     // lanes per head row
+    constexpr int RPW = 32 / LPR;  // rows per warp pass
+    constexpr int HALF = LPR / 2;
+    const unsigned FULL = 0xffffffffu;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar[kK1TWarps * 2];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane % LPR, grp = lane / LPR;
+    const uint32_t qbytes = static_cast<uint32_t>(p.Hq) * D * 2;
+    const uint32_t kvbytes = static_cast<uint32_t>(p.Hkv) * D * 2;
+    const uint32_t stage_bytes = (qbytes + 2 * kvbytes + 127) & ~127u;
+    uint8_t *ring = smem + static_cast<size_t>(warp) * 2 * stage_bytes;
+    const uint32_t bar0 = smem_u32(&bar[2 * warp]);
+
+    if (blockIdx.x == 0 && threadIdx.x < p.nseq)
+        p.lens[p.seq_slot0 + threadIdx.x] =
+            p.start[threadIdx.x] + p.cu[threadIdx.x + 1] - p.cu[threadIdx.x];
+    if (lane == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const uint4 wqv = __ldg(reinterpret_cast<const uint4 *>(p.wq) + sub);
+    const uint4 wkv = __ldg(reinterpret_cast<const uint4 *>(p.wk) + sub);
+
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kK1TWarps;
+    int64_t t = static_cast<int64_t>(blockIdx.x) * kK1TWarps + warp;
+    auto load = [&](int64_t tok, int s) {  // lane 0 only
+        const uint32_t dst = smem_u32(ring + s * stage_bytes);
+        const uint32_t b = bar0 + 8 * s;
+        mbar_expect_tx(b, qbytes + 2 * kvbytes);
+        bulk_g2s(dst, p.q + tok * p.Hq * D, qbytes, b);
+        bulk_g2s(dst + qbytes, p.k + tok * p.Hkv * D, kvbytes, b);
+        bulk_g2s(dst + qbytes + kvbytes, p.v + tok * p.Hkv * D, kvbytes, b);
+    };
+    if (lane == 0 && t < p.T) load(t, 0);
+    int abort_flag = 0;  // each warp gives up on its own
+    int i = 0;
+    bool ok = true;
+    for (; t < p.T; ++i, t += stride) {
+        const int s = i & 1;
+        const int64_t tn = t + stride;
+        if (lane == 0 && tn < p.T) {
+            bulk_wait_read_all();  // the query store of the stage's previous token has read it
+            load(tn, s ^ 1);
+        }
+        ok = mbar_wait(bar0 + 8 * s, (i >> 1) & 1, &abort_flag, p.err, kKernK1, 2);
+        ok = __all_sync(FULL, ok);
+        if (!ok) break;
+        int b = 0;
+        while (b + 1 < p.nseq && t >= p.cu[b + 1]) ++b;
+        const int pos = p.start[b] + static_cast<int>(t - p.cu[b]);
+        const bool in_cap = pos < p.cap;  // always, after host validation
+        if (!in_cap && lane == 0) set_error(p.err, kErrBounds, kKernK1, 1);
+        const float4 *tab = reinterpret_cast<const float4 *>(
+            p.rope + static_cast<int64_t>(in_cap ? pos : 0) * (D / 2) + 8 * (sub % HALF));
+        float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + e);
+        uint8_t *st = ring + s * stage_bytes;
+        const int64_t slot = static_cast<int64_t>(p.seq_slot0 + b) * p.seq_stride +
+                             static_cast<int64_t>(pos) * D;
+        // q and k rows, in place: q' stays in the stage for the bulk store, k'
+        // also goes to its cache slot.
+        const int nqk = p.Hq + p.Hkv;
+        for (int r0 = 0; r0 < nqk; r0 += RPW) {  // warp-uniform
+            const int r = r0 + grp;
+            const bool act = r < nqk;
+            uint4 *row = reinterpret_cast<uint4 *>(st + static_cast<size_t>(act ? r : 0) * D * 2) + sub;
+            const uint4 xv = *row;
+            const uint4 o = k1_norm_rope16(xv, r < p.Hq ? wqv : wkv, cs, p.eps, sub, LPR);
+            if (act) {
+                *row = o;
+                if (r >= p.Hq && in_cap)
+                    reinterpret_cast<uint4 *>(p.kc + slot + (r - p.Hq) * p.head_stride)[sub] = o;
+            }
+        }
+        // v rows: copied bit-exactly from the stage to their cache slots.
+        const uint8_t *vs = st + qbytes + kvbytes;
+        for (int r0 = 0; r0 < p.Hkv; r0 += RPW) {
+            const int r = r0 + grp;
+            if (r < p.Hkv && in_cap)
+                reinterpret_cast<uint4 *>(p.vc + slot + r * p.head_stride)[sub] =
+                    reinterpret_cast<const uint4 *>(vs + static_cast<size_t>(r) * D * 2)[sub];
+        }
+        // The warp's shared-memory accesses come before the bulk store reads the
+        // stage and before the next bulk copy overwrites it.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            bulk_s2g(p.qp + t * p.Hq * D, smem_u32(st), qbytes);
+            bulk_commit();
+        }
+    }
+    if (lane == 0) {
+        // A copy requested for a token that was not reached (the loop gave up):
+        // wait for it (bounded) before the shared memory goes away.
+        if (!ok && t + stride < p.T) {
+            int dummy = 0;
+            mbar_wait(bar0 + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1, &dummy, p.err, kKernK1, 3);
+        }
+        bulk_wait_all();  // every query store has completed
+    }
+}
+
+// Shared memory of the token-tiled form for a geometry (0: a token does not fit).
+static size_t k1t_smem_bytes(int Hq, int Hkv, int D) {
+    const size_t stage = (static_cast<size_t>(Hq + 2 * Hkv) * D * 2 + 127) & ~static_cast<size_t>(127);
+    const size_t bytes = static_cast<size_t>(kK1TWarps) * 2 * stage + 128;
+    return bytes <= 200 * 1024 ? bytes : 0;
+}
+
+template <int D>
+static cudaError_t launch_k1t(const K1Params &p, size_t smem, cudaStream_t stream) {
+    static std::atomic<unsigned> configured{0u};  // devices 0..31 set up (one bit each)
+    static std::atomic<int> sms_cache[32] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 32 || !((configured.load(std::memory_order_acquire) >> dev) & 1u)) {
+        cudaError_t e = cudaFuncSetAttribute(k1t_norm_rope_append_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 128);
+        if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 32) {
+            sms_cache[dev].store(sms, std::memory_order_relaxed);
+            configured.fetch_or(1u << dev, std::memory_order_release);
+        }
+    }
+    int sms = dev < 32 ? sms_cache[dev].load(std::memory_order_relaxed) : 0;
+    if (sms <= 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const int64_t need = (static_cast<int64_t>(p.T) + kK1TWarps - 1) / kK1TWarps;
+    const int blocks = static_cast<int>(std::min<int64_t>(need, sms));
+    k1t_norm_rope_append_kernel<D><<<blocks, kK1TWarps * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_k1(const K1Params &p, int D, cudaStream_t stream) {
+    if (p.T <= 0) return cudaSuccess;
+    const size_t smem = k1t_smem_bytes(p.Hq, p.Hkv, D);
+    if (smem > 0) return D == 128 ? launch_k1t<128>(p, smem, stream) : launch_k1t<64>(p, smem, stream);
+    return launch_k1_rows(p, D, stream);
+}
+
+// Per-block form, for geometries whose token does not fit a stage.
+cudaError_t launch_k1_rows(const K1Params &p, int D, cudaStream_t stream) {
     const int RG = (p.Hq + 2 * p.Hkv + kRowsPerGroup - 1) / kRowsPerGroup;
     const int64_t groups = static_cast<int64_t>(p.T) * RG;  // < 2^31: T is limited by the caller
     const int groups_per_block = (256 / 32) * (32 / (D / 8));

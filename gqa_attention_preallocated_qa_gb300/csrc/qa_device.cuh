@@ -140,6 +140,26 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// Contiguous shared -> global copy (16-byte aligned, size a multiple of 16),
+// tracked by this thread's bulk async-groups.
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every bulk store this thread committed has finished reading its
+// shared-memory source (the source may then be overwritten).
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every bulk store this thread committed has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // 3-D tiled tensor copy global -> shared (coordinates innermost first).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int c0, int c1, int c2,
                                             uint32_t bar) {
