@@ -160,40 +160,45 @@ __global__ void __launch_bounds__(256, 4) k1_norm_rope_append_kernel(const __gri
 // refilled only after the bulk store of its previous token has read it.
 // Bytes in flight: a token (12 KB at the Qwen3-4B geometry) per warp, eight
 // warps per SM.
-__device__ __forceinline__ uint4 k1_norm_rope16(uint4 xv, uint4 wv, const float4 (&cs)[4], float eps,
-                                               int sub, int lpr) {
+// RMSNorm + RoPE of this lane's 8 dims of a head row (lpr lanes per row, the
+// rotate-half partner lpr/2 lanes away): x_hat = bf16(x * r), y = bf16(w *
+// x_hat) (a bf16x2 multiply: the product of two bf16 values is exact in fp32,
+// so it rounds exactly as the per-block form's fp32 multiply does), then the
+// rotation in fp32 pairs and one rounding.  sn holds the sines signed for this
+// lane's half (-sin below D/2, +sin above).
+__device__ __forceinline__ uint4 k1_norm_rope16(uint4 xv, uint4 wv, const float2 (&cs2)[4],
+                                               const float2 (&sn2)[4], float eps, int lpr) {
     const unsigned FULL = 0xffffffffu;
     const int half = lpr / 2;
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
     const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-    float x[8], wf[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        x[2 * e] = bf16lo(xw[e]);
-        x[2 * e + 1] = bf16hi(xw[e]);
-        wf[2 * e] = bf16lo(ww[e]);
-        wf[2 * e + 1] = bf16hi(ww[e]);
-    }
+    float2 x[4];
     float ss = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+    for (int e = 0; e < 4; ++e) {
+        x[e] = make_float2(bf16lo(xw[e]), bf16hi(xw[e]));
+        ss = fmaf(x[e].x, x[e].x, fmaf(x[e].y, x[e].y, ss));
+    }
     for (int o = half; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
     const float rr = rsqrtf(ss * (1.0f / static_cast<float>(lpr * 8)) + eps);
+    const float2 r2 = make_float2(rr, rr);
     uint32_t yw[4], pw[4], ow[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-        yw[e] = pack_bf16(wf[2 * e] * round_bf16(x[2 * e] * rr),
-                          wf[2 * e + 1] * round_bf16(x[2 * e + 1] * rr));
+    for (int e = 0; e < 4; ++e) {
+        const float2 xh = __fmul2_rn(x[e], r2);
+        const uint32_t xb = pack_bf16(xh.x, xh.y);
+        const __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&xb),
+                                         *reinterpret_cast<const __nv_bfloat162 *>(&ww[e]));
+        yw[e] = *reinterpret_cast<const uint32_t *>(&y);
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) pw[e] = __shfl_xor_sync(FULL, yw[e], half);
-    const bool lower = (sub % lpr) < half;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float y0 = bf16lo(yw[e]), y1 = bf16hi(yw[e]);
-        const float q0 = bf16lo(pw[e]), q1 = bf16hi(pw[e]);
-        const float r0 = lower ? y0 * cs[e].x - q0 * cs[e].y : y0 * cs[e].x + q0 * cs[e].y;
-        const float r1 = lower ? y1 * cs[e].z - q1 * cs[e].w : y1 * cs[e].z + q1 * cs[e].w;
-        ow[e] = pack_bf16(r0, r1);
+        const float2 y = make_float2(bf16lo(yw[e]), bf16hi(yw[e]));
+        const float2 q = make_float2(bf16lo(pw[e]), bf16hi(pw[e]));
+        const float2 rot = __ffma2_rn(q, sn2[e], __fmul2_rn(y, cs2[e]));
+        ow[e] = pack_bf16(rot.x, rot.y);
     }
     return make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
@@ -263,25 +268,43 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
         if (!in_cap && lane == 0) set_error(p.err, kErrBounds, kKernK1, 1);
         const float4 *tab = reinterpret_cast<const float4 *>(
             p.rope + static_cast<int64_t>(in_cap ? pos : 0) * (D / 2) + 8 * (sub % HALF));
-        float4 cs[4];  // (cos_a, sin_a, cos_b, sin_b) of this lane's 8 dims
+        // (cos, sin) of this lane's 8 dims as pairs, the sines signed for its half
+        float2 cs2[4], sn2[4];
+        const float sgn = (sub % LPR) < HALF ? -1.f : 1.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + e);
+        for (int e = 0; e < 4; ++e) {
+            const float4 c4 = __ldg(tab + e);
+            cs2[e] = make_float2(c4.x, c4.z);
+            sn2[e] = make_float2(sgn * c4.y, sgn * c4.w);
+        }
         uint8_t *st = ring + s * stage_bytes;
         const int64_t slot = static_cast<int64_t>(p.seq_slot0 + b) * p.seq_stride +
                              static_cast<int64_t>(pos) * D;
         // q and k rows, in place: q' stays in the stage for the bulk store, k'
-        // also goes to its cache slot.
+        // also goes to its cache slot.  Four independent rows per lane at a time.
+        constexpr int U = 4;
         const int nqk = p.Hq + p.Hkv;
-        for (int r0 = 0; r0 < nqk; r0 += RPW) {  // warp-uniform
-            const int r = r0 + grp;
-            const bool act = r < nqk;
-            uint4 *row = reinterpret_cast<uint4 *>(st + static_cast<size_t>(act ? r : 0) * D * 2) + sub;
-            const uint4 xv = *row;
-            const uint4 o = k1_norm_rope16(xv, r < p.Hq ? wqv : wkv, cs, p.eps, sub, LPR);
-            if (act) {
-                *row = o;
-                if (r >= p.Hq && in_cap)
-                    reinterpret_cast<uint4 *>(p.kc + slot + (r - p.Hq) * p.head_stride)[sub] = o;
+        for (int r0 = 0; r0 < nqk; r0 += RPW * U) {  // warp-uniform
+            uint4 xv[U];
+            int rr[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                rr[u] = r0 + u * RPW + grp;
+                const int rs = rr[u] < nqk ? rr[u] : 0;
+                xv[u] = reinterpret_cast<const uint4 *>(st + static_cast<size_t>(rs) * D * 2)[sub];
+            }
+            uint4 o[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                o[u] = k1_norm_rope16(xv[u], rr[u] < p.Hq ? wqv : wkv, cs2, sn2, p.eps, LPR);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int r = rr[u];
+                if (r < nqk) {
+                    reinterpret_cast<uint4 *>(st + static_cast<size_t>(r) * D * 2)[sub] = o[u];
+                    if (r >= p.Hq && in_cap)
+                        reinterpret_cast<uint4 *>(p.kc + slot + (r - p.Hq) * p.head_stride)[sub] = o[u];
+                }
             }
         }
         // v rows: copied bit-exactly from the stage to their cache slots.
