@@ -46,7 +46,7 @@ class L2Flush:
 
     def zero_(self):
         import torch
-        torch.sum(self.buf, dtype=torch.int64, out=self.sink)
+        torch.sum(self.buf, dim=0, dtype=torch.int64, out=self.sink)
         return self
 
 
