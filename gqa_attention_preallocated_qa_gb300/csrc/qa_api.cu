@@ -361,8 +361,14 @@ qa_status run_multi(qa_cache *c, int layer, int batch, const int32_t *lens, int 
         const qa::FaultPlan f = qa::take_fault(QA_KERNEL_DECODE_ATTN);
         l.first.fault = f.fault;
         l.first.wait_ns = f.wait_ns;
-        if (qa::launch_k3_multi(l.first, l.second, g.head_dim, HPC, s) != cudaSuccess)
+        if (qa::launch_k3_multi(l.first, l.second, g.head_dim, HPC, s) != cudaSuccess) {
+            // The launches before this one were enqueued and advance their
+            // sequences' device lengths: the host copy follows them.
+            int32_t *host = c->lens_host.data() + static_cast<size_t>(layer) * g.max_batch;
+            for (auto *e = launches.data(); e != &l; ++e)
+                for (int z = 0; z < e->first.B; ++z) host[e->second.seq[z]] += e->second.ntok[z];
             return QA_ERR_CUDA;
+        }
         c->launches[QA_KERNEL_DECODE_ATTN]++;
     }
     return QA_OK;
@@ -703,8 +709,13 @@ qa_status decode_step(qa_cache *c, int layer, int batch, const void *q, const vo
         const qa::FaultPlan f = qa::take_fault(QA_KERNEL_DECODE_ATTN);
         p.fault = f.fault;
         p.wait_ns = f.wait_ns;
-        if (qa::launch_k3(p, g.head_dim, c->HPC, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        if (qa::launch_k3(p, g.head_dim, c->HPC, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+            // The launches before this one were enqueued and advance their
+            // sequences' device lengths: the host copy follows them.
+            if (!dev_pos)
+                for (int b = 0; b < b0; ++b) mirror[b] += 1;
             return QA_ERR_CUDA;
+        }
         c->launches[QA_KERNEL_DECODE_ATTN]++;
     }
     if (!dev_pos)

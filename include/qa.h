@@ -150,7 +150,9 @@ qa_status qa_prefill(qa_cache *cache, int layer, int batch, const int32_t *promp
  * successors start before they themselves have waited for their predecessor
  * (the usual use of programmatic dependent launch).
  * Errors: INVALID_ARG, ALIGNMENT, CAPACITY (a sequence already holds
- * `capacity` tokens; nothing is evicted or wrapped). */
+ * `capacity` tokens; nothing is evicted or wrapped), CUDA (a launch failed;
+ * with more than 64 sequences the launches before it were enqueued and their
+ * sequences have advanced, on the device and in the host copy). */
 qa_status qa_decode_step(qa_cache *cache, int layer, int batch,
                          const void *q, const void *k, const void *v,
                          const void *q_norm_w, const void *k_norm_w, void *out, void *stream);
