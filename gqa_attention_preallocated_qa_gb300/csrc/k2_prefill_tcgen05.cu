@@ -7,24 +7,17 @@
 // the order of the arithmetic differs from the definition ("reorderings are
 // affordable", same guide, "Numerics").
 //
-// One CTA = one 128-row block of a sequence's new tokens (a whole prompt, or a
-// chunk appended after the tokens the layer already holds) for NT query heads
-// of one kv head (kK2HeadsPerCta: 1 by default, so that two CTAs share an SM
-// and one's prologue and epilogue overlap the other's main loop; with 2, both
-// heads share every K/V tile).  Warp roles (NT * 128 + 64 threads):
-//   warps 0-3        softmax warpgroup 0 (query head h0): thread r owns row r
-//   warps 4-7        softmax warpgroup 1 (query head h1; NT = 2 only)
-//   warp  4*NT       TMA producer: Q once, then K_j, V_j tiles into a ring
-//   warp  4*NT + 1   tcgen05 issuer (one thread) and TMEM owner
-// Tensor memory (NT * 256 columns x 128 lanes, fp32):
-//   NT = 1: [0,128) S0/P0   [128,128+D) O0
-//   NT = 2: [0,128) S0/P0   [128,256) S1/P1   [256,256+D) O0   [256+D,256+2D) O1
-// S_t = Q_t K_j^T (both operands K-major, 128-byte swizzled smem); the softmax
-// threads read their row of S_t with tcgen05.ld, compute p = 2^(s*c - m*c) in
-// fp32, write P as bf16 over the first 64 columns of S_t, rescale O_t when the
-// running max grew, and signal; O_t += P_t V_j reads P from TMEM and V
-// (MN-major) from smem.  S_t(j+1) is issued right behind PV_t(j) by the same
-// thread, so it overwrites P_t only after PV_t(j) has read it.
+// The kernel is persistent: one CTA per SM walks a fixed share of the work
+// items (described below).  An item is one 128-row block of a sequence's new
+// tokens (a whole prompt, or a chunk appended after the tokens the layer
+// already holds) for one or two query heads of a kv head; with two, both heads
+// share every K/V tile.  S_t = Q_t K_j^T (both operands K-major, 128-byte
+// swizzled smem); the softmax threads read their row of S_t with tcgen05.ld,
+// compute p = 2^(s*c - m*c) in fp32, write P as bf16 over the first 64 columns
+// of S_t, rescale O_t when the running max grew, and signal; O_t += P_t V_j
+// reads P from TMEM and V (MN-major) from smem.  S_t(j+1) is issued right
+// behind PV_t(j) by the same thread, so it overwrites P_t only after PV_t(j)
+// has read it.
 //
 // K and V come straight out of the cache through one 3-D tensor map per
 // sequence, (D, P_b + L_b, Hkv), so rows at or past the sequence's length read
@@ -40,22 +33,6 @@
 #include "qa_device.cuh"
 
 namespace qa {
-
-// NT = query heads (128-row tiles) per CTA.
-template <int D, int NT>
-struct K2Layout {
-    static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 64 bf16
-    static constexpr int kBoxes = D / 64;
-    static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D
-    // two CTAs per SM with one tile each: Q + 2 K/V stages fit twice
-    static constexpr int kStages = NT == 2 ? ((D == 128) ? 4 : 6) : ((D == 128) ? 2 : 4);
-    static constexpr int kQBytes = NT * kTileBytes;
-    static constexpr int kSmemBytes = kQBytes + kStages * kTileBytes + 1024;  // + alignment slack
-    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = NT * 128, kColO1 = NT * 128 + D;
-    static constexpr uint32_t kTmemCols = NT == 2 ? 512 : 256;
-    static constexpr int kThreads = NT * 128 + 64;  // softmax warpgroups, TMA warp, MMA warp
-    static constexpr int kTmaWarp = 4 * NT, kMmaWarp = 4 * NT + 1;
-};
 
 // max(a, b, c) in one instruction (NaN inputs are ignored, as by fmaxf).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -105,354 +82,13 @@ __device__ __forceinline__ bool k2_decode_item(const K2Params &p, int idx, int &
     return false;
 }
 
-template <int D, bool kWindow, int NT>
-__global__ void __launch_bounds__(K2Layout<D, NT>::kThreads, NT == 1 ? 2 : 1)
-    k2_prefill_kernel(const __grid_constant__ K2Params p) {
-    using Lay = K2Layout<D, NT>;
-    constexpr int NS = Lay::kStages;
-    const unsigned FULL = 0xffffffffu;
-
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_q, bar_kv_full[NS], bar_kv_empty[NS];
-    __shared__ __align__(8) uint64_t bar_s[2], bar_p[2], bar_pv[2];
-    __shared__ uint32_t s_tmem;
-    __shared__ int s_abort;
-
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t sQ = smem_u32(smem);
-    const uint32_t sKV = sQ + Lay::kQBytes;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int b = 0, kvh = 0, pair = 0, qb = 0;
-    if (!k2_decode_item(p, blockIdx.x, b, kvh, pair, qb)) return;  // uniform per CTA
-    const bool two = NT == 2 && 2 * pair + 1 < p.G;
-    const int h0 = kvh * p.G + NT * pair;
-    const int L = p.len[b];
-    // Query row r of the block is new token qb*128 + r at position qmin + r; it
-    // sees keys 0..qmin + r, or with an attention window of W keys
-    // qmin + r + 1 - W..qmin + r.  Key tiles j0..j0+nkv-1 reach from row 0's
-    // first visible key to the block's last one; tiles from jmask on may hold
-    // keys past a row's position.
-    const int qmin = p.start[b] + qb * 128;
-    const int j0 = kWindow ? max(0, qmin + 1 - p.window) / 128 : 0;
-    const int nkv = (qmin + min(127, L - 1 - qb * 128)) / 128 + 1 - j0;
-    const int jmask = qmin / 128;
-
-    if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bar_q), 1);
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(smem_u32(&bar_kv_full[s]), 1);
-            mbar_init(smem_u32(&bar_kv_empty[s]), 1);
-        }
-        for (int t = 0; t < NT; ++t) {
-            mbar_init(smem_u32(&bar_s[t]), 1);
-            mbar_init(smem_u32(&bar_p[t]), 128);
-            mbar_init(smem_u32(&bar_pv[t]), 1);
-        }
-        s_abort = 0;
-        fence_mbar_init();
-    }
-    if (warp == Lay::kMmaWarp) {
-        tmem_alloc(smem_u32(&s_tmem), Lay::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = s_tmem;
-
-    if (warp == Lay::kTmaWarp) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            prefetch_tmap(&p.tm_q);
-            prefetch_tmap(&p.tm_k[b]);
-            prefetch_tmap(&p.tm_v[b]);
-            const uint32_t bq = smem_u32(&bar_q);
-            mbar_expect_tx(bq, (two ? 2 : 1) * Lay::kTileBytes);
-            const int row0 = p.cu[b] + qb * 128;
-            for (int t = 0; t < (two ? 2 : 1); ++t)
-                for (int x = 0; x < Lay::kBoxes; ++x)
-                    tma_load_3d(sQ + t * Lay::kTileBytes + x * Lay::kBoxBytes, &p.tm_q, x * 64,
-                                h0 + t, row0, bq);
-            // Test hook: CTA 0 withholds the copy of V tile 0 (nothing will complete
-            // that stage's phase), so the MMA warp's wait for it runs out.
-            const int withheld = (p.fault && blockIdx.x == 0) ? 1 : -1;
-            int issued = 0;
-            for (int idx = 0; idx < 2 * nkv; ++idx, ++issued) {
-                const int st = idx % NS;
-                if (idx >= NS &&
-                    !mbar_wait(smem_u32(&bar_kv_empty[st]), ((idx / NS) - 1) & 1, &s_abort, p.err,
-                               kKernK2, 1, p.wait_ns))
-                    break;
-                if (idx == withheld) continue;
-                const uint32_t fb = smem_u32(&bar_kv_full[st]);
-                mbar_expect_tx(fb, Lay::kTileBytes);
-                const CUtensorMap *tm = (idx & 1) ? &p.tm_v[b] : &p.tm_k[b];
-                for (int x = 0; x < Lay::kBoxes; ++x)
-                    tma_load_3d(sKV + st * Lay::kTileBytes + x * Lay::kBoxBytes, tm, x * 64,
-                                (j0 + (idx >> 1)) * 128, kvh, fb);
-            }
-            // Never leave a copy in flight: bounded wait for the last ones and Q.
-            int dummy = 0;
-            for (int i = max(0, issued - NS); i < issued; ++i)
-                if (i != withheld)
-                    mbar_wait(smem_u32(&bar_kv_full[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2,
-                              2, p.wait_ns);
-            mbar_wait(bq, 0, &dummy, p.err, kKernK2, 3, p.wait_ns);
-        }
-    } else if (warp == Lay::kMmaWarp) {
-        // ------------------------------------------------------------ tcgen05 issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
-            const uint32_t tS[2] = {tmem + Lay::kColS0, tmem + Lay::kColS1};
-            const uint32_t tO[2] = {tmem + Lay::kColO0, tmem + Lay::kColO1};
-            const int ntiles = two ? 2 : 1;
-            bool ok = mbar_wait(smem_u32(&bar_q), 0, &s_abort, p.err, kKernK2, 4, p.wait_ns);
-            tc_fence_after();
-
-            // S_t = Q_t K^T: K-major A and B, 128-byte swizzle, 8-row groups 1024 B apart;
-            // K-step k of 16 elements = 32 bytes inside the 128-byte row of box k/4.
-            // Descriptors are built once per operand tile; a K-step only moves the
-            // start address (bits 0-13, in 16-byte units, never carrying out at
-            // shared-memory addresses), so it is one 32-bit add on the low word.
-            auto desc_at = [](uint64_t base, uint32_t byte_off) -> uint64_t {
-                return (base & 0xFFFFFFFF00000000ull) |
-                       static_cast<uint32_t>(static_cast<uint32_t>(base) + (byte_off >> 4));
-            };
-            const uint64_t dQ[2] = {sdesc_sw128(sQ, 16, 1024),
-                                    sdesc_sw128(sQ + (NT - 1) * Lay::kTileBytes, 16, 1024)};
-            auto issue_s = [&](int t, int st) {
-                const uint64_t dK = sdesc_sw128(sKV + st * Lay::kTileBytes, 16, 1024);
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * Lay::kBoxBytes + (k % 4) * 32;
-                    mma_ss(tS[t], desc_at(dQ[t], off), desc_at(dK, off), idesc_qk, k > 0 ? 1u : 0u);
-                }
-            };
-            // O_t += P_t V: P (bf16, 2 per column) from TMEM, V MN-major in smem:
-            // 64-wide d blocks one box (16 KB) apart, 8-row key groups 1024 B apart;
-            // K-step k of 16 keys = 16 rows = 2048 bytes.
-            auto issue_pv = [&](int t, int st, bool acc) {
-                const uint64_t dV = sdesc_sw128(sKV + st * Lay::kTileBytes, Lay::kBoxBytes, 1024);
-#pragma unroll
-                for (int k = 0; k < 128 / 16; ++k)
-                    mma_ts(tO[t], tS[t] + k * 8, desc_at(dV, k * 2048), idesc_pv,
-                           (acc || k > 0) ? 1u : 0u);
-            };
-
-            if (ok) ok = mbar_wait(smem_u32(&bar_kv_full[0]), 0, &s_abort, p.err, kKernK2, 5, p.wait_ns);
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < ntiles; ++t) {
-                    issue_s(t, 0);
-                    mma_commit(smem_u32(&bar_s[t]));
-                }
-                mma_commit(smem_u32(&bar_kv_empty[0]));
-            }
-            int committed = ok ? 1 : 0;  // ring slots handed back (for the final drain)
-            // Per KV tile j and query tile t, as soon as softmax t has written P_t(j):
-            // O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T right behind it.  S_t(j+1)
-            // overwrites the TMEM columns P_t(j) sits in; tcgen05.mma operations issued
-            // by one thread execute in issue order, so P.V_t(j) has read P_t(j) before
-            // S_t(j+1) writes there, and no wait is needed between the two.  Tile t+1
-            // never waits for tile t's next S, so the two softmax warpgroups and the
-            // tensor pipe overlap.
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int iv = 2 * j + 1, sv = iv % NS;
-                const int ik = 2 * (j + 1), sk = ik % NS;
-                const bool more = j + 1 < nkv;
-                ok = mbar_wait(smem_u32(&bar_kv_full[sv]), (iv / NS) & 1, &s_abort, p.err, kKernK2, 6, p.wait_ns);
-                if (ok && more)
-                    ok = mbar_wait(smem_u32(&bar_kv_full[sk]), (ik / NS) & 1, &s_abort, p.err,
-                                   kKernK2, 8, p.wait_ns);
-                for (int t = 0; ok && t < ntiles; ++t) {
-                    ok = mbar_wait(smem_u32(&bar_p[t]), j & 1, &s_abort, p.err, kKernK2, 7, p.wait_ns);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(t, sv, j > 0);
-                    if (!more) mma_commit(smem_u32(&bar_pv[t]));  // O_t final
-                    if (t == ntiles - 1) {
-                        mma_commit(smem_u32(&bar_kv_empty[sv]));
-                        ++committed;
-                    }
-                    if (more) {
-                        issue_s(t, sk);
-                        mma_commit(smem_u32(&bar_s[t]));
-                        if (t == ntiles - 1) {
-                            mma_commit(smem_u32(&bar_kv_empty[sk]));
-                            ++committed;
-                        }
-                    }
-                }
-            }
-            // Drain: every commit above must have arrived before the CTA exits.
-            int dummy = 0;
-            for (int i = max(0, committed - NS); i < committed; ++i)
-                mbar_wait(smem_u32(&bar_kv_empty[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2, 10, p.wait_ns);
-        }
-    } else {
-        // ------------------------------------------------------------ softmax warpgroups
-        const int t = warp >> 2;  // 0 or 1
-        if (t == 0 || two) {
-            const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
-            const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            const uint32_t tS = tmem + (t ? Lay::kColS1 : Lay::kColS0) + lane_off;
-            const uint32_t tO = tmem + (t ? Lay::kColO1 : Lay::kColO0) + lane_off;
-            const float c = p.scale_log2;
-            const int qpos = qmin + r;  // this row's position
-            // mref: the reference max of this row in the exp2 domain's units (raw
-            // scores).  It only moves when the row max exceeds it by more than
-            // kRescaleLog2 / c, so O is rescaled rarely; p = 2^(s*c - mref*c) then
-            // stays below 2^kRescaleLog2, and out = O / l is exact for any mref.
-            float mref = -INFINITY, l = 0.f;
-            bool ok = true;
-            for (int j = 0; j < nkv; ++j) {
-                ok = mbar_wait(smem_u32(&bar_s[t]), j & 1, &s_abort, p.err, kKernK2, 11, p.wait_ns);
-                ok = __all_sync(FULL, ok);
-                if (!ok) break;
-                tc_fence_after();
-                const int jt = j0 + j;            // key tile
-                const int thr = qpos - jt * 128;  // last visible key index in the tile
-                const int tlo = kWindow ? qpos + 1 - p.window - jt * 128 : 0;  // first visible
-                // The row of S: 4 TMEM loads in flight, one wait.
-                uint32_t sr[128];
-                {
-                    uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr);
-                    uint32_t(&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 32);
-                    uint32_t(&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 64);
-                    uint32_t(&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 96);
-                    tmem_ld32_async(tS, s0);
-                    tmem_ld32_async(tS + 32, s1);
-                    tmem_ld32_async(tS + 64, s2);
-                    tmem_ld32_async(tS + 96, s3);
-                    tmem_wait_ld4(s0, s1, s2, s3);
-                }
-                if (jt >= jmask || tlo > 0) {  // keys outside the row's range are masked
-#pragma unroll
-                    for (int i = 0; i < 128; ++i)
-                        if (i > thr || i < tlo) sr[i] = __float_as_uint(-INFINITY);
-                }
-                // Row max: 8 independent chains of three-input maxima.
-                float mx8[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mx8[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
-#pragma unroll
-                for (int i = 16; i < 128; i += 16) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        mx8[k] = fmax3(mx8[k], __uint_as_float(sr[i + k]), __uint_as_float(sr[i + 8 + k]));
-                }
-                const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
-                                       fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-                // The first P.V overwrites O, so tile 0 just sets mref; later tiles move
-                // it (and rescale O by alpha, after P is written) only when it grew.
-                bool rescale = false;
-                float alpha = 1.f;
-                if (j == 0) {
-                    // (a window can mask a whole first tile of a row: keep mref finite)
-                    mref = mx == -INFINITY ? 0.f : mx;
-                } else {
-                    const bool grow = (mx - mref) * c > kRescaleLog2;
-                    rescale = __any_sync(FULL, grow);
-                    if (grow) {
-                        alpha = k2_ex2((mref - mx) * c);
-                        mref = mx;
-                        l *= alpha;
-                    }
-                }
-                // p = 2^(s*c - mref*c): packed fp32x2 scale-and-subtract, then the exp
-                // unit; P is stored 32 columns at a time over the first 64 columns of S_t
-                // (all of S is already in registers).
-                const float2 c2 = make_float2(c, c);
-                const float2 n2 = make_float2(-mref * c, -mref * c);
-                float2 sum4[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) sum4[k] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int col = ch * 32 + 2 * i;
-                        const float2 x = __ffma2_rn(
-                            make_float2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2, n2);
-                        const float2 pv = make_float2(k2_ex2(x.x), k2_ex2(x.y));
-                        pk[i] = pack_bf16(pv.x, pv.y);
-                        sum4[i & 3] = __fadd2_rn(sum4[i & 3], pv);
-                    }
-                    tmem_st16(tS + ch * 16, pk);
-                }
-                const float2 sp = __fadd2_rn(__fadd2_rn(sum4[0], sum4[1]), __fadd2_rn(sum4[2], sum4[3]));
-                l += sp.x + sp.y;
-                if (rescale) {
-                    // P.V_t(j-1) is complete: the commit that signalled S_t(j) tracks
-                    // every tcgen05 operation issued before it.
-                    const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-                    for (int ch = 0; ch < D / 32; ++ch) {
-                        uint32_t u[32];
-                        tmem_ld32(tO + ch * 32, u);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float2 v = __fmul2_rn(
-                                make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), a2);
-                            u[2 * i] = __float_as_uint(v.x);
-                            u[2 * i + 1] = __float_as_uint(v.y);
-                        }
-                        tmem_st32(tO + ch * 32, u);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(smem_u32(&bar_p[t]));
-            }
-            if (ok) {
-                ok = mbar_wait(smem_u32(&bar_pv[t]), 0, &s_abort, p.err, kKernK2, 12, p.wait_ns);
-                ok = __all_sync(FULL, ok);
-            }
-            if (ok) {
-                tc_fence_after();
-                const float inv = 1.f / l;
-                const int row = qb * 128 + r;  // new token index within the sequence
-                const bool valid = row < L;
-                __nv_bfloat16 *dst =
-                    p.out + (static_cast<int64_t>(p.cu[b] + row) * p.Hq + h0 + t) * D;
-#pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t u[32];
-                    tmem_ld32(tO + ch * 32, u);
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        w[i] = pack_bf16(__uint_as_float(u[2 * i]) * inv,
-                                         __uint_as_float(u[2 * i + 1]) * inv);
-                    if (valid) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                    }
-                }
-            }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == Lay::kMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem, Lay::kTmemCols);
-    }
-}
-
-// ==================================================================== persistent form
+// ==================================================================== the kernel
 // One CTA per SM walks a fixed share of the work items.  An item is one
-// 128-row query block of one sequence for the two query heads 2*pair and
-// 2*pair + 1 of a kv head (one head when the group size is 1): both heads'
-// tiles share every K/V tile of the ring.  Items are listed heaviest first
+// 128-row query block of one sequence for the query heads hpi*pair ..
+// hpi*pair + hpi - 1 of a kv head, hpi (heads per item) being 2 unless the
+// group size is 1 or two-head items would not give every SM one (a short
+// prompt or chunk), then 1: the item's head tiles share every K/V tile of the
+// ring.  Items are listed heaviest first
 // (most key tiles) and dealt out in snake order (round k gives CTA c item
 // k*G + c for even k and k*G + G-1-c for odd k, G = CTAs), which balances the
 // key tiles per CTA.  Across items the pipeline never drains:
@@ -503,7 +139,7 @@ __device__ __forceinline__ bool k2p_item(const K2Params &p, int k, K2Item &it) {
     if (idx >= p.nitems) return false;
     int pair = 0;
     if (!k2_decode_item(p, idx, it.b, it.kvh, pair, it.qb)) return false;
-    it.h0 = it.kvh * p.G + 2 * pair;
+    it.h0 = it.kvh * p.G + p.hpi * pair;
     it.L = p.len[it.b];
     it.qmin = p.start[it.b] + it.qb * 128;
     it.j0 = kWindow ? max(0, it.qmin + 1 - p.window) / 128 : 0;
@@ -531,7 +167,7 @@ __global__ void __launch_bounds__(K2PLayout<D>::kThreads, 1)
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sKV = sQ + Lay::kQBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntiles = p.G > 1 ? 2 : 1;  // query heads per item (the same for every item)
+    const int ntiles = p.hpi;  // query heads per item (the same for every item)
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bar_q), 1);
@@ -896,40 +532,31 @@ static int k2_num_sms() {
 
 template <int D, bool kWindow>
 static cudaError_t launch_k2_t(const K2Params &p, int nitems, cudaStream_t stream) {
-#if QA_K2_FORM == 1
-    {
-        using Lay = K2PLayout<D>;
-        constexpr int smem = Lay::kSmemBytes;
-        static std::atomic<unsigned> configured{0u};  // devices 0..31 set up (one bit each)
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 32 || !((configured.load(std::memory_order_acquire) >> dev) & 1u)) {
-            cudaError_t e = cudaFuncSetAttribute(k2p_prefill_kernel<D, kWindow>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess) return e;
-            if (dev < 32) configured.fetch_or(1u << dev, std::memory_order_release);
-        }
-        const int sms = k2_num_sms();
-        if (sms <= 0) return cudaErrorInvalidDevice;
-        K2Params q = p;
-        q.nitems = nitems;
-        k2p_prefill_kernel<D, kWindow><<<std::min(nitems, sms), Lay::kThreads, smem, stream>>>(q);
-        return cudaGetLastError();
-    }
-#endif
-    constexpr int NT = kK2HeadsPerCta;
-    using Lay = K2Layout<D, NT>;
+    using Lay = K2PLayout<D>;
     constexpr int smem = Lay::kSmemBytes;
     static std::atomic<unsigned> configured{0u};  // devices 0..31 set up (one bit each)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 32 || !((configured.load(std::memory_order_acquire) >> dev) & 1u)) {
-        cudaError_t e = cudaFuncSetAttribute(k2_prefill_kernel<D, kWindow, NT>,
+        cudaError_t e = cudaFuncSetAttribute(k2p_prefill_kernel<D, kWindow>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (dev < 32) configured.fetch_or(1u << dev, std::memory_order_release);
     }
-    k2_prefill_kernel<D, kWindow, NT><<<nitems, Lay::kThreads, smem, stream>>>(p);
+    const int sms = k2_num_sms();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    K2Params q = p;
+    q.hpi = p.G > 1 ? 2 : 1;
+    q.npairs = (p.G + q.hpi - 1) / q.hpi;
+    q.nitems = nitems / p.npairs * q.npairs;
+    if (q.hpi == 2 && q.nitems < sms) {
+        // Fewer two-head items than SMs (a short prompt or chunk): one query
+        // head per item, twice the work units.
+        q.hpi = 1;
+        q.npairs = p.G;
+        q.nitems = nitems / p.npairs * q.npairs;
+    }
+    k2p_prefill_kernel<D, kWindow><<<std::min(q.nitems, sms), Lay::kThreads, smem, stream>>>(q);
     return cudaGetLastError();
 }
 

@@ -425,7 +425,7 @@ qa_status plan_k2(qa_cache *c, int layer, int batch, const int32_t *lens, const 
             p.Hq = g.n_q_heads;
             p.Hkv = g.n_kv_heads;
             p.G = c->G;
-            p.npairs = (c->G + qa::kK2HeadsPerCta - 1) / qa::kK2HeadsPerCta;
+            p.npairs = (c->G + 1) / 2;  // two-head items; the launch may halve them
             p.max_qblocks = maxqb;
             p.window = c->window[layer];
             p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));

@@ -52,23 +52,6 @@ struct K1Params {
 };
 
 // ---------------------------------------------------------------- K2
-// Query heads (128-row tiles) per prefill CTA: 1 (two CTAs per SM, each with
-// one softmax warpgroup, a TMA warp and an MMA warp; the default: one CTA's
-// per-block prologue and epilogue overlap the other's main loop) or 2 (one CTA
-// per SM; the two heads share every K/V tile).
-// QA_K2_FORM selects the prefill kernel: 1 (default) the persistent form (one
-// CTA per SM walking a fixed share of the work items, two query heads of one kv
-// head per item sharing every K/V tile, the next item's loads and first S
-// overlapping the current item's end); 0 the per-block form (one CTA per work
-// item, QA_K2_HEADS_PER_CTA query heads each).
-#ifndef QA_K2_FORM
-#define QA_K2_FORM 1
-#endif
-#ifndef QA_K2_HEADS_PER_CTA
-#define QA_K2_HEADS_PER_CTA 1
-#endif
-constexpr int kK2HeadsPerCta = QA_K2_FORM == 1 ? 2 : QA_K2_HEADS_PER_CTA;
-static_assert(kK2HeadsPerCta == 1 || kK2HeadsPerCta == 2, "one or two query heads per CTA");
 constexpr int kK2BlockM = 128;    // query rows per tile
 constexpr int kK2BlockN = 128;    // keys per tile
 
@@ -78,7 +61,8 @@ struct alignas(64) K2Params {
     CUtensorMap tm_v[kMaxSeqPerLaunch];
     __nv_bfloat16 *out;                       // [T][Hq][D]
     uint32_t *err;
-    int nseq, Hq, Hkv, G, npairs;             // npairs: CTAs (head tiles) per kv head and block
+    int nseq, Hq, Hkv, G, npairs;             // npairs: items per kv head and query block
+    int hpi;                                  // query heads per item (1 or 2; set at launch)
     int len[kMaxSeqPerLaunch];                // new tokens of each sequence
     int start[kMaxSeqPerLaunch];              // position of each sequence's first new token
     int cu[kMaxSeqPerLaunch];                 // first row of each sequence in q'/out
