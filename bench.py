@@ -672,6 +672,17 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
         us = e0.elapsed_time(e1) * 1e3 / steps
         byts /= steps
         gbs = byts / (us * 1e-6) / 1e9
+        # the same on one layer, for reference (its K/V may stay in L2)
+        n1 = same_steps
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(n1):
+            st |= lib.qa_decode_step(h, 0, pt.B, *args_c, sh)
+        e3.record(stream)
+        lens[0] += n1
+        torch.cuda.synchronize()
+        if st or qa.qa_get_device_error(h)[0]:
+            raise RuntimeError(f"decode sweep point {pt.name} failed")
         if iso:
             qa.qa_cache_set_decode_overlap(h, 1)
             iso_splits = qa.qa_decode_splits(h, 0, pt.B)
@@ -701,19 +712,8 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
                         "how": "median of per-launch events; a spacer kernel before each launch, "
                                "layers cycled (HBM-cold), split plan for one launch, the host "
                                "ahead of the device"}
-            qa.qa_cache_set_decode_overlap(h, args.sweep_overlap or 4)
-        # the same on one layer, for reference (its K/V may stay in L2)
-        n1 = same_steps
-        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2.record(stream)
-        for _ in range(n1):
-            st |= lib.qa_decode_step(h, 0, pt.B, *args_c, sh)
-        e3.record(stream)
-        torch.cuda.synchronize()
-        if st or qa.qa_get_device_error(h)[0]:
-            raise RuntimeError(f"decode sweep point {pt.name} failed")
         points.append({"sweep": pt.name, "B": pt.B, "L": pt.L, "steps": steps, "layers": NL,
-                       "splits": splits, "overlap": args.sweep_overlap or 4, "us_per_step": round(us, 3),
+                       "splits": splits, "overlap": args.sweep_overlap or "per launch", "us_per_step": round(us, 3),
                        "host_us_per_call": round(host_us, 3),
                        "kv_bytes_per_step": round(byts), "hbm_gbs": round(gbs, 1),
                        "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),

@@ -153,11 +153,10 @@ __global__ void __launch_bounds__(256, 4) k1_norm_rope_append_kernel(const __gri
 // the tokens (token t goes to warp t mod (CTAs x warps)).  Lane 0 copies a
 // token's q, k and v rows (three contiguous runs of the packed input) into the
 // next stage with bulk copies completing on the stage's mbarrier while the
-// warp transforms the current stage in place (RMSNorm + RoPE of the q and k
-// rows, the cast placement of the per-block form); the normed, rotated
-// queries go out in one bulk store, and the k' and v rows to their cache
-// slots with 16-byte stores (one row of 256 bytes per 16 lanes).  A stage is
-// refilled only after the bulk store of its previous token has read it.
+// warp transforms the current stage (RMSNorm + RoPE of the q and k rows, the
+// cast placement of the per-row form) and writes q', k' and v to their
+// places with 16-byte stores (one row of 256 bytes per 16 lanes); the stage is
+// only read, so the next copy into it follows the warp's last read of it.
 // Bytes in flight: a token (12 KB at the Qwen3-4B geometry) per warp, eight
 // warps per SM.
 // RMSNorm + RoPE of this lane's 8 dims of a head row (lpr lanes per row, the
@@ -254,10 +253,7 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
     for (; t < p.T; ++i, t += stride) {
         const int s = i & 1;
         const int64_t tn = t + stride;
-        if (lane == 0 && tn < p.T) {
-            bulk_wait_read_all();  // the query store of the stage's previous token has read it
-            load(tn, s ^ 1);
-        }
+        if (lane == 0 && tn < p.T) load(tn, s ^ 1);  // the warp is done with that stage
         ok = mbar_wait(bar0 + 8 * s, (i >> 1) & 1, &abort_flag, p.err, kKernK1, 2);
         ok = __all_sync(FULL, ok);
         if (!ok) break;
@@ -280,8 +276,8 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
         uint8_t *st = ring + s * stage_bytes;
         const int64_t slot = static_cast<int64_t>(p.seq_slot0 + b) * p.seq_stride +
                              static_cast<int64_t>(pos) * D;
-        // q and k rows, in place: q' stays in the stage for the bulk store, k'
-        // also goes to its cache slot.  Four independent rows per lane at a time.
+        // q and k rows: q' to the output rows, k' to its cache slot, 16 bytes per
+        // lane straight from registers.  Four independent rows per lane at a time.
         constexpr int U = 4;
         const int nqk = p.Hq + p.Hkv;
         for (int r0 = 0; r0 < nqk; r0 += RPW * U) {  // warp-uniform
@@ -300,11 +296,10 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int r = rr[u];
-                if (r < nqk) {
-                    reinterpret_cast<uint4 *>(st + static_cast<size_t>(r) * D * 2)[sub] = o[u];
-                    if (r >= p.Hq && in_cap)
-                        reinterpret_cast<uint4 *>(p.kc + slot + (r - p.Hq) * p.head_stride)[sub] = o[u];
-                }
+                if (r < p.Hq)
+                    reinterpret_cast<uint4 *>(p.qp + (t * p.Hq + r) * D)[sub] = o[u];
+                else if (r < nqk && in_cap)
+                    reinterpret_cast<uint4 *>(p.kc + slot + (r - p.Hq) * p.head_stride)[sub] = o[u];
             }
         }
         // v rows: copied bit-exactly from the stage to their cache slots.
@@ -315,14 +310,9 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
                 reinterpret_cast<uint4 *>(p.vc + slot + r * p.head_stride)[sub] =
                     reinterpret_cast<const uint4 *>(vs + static_cast<size_t>(r) * D * 2)[sub];
         }
-        // The warp's shared-memory accesses come before the bulk store reads the
-        // stage and before the next bulk copy overwrites it.
+        // The warp's reads of the stage come before the next bulk copy overwrites it.
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-            bulk_s2g(p.qp + t * p.Hq * D, smem_u32(st), qbytes);
-            bulk_commit();
-        }
     }
     if (lane == 0) {
         // A copy requested for a token that was not reached (the loop gave up):
@@ -331,7 +321,6 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
             int dummy = 0;
             mbar_wait(bar0 + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1, &dummy, p.err, kKernK1, 3);
         }
-        bulk_wait_all();  // every query store has completed
     }
 }
 

@@ -39,7 +39,7 @@ struct qa_cache {
     uint32_t *err = nullptr;
     uint32_t *seq_cnt = nullptr;  // decode with device lengths: groups done per sequence
     std::vector<int> window;      // per layer: attention window in keys (0: full)
-    int overlap = 4;              // decode launches whose clusters the split plan fits at once
+    int overlap = 6;              // decode launches whose clusters the split plan fits at once
     bool overlap_fixed = false;   // set by qa_cache_set_decode_overlap: no per-launch choice
     std::vector<CUtensorMap> maps;  // [layer][K, V] decode tensor maps (copied into each launch)
     std::vector<int32_t> lens_host;
@@ -191,10 +191,21 @@ int plan_overlap(const qa_cache *c, cudaStream_t stream, int layer, int64_t resi
     }
 }
 
+// Split count for `overlap` launches of `groups` clusters.  Unless the caller
+// fixed the number of launches, fewer are planned for as long as the plan
+// would leave fewer than two splits (one split streams a whole sequence's
+// cache per CTA, whose latency then outweighs the extra overlap).
+int plan_splits(const qa_cache *c, int groups, int pos_max, bool multi, int HPC, int overlap) {
+    int S = qa::k3_choose_splits(c->cfg.head_dim, HPC, groups, pos_max, multi, overlap);
+    if (!c->overlap_fixed)
+        for (int n = overlap - 1; S < 2 && n >= 1; --n)
+            S = qa::k3_choose_splits(c->cfg.head_dim, HPC, groups, pos_max, multi, n);
+    return S;
+}
+
 // overlap: launches whose clusters should fit at once (see qa_cache_set_decode_overlap).
 int choose_splits(const qa_cache *c, int batch, int pos_max, int overlap) {
-    return qa::k3_choose_splits(c->cfg.head_dim, c->HPC, batch * c->cfg.n_kv_heads * c->HG,
-                                pos_max, false, overlap);
+    return plan_splits(c, batch * c->cfg.n_kv_heads * c->HG, pos_max, false, c->HPC, overlap);
 }
 
 // Validation shared by qa_prefill and qa_prefill_transform.
@@ -335,8 +346,8 @@ qa_status run_multi(qa_cache *c, int layer, int batch, const int32_t *lens, int 
     auto flush = [&]() {
         if (nz == 0) return;
         p.B = nz;
-        p.S = qa::k3_choose_splits(g.head_dim, HPC, nz * g.n_kv_heads * p.HG, pos_max, true,
-                                   launches.empty() ? ov : std::min(2, ov));
+        p.S = plan_splits(c, nz * g.n_kv_heads * p.HG, pos_max, true, HPC,
+                          launches.empty() ? ov : std::min(2, ov));
         launches.emplace_back(p, m);
         nz = 0;
         pos_max = 0;

@@ -204,15 +204,17 @@ qa_status qa_cache_set_window(qa_cache *cache, int layer, int window);
  * Until this is called, each host-position launch chooses from the library's
  * record of the launches on its stream: 1 when nothing may still run beside
  * it (right after a prefill, a reset or a synchronisation through this
- * library), 2 when launches on its own layer may (a single-layer loop), 4
- * when only other layers' launches may (a loop over attention layers; on
- * GB300 it gave the best rate per step at batch 1 and 4 for caches of 512 to
- * 16384 keys).  Kernels of other code are not in that record: a caller whose
+ * library), 2 when launches on its own layer may (a single-layer loop), and
+ * up to 6 when only other layers' launches may (a loop over attention
+ * layers), fewer while 6 would leave a launch a single split (on GB300 this
+ * gave the best rate per step at batch 1 and 4 for caches of 512 to 16384
+ * keys).  Kernels of other code are not in that record: a caller whose
  * decode launches are separated by other kernels (a model's projections
  * between the attention layers) gets the most splits per launch with 1.
- * Device-length steps always plan for 4 (or the number set here), so a
- * captured step and the same step run eagerly agree bit for bit.  Any value
- * gives the same result up to the summation order of the split merge.
+ * Device-length steps always plan for that last case (or the number set
+ * here), so a captured step and the same step run eagerly agree bit for bit.
+ * Any value gives the same result up to the summation order of the split
+ * merge.
  * Host-side only, takes effect for launches after the call.
  * Errors: INVALID_ARG (launches outside 1..8). */
 qa_status qa_cache_set_decode_overlap(qa_cache *cache, int launches);
@@ -291,7 +293,7 @@ qa_status qa_memory_info(qa_cache *cache, uint64_t *kv_bytes, uint64_t *scratch_
 
 /* Number of key-range splits qa_decode_step uses for the current lengths of
  * `layer` and `batch` sequences when it runs beside other layers' launches
- * (the cache's overlap setting, 4 unless set; see qa_cache_set_decode_overlap;
+ * (up to 6 launches unless set; see qa_cache_set_decode_overlap;
  * a pure host computation; a step launches one kernel per 64 sequences, and
  * this is the first one's count). */
 int qa_decode_splits(qa_cache *cache, int layer, int batch);
