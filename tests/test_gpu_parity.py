@@ -51,8 +51,12 @@ def _check_cache(c, lay, lens, D, layer=0):
 
 
 # ------------------------------------------------------------------ K1 alone
+# The last three have token row counts (q, k and v heads) that are not a whole
+# number of a warp's passes, and q rows that end mid-pass.
 @pytest.mark.parametrize("lens,Hq,Hkv,D,cap", [((64,), 2, 1, 64, 72), ((512,), 32, 8, 128, 544),
-                                               ((3, 130, 1, 64), 8, 2, 128, 140)])
+                                               ((3, 130, 1, 64), 8, 2, 128, 140),
+                                               ((7, 33), 16, 2, 128, 40), ((50,), 12, 6, 64, 56),
+                                               ((9, 2), 4, 1, 64, 12)])
 def test_k1_transform_matches_oracle(qa, oracle_mod, lens, Hq, Hkv, D, cap):
     inp = layer_inputs(11, lens, Hq, Hkv, D, steps=0)
     c = GpuCache(qa, 1, len(lens), Hq, Hkv, D, cap)
