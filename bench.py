@@ -294,8 +294,8 @@ def run_ours(args):
     flops = w.causal_flops()
     L0 = w.prompt_lens[0]
     dec_bytes = sum(w.B * w.Hkv * (L0 + s + 1) * w.D * 2 * 2 for s in range(w.steps))
-    pre_us = statistics.median(pre_ms) * 1e3
-    dec_us_per_step = statistics.median(dec_ms) * 1e3 / w.steps
+    pre_us = statistics.mean(pre_ms) * 1e3
+    dec_us_per_step = statistics.mean(dec_ms) * 1e3 / w.steps
     pre_tflops = flops / (pre_us * 1e-6) / 1e12
     dec_gbs = dec_bytes / w.steps / (dec_us_per_step * 1e-6) / 1e9
     dec_share = sum(dec_ms) / total_ms
@@ -337,19 +337,19 @@ def run_ours(args):
                "frac": round(dec_gbs / pk["hbm_gbs"], 4), "traffic": None,
                "per_launch_bytes": round(dec_bytes / w.steps),
                "duration": "decode span / 128 launches (includes inter-launch gaps)"}
-    roof_k1 = {"bound": "hbm", "kernel": "k1_norm_rope_append_kernel<128>",
+    roof_k1 = {"bound": "hbm", "kernel": "k1t_norm_rope_append_kernel<128> (token-tiled)",
                "workload": "qa_prefill_transform, B=4 x 2048 prompt rows",
                "achieved": round(k1_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                "frac": round(k1_gbs / pk["hbm_gbs"], 4),
                "traffic": traffic_for("k1_norm", k1_bytes), "per_launch_bytes": k1_bytes,
-               "duration": "median over launches, L2 flushed before each"}
-    roof_k2 = {"bound": "tensor", "kernel": "k2_prefill_kernel<128>",
+               "duration": "mean over 40 launches, L2 flushed before each"}
+    roof_k2 = {"bound": "tensor", "kernel": "k2c_prefill_kernel (CTA pairs, cta_group::2)",
                "workload": "qa_prefill_attend, B=4 x 2048 causal",
                "achieved": round(k2_tflops, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                "frac": round(k2_tflops / pk["bf16_tflops"], 4),
                "traffic": traffic_for("k2_prefill", None), "per_launch_flops": flops,
-               "duration": "median over launches, L2 flushed before each"}
-    roof_pre = {"bound": "tensor", "kernel": "k1 + k2_prefill_kernel<128>",
+               "duration": "mean over 40 launches, L2 flushed before each"}
+    roof_pre = {"bound": "tensor", "kernel": "k1t_norm_rope_append_kernel<128> + k2c_prefill_kernel",
                 "workload": "qa_prefill call (K1 + K2), B=4 x 2048",
                 "achieved": round(pre_tflops, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(pre_tflops / pk["bf16_tflops"], 4), "traffic": None,
@@ -410,10 +410,12 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_prefill_halves(args, qa, h, w, P, lens_arr, flush, stream, reps=10):
-    """Median µs of K1 alone (qa_prefill_transform) and of K2 alone
+def time_prefill_halves(args, qa, h, w, P, lens_arr, flush, stream, reps=40):
+    """Mean µs of K1 alone (qa_prefill_transform) and of K2 alone
     (qa_prefill_attend over the rows K1 just appended), each launch after an
-    L2 flush, on the generate call's prompt."""
+    L2 flush, on the generate call's prompt.  A mean, not a median: event
+    timestamps come in steps of about a microsecond, and the launches start at
+    random phases of that step, so the mean resolves what one sample cannot."""
     import torch
     lib = qa.lib
     sh = stream.cuda_stream
@@ -441,7 +443,7 @@ def time_prefill_halves(args, qa, h, w, P, lens_arr, flush, stream, reps=10):
             t2.append(c.elapsed_time(d) * 1e3)
     if qa.qa_get_device_error(h)[0]:
         raise RuntimeError("device error while timing the prefill halves")
-    return statistics.median(t1), statistics.median(t2)
+    return statistics.mean(t1), statistics.mean(t2)
 
 
 def run_e2e(args, qa, h, w, inp, stream):
@@ -703,13 +705,13 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
             torch.cuda.synchronize()
             if st or qa.qa_get_device_error(h)[0]:
                 raise RuntimeError("isolated decode steps failed")
-            iso_us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+            iso_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in evs)
             iso_gbs = ib / iso / (iso_us * 1e-6) / 1e9
             isolated = {"B": pt.B, "L": pt.L, "steps": iso, "splits": iso_splits,
                         "us_per_step": round(iso_us, 3), "hbm_gbs": round(iso_gbs, 1),
                         "frac_of_measured_hbm": round(iso_gbs / pk["hbm_gbs"], 4),
                         "kv_bytes_per_step": round(ib / iso),
-                        "how": "median of per-launch events; a spacer kernel before each launch, "
+                        "how": "mean of per-launch events; a spacer kernel before each launch, "
                                "layers cycled (HBM-cold), split plan for one launch, the host "
                                "ahead of the device"}
         points.append({"sweep": pt.name, "B": pt.B, "L": pt.L, "steps": steps, "layers": NL,

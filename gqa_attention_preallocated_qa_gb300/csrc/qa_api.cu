@@ -116,16 +116,17 @@ qa_status check_layer(const qa_cache *c, int layer, int batch) {
 }
 
 // Per-sequence K (or V) tensor map over one layer's cache: (D, L, Hkv) with the
-// head stride of the cache, 64 x 128 x 1 boxes, 128-byte swizzle; rows at or
-// beyond L read as zero.
-bool encode_kv_map(CUtensorMap *m, void *base, int D, int L, int Hkv, int cap) {
+// head stride of the cache, 64 x box_rows x 1 boxes, 128-byte swizzle; rows at
+// or beyond L read as zero.  K uses 64-row boxes (the CTA-pair prefill loads
+// half a key tile per CTA), V 128-row boxes.
+bool encode_kv_map(CUtensorMap *m, void *base, int D, int L, int Hkv, int cap, int box_rows) {
     auto enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
                                 static_cast<cuuint64_t>(Hkv)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                                    static_cast<cuuint64_t>(cap) * D * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -413,8 +414,8 @@ qa_status plan_k2(qa_cache *c, int layer, int batch, const int32_t *lens, const 
                                     static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
                 __nv_bfloat16 *vb = c->V + layer * c->layer_elems +
                                     static_cast<int64_t>(s0 + i) * g.n_kv_heads * g.capacity * D;
-                if (!encode_kv_map(&p.tm_k[nseq], kb, D, P + L, g.n_kv_heads, g.capacity) ||
-                    !encode_kv_map(&p.tm_v[nseq], vb, D, P + L, g.n_kv_heads, g.capacity))
+                if (!encode_kv_map(&p.tm_k[nseq], kb, D, P + L, g.n_kv_heads, g.capacity, 64) ||
+                    !encode_kv_map(&p.tm_v[nseq], vb, D, P + L, g.n_kv_heads, g.capacity, 128))
                     return QA_ERR_CUDA;
                 p.len[nseq] = L;
                 p.start[nseq] = P;

@@ -57,12 +57,12 @@ constexpr int kK2BlockN = 128;    // keys per tile
 
 struct alignas(64) K2Params {
     CUtensorMap tm_q;                         // q' [T][Hq][D] as (D, Hq, T)
-    CUtensorMap tm_k[kMaxSeqPerLaunch];       // per sequence: (D, start_b + L_b, Hkv) over the cache
-    CUtensorMap tm_v[kMaxSeqPerLaunch];
+    CUtensorMap tm_k[kMaxSeqPerLaunch];       // per sequence: (D, start_b + L_b, Hkv) over the cache, 64-row boxes
+    CUtensorMap tm_v[kMaxSeqPerLaunch];       // the same with 128-row boxes
     __nv_bfloat16 *out;                       // [T][Hq][D]
     uint32_t *err;
     int nseq, Hq, Hkv, G, npairs;             // npairs: items per kv head and query block
-    int hpi;                                  // query heads per item (1 or 2; set at launch)
+    int hpi;                                  // query heads per item (1, 2, or 4 for a CTA pair; set at launch)
     int len[kMaxSeqPerLaunch];                // new tokens of each sequence
     int start[kMaxSeqPerLaunch];              // position of each sequence's first new token
     int cu[kMaxSeqPerLaunch];                 // first row of each sequence in q'/out
