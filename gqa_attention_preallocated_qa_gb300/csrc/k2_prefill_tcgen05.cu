@@ -551,11 +551,13 @@ struct K2CLayout {
     static constexpr int kKBoxBytes = 64 * 128;          // 64 keys x 64 bf16
     static constexpr int kHalfBytes = 2 * kKBoxBytes;    // this CTA's half of a K or V tile
     static constexpr int kStages = 4;                    // ring of halves: 2 key tiles
-    static constexpr int kSmemBytes = kQSlots * kQBytes + kStages * kHalfBytes + 1024;
+    static constexpr int kStageOutBytes = 32 * 128;      // per softmax warp: 32 rows x 64 bf16
+    static constexpr int kSmemBytes =
+        kQSlots * kQBytes + kStages * kHalfBytes + 8 * kStageOutBytes + 1024;
     static constexpr uint32_t kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kThreads = 320;
-    static constexpr int kTmaWarp = 8, kMmaWarp = 9;
+    static constexpr int kThreads = 352;
+    static constexpr int kTmaWarp = 8, kMmaWarp = 9, kQWarp = 10;
 };
 
 template <bool kWindow>
@@ -577,6 +579,7 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sQ = smem_u32(smem);  // item k's Q tiles in slot k mod 2
     const uint32_t sKV = sQ + Lay::kQSlots * Lay::kQBytes;
+    uint8_t *sOut = smem + Lay::kQSlots * Lay::kQBytes + NS * Lay::kHalfBytes;  // output staging
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs of the pair
     const int pair_id = blockIdx.x >> 1;
@@ -610,36 +613,18 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
     const uint32_t tmem = s_tmem;
 
     if (warp == Lay::kTmaWarp) {
-        // ------------------------------------------------------------ TMA producers (both CTAs)
+        // ------------------------------------------------------------ K/V producer (both CTAs)
+        int no_abort = 0;  // see above: the producers' waits do not follow s_abort
         if (lane == 0) {
-            prefetch_tmap(&p.tm_q);
             // Test hook: both CTAs of the first pair withhold their halves of its
             // first item's V tile 0 (no byte of that copy is ever in flight).
             const uint32_t withheld = (p.fault && pair_id == 0) ? 1u : 0xffffffffu;
-            int no_abort = 0;  // see above: the producers' waits do not follow s_abort
             uint32_t g = 0;
-            int nq = 0;
             bool ok = true;
             K2Item it;
             for (int k = 0; ok && k2p_item<kWindow>(p, k, it, 1); ++k) {
-                // Q slot k mod 2 is free once item k - 2's last S MMAs are done;
-                // item k's Q tiles thus load while item k - 1 still runs.
-                const int qs = k & 1;
-                if (k >= 2 && !mbar_wait(smem_u32(&bar_qfree[qs]), ((k >> 1) - 1) & 1, &no_abort,
-                                         p.err, kKernK2, 40, p.wait_ns))
-                    break;
                 prefetch_tmap(&p.tm_k[it.b]);
                 prefetch_tmap(&p.tm_v[it.b]);
-                const uint32_t bq = smem_u32(&bar_q[qs]);
-                if (rank == 0) mbar_expect_tx(bq, 2 * Lay::kQBytes);
-                const uint32_t bq_lead = map_rank(bq, 0);
-                for (int t = 0; t < 2; ++t)
-                    for (int x = 0; x < 2; ++x)
-                        tma_load_3d_pair(sQ + qs * Lay::kQBytes + t * Lay::kQTileBytes +
-                                             x * Lay::kQBoxBytes,
-                                         &p.tm_q, x * 64, it.h0 + 2 * static_cast<int>(rank) + t,
-                                         it.row0, bq_lead);
-                ++nq;
                 for (int idx = 0; idx < 2 * it.nkv; ++idx, ++g) {
                     const int st = g % NS;
                     if (g >= NS && !mbar_wait(smem_u32(&bar_kv_empty[st]), ((g / NS) - 1) & 1,
@@ -664,13 +649,51 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
                 }
             }
             if (rank == 0) {
-                // Never leave a copy in flight: both CTAs' last copies and Q tiles
-                // complete on these barriers (bounded waits).
+                // Never leave a copy in flight: both CTAs' last copies complete on
+                // these barriers (bounded waits).
                 int dummy = 0;
                 for (uint32_t i = g > NS ? g - NS : 0; i < g; ++i)
                     if (i != withheld)
                         mbar_wait(smem_u32(&bar_kv_full[i % NS]), (i / NS) & 1, &dummy, p.err,
                                   kKernK2, 42, p.wait_ns);
+            }
+        }
+    } else if (warp == Lay::kQWarp) {
+        // ------------------------------------------------------------ Q producer (both CTAs)
+        // A warp of its own, so its waits never hold up the K/V copies: each
+        // item's Q tiles load as soon as their slot is free, about an item ahead.
+        int no_abort = 0;
+        if (lane == 0) {
+            prefetch_tmap(&p.tm_q);
+            int nq = 0;
+            K2Item it;
+            for (int k = 0; k2p_item<kWindow>(p, k, it, 1); ++k) {
+                // Q slot k mod 2 is free once item k - 2's last S MMAs are done.
+                const int qs = k & 1;
+                if (k >= 2 && !mbar_wait(smem_u32(&bar_qfree[qs]), ((k >> 1) - 1) & 1, &no_abort,
+                                         p.err, kKernK2, 40, p.wait_ns))
+                    break;
+                const uint32_t bq = smem_u32(&bar_q[qs]);
+                if (rank == 0) mbar_expect_tx(bq, 2 * Lay::kQBytes);
+                const uint32_t bq_lead = map_rank(bq, 0);
+                for (int t = 0; t < 2; ++t)
+                    for (int x = 0; x < 2; ++x)
+                        tma_load_3d_pair(sQ + qs * Lay::kQBytes + t * Lay::kQTileBytes +
+                                             x * Lay::kQBoxBytes,
+                                         &p.tm_q, x * 64, it.h0 + 2 * static_cast<int>(rank) + t,
+                                         it.row0, bq_lead);
+                ++nq;
+                // The next item's Q tiles into L2 meanwhile: a short item leaves
+                // less time than a copy from HBM takes.
+                K2Item nx;
+                if (k2p_item<kWindow>(p, k + 1, nx, 1))
+                    for (int t = 0; t < 2; ++t)
+                        for (int x = 0; x < 2; ++x)
+                            tma_prefetch_3d(&p.tm_q, x * 64, nx.h0 + 2 * static_cast<int>(rank) + t,
+                                            nx.row0);
+            }
+            if (rank == 0) {
+                int dummy = 0;
                 for (int i = nq > 2 ? nq - 2 : 0; i < nq; ++i)
                     mbar_wait(smem_u32(&bar_q[i & 1]), (i >> 1) & 1, &dummy, p.err, kKernK2, 43,
                               p.wait_ns);
@@ -901,25 +924,45 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
             if (!ok) break;
             ++nitem;
             tc_fence_after();
+            // O_t / l in bf16 through this warp's staging area, half a row (64
+            // columns, 128 bytes) at a time: each lane writes its own row (16-byte
+            // chunks XOR-swizzled by row, so the 32 rows spread over all banks),
+            // then the warp reads back four rows x 128 bytes per instruction and
+            // stores whole 128-byte lines (rows past the sequence's end skipped).
             const float inv = 1.f / l;
-            const int row = it.qb * 128 + r;
-            const bool valid = row < it.L;
-            __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(p.cu[it.b] + row) * p.Hq + it.h0 +
-                                          2 * static_cast<int>(rank) + t) * D;
+            uint8_t *stg = sOut + warp * Lay::kStageOutBytes;
+            const int rw = lane >> 3, cw = lane & 7;  // read-back: row within a group of 4, chunk
+            const int row_base = it.qb * 128 + (warp & 3) * 32;  // token index of the warp's row 0
+            __nv_bfloat16 *obase = p.out + (static_cast<int64_t>(p.cu[it.b]) * p.Hq + it.h0 +
+                                            2 * static_cast<int>(rank) + t) * D;
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t u[32];
-                tmem_ld32(tO + ch * 32, u);
-                uint32_t w[16];
+            for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = pack_bf16(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
-                if (valid) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t u[32];
+                    tmem_ld32(tO + h * 64 + c2 * 32, u);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 v = make_uint4(
+                            pack_bf16(__uint_as_float(u[8 * i]) * inv, __uint_as_float(u[8 * i + 1]) * inv),
+                            pack_bf16(__uint_as_float(u[8 * i + 2]) * inv, __uint_as_float(u[8 * i + 3]) * inv),
+                            pack_bf16(__uint_as_float(u[8 * i + 4]) * inv, __uint_as_float(u[8 * i + 5]) * inv),
+                            pack_bf16(__uint_as_float(u[8 * i + 6]) * inv, __uint_as_float(u[8 * i + 7]) * inv));
+                        const int chunk = c2 * 4 + i;
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + ((chunk ^ (lane & 7)) << 4)) = v;
+                    }
                 }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = 4 * i + rw;  // row within the warp's 32
+                    const uint4 v =
+                        *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((cw ^ (rr & 7)) << 4));
+                    if (row_base + rr < it.L)
+                        reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(row_base + rr) * p.Hq * D +
+                                                  h * 64)[cw] = v;
+                }
+                __syncwarp();  // read back before the next half overwrites the stage
             }
         }
     }

@@ -169,6 +169,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
+// Prefetch a 3-D tile of a tensor map into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
