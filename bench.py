@@ -597,9 +597,9 @@ def host_ahead(launches: int, us_per_launch: float = 6.0):
 
 def decode_sweep(args, pk, steps, isolated_steps=200):
     """Decode-only sweep (batch 1 and 4, cache lengths 512 to 16384).  Each
-    point allocates NL layer caches, NL large enough that together they hold
-    at least 3x the L2 (129 MB), every one filled with L raw N(0,1) keys/values
-    per sequence; the `steps` timed decode steps cycle through the layers (step
+    point allocates NL layer caches, NL at least the 36 attention layers of
+    Qwen3-4B and large enough that together they hold at least 3x the L2
+    (129 MB), every one filled with L raw N(0,1) keys/values per sequence; the `steps` timed decode steps cycle through the layers (step
     s decodes layer s mod NL, as a model's layer loop does), so each step reads
     its layer's K/V from HBM, not from L2.  The length of a layer grows by one
     per visit; bytes are counted exactly.  A GPU sleep before the loop lets the
@@ -627,7 +627,7 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
     for pt in DECODE_SWEEP:
         inp = pt.inputs()
         layer_bytes = pt.B * pt.Hkv * pt.L * pt.D * 4
-        NL = max(1, min(256, -(-3 * l2_bytes // layer_bytes)))
+        NL = max(36, min(256, -(-3 * l2_bytes // layer_bytes)))
         iso = isolated_steps if (pt.B, pt.L) == (4, 2048) else 0
         visits = -(-(steps + args.warmup + iso) // NL) + args.warmup + 1
         same_steps = 200

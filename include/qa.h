@@ -269,9 +269,10 @@ qa_status qa_get_device_error(qa_cache *cache, uint32_t *detail);
 /* Failure-detection test hook.  Arms the next launch of `kernel`
  * (QA_KERNEL_PREFILL_ATTN, or QA_KERNEL_DECODE_ATTN: decode steps, short
  * chunks and qa_decode_step_noalloc), process-wide: in that launch one tile
- * copy is withheld (prefill: a V tile of the first thread block; decode: the
- * first cache chunk of each block of the first sequence's first kv-head group
- * that streams any), so a wait for it can never succeed, and every bounded
+ * copy is withheld (prefill: a V tile of the first thread block, or both
+ * halves of it in the first CTA pair of the pair form; decode: the first cache
+ * chunk of each block of the first sequence's first kv-head group that streams
+ * any), so a wait for it can never succeed, and every bounded
  * wait of the launch gives up after wait_us
  * microseconds (1 .. 2000000) instead of 2 s.  The waiting thread records
  * QA_ERR_DEVICE_TIMEOUT (kernel and site in the detail word) in the error

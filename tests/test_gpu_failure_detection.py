@@ -2,8 +2,9 @@
 kernels is bounded, and a wait that runs out is reported, not hung on.
 
 The library's test hook (qa_debug_arm_wait_timeout) makes the next launch of a
-kernel withhold one tile copy in its first thread block, so a wait for that
-tile can never succeed, and gives the launch's waits a short limit.  The
+kernel withhold one tile copy in its first thread block (both CTAs of the
+first pair in the CTA-pair prefill), so a wait for that tile can never
+succeed, and gives the launch's waits a short limit.  The
 kernel records QA_ERR_DEVICE_TIMEOUT in the error word, waits for its own
 copies in flight (and, in the decode kernel's clusters, for what its peers
 send it), frees its tensor memory and exits.  The host reads the status; the
@@ -39,8 +40,12 @@ def _check_word(st, word, kernel):
     assert (word & 0xff) == TIMEOUT and ((word >> 8) & 0xff) == kernel, hex(word)
 
 
-def test_prefill_wait_that_runs_out_is_reported_and_the_cache_stays_usable(qa, oracle_mod):
-    lens, Hq, Hkv, D, cap, steps = (300, 129), 8, 2, 128, 140 + 300, 2
+# The first geometry runs the one-CTA prefill (10 four-head items, fewer than
+# the device holds pairs); the second the CTA-pair prefill (128 items).
+@pytest.mark.parametrize("lens,Hq,Hkv,D,cap,steps", [((300, 129), 8, 2, 128, 440, 2),
+                                                     ((1024, 900), 32, 8, 128, 1030, 2)])
+def test_prefill_wait_that_runs_out_is_reported_and_the_cache_stays_usable(qa, oracle_mod, lens, Hq,
+                                                                           Hkv, D, cap, steps):
     inp = layer_inputs(61, lens, Hq, Hkv, D, steps)
     c = GpuCache(qa, 1, len(lens), Hq, Hkv, D, cap)
     try:
