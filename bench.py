@@ -1081,12 +1081,11 @@ def main():
         run_profile_case(args)
     elif args.sweep:
         run_sweep(args)
-    elif args.verify:
-        run_verify(args)
-    elif args.graph:
-        run_graph(args)
-    elif args.window:
-        run_window(args)
+    elif args.verify or args.graph or args.window:
+        # each mode's JSON lines, then the clocks seen while it ran
+        with ClockSampler(0) as clocks:
+            (run_verify if args.verify else run_graph if args.graph else run_window)(args)
+        print(json.dumps({"clocks": clocks.summary()}), flush=True)
     elif args.impl == "reference":
         run_reference(args)
     else:
