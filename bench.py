@@ -707,10 +707,32 @@ def decode_sweep(args, pk, steps, isolated_steps=200):
                 raise RuntimeError("isolated decode steps failed")
             iso_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in evs)
             iso_gbs = ib / iso / (iso_us * 1e-6) / 1e9
+            # The floor of this measurement: the same spacer and events around
+            # the library's reset kernel (one CTA zeroing a few lengths) on a
+            # separate small cache.
+            h0 = qa.qa_cache_alloc(1, 1, pt.Hq, pt.Hkv, pt.D, 8, pt.theta, pt.eps)
+            fevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(iso)]
+            torch.cuda.synchronize()
+            host_ahead(3 * iso)
+            for a, b in fevs:
+                spacer.add_(1.0)
+                a.record(stream)
+                st |= lib.qa_cache_reset(h0, sh)
+                b.record(stream)
+            torch.cuda.synchronize()
+            qa.qa_cache_free(h0)
+            if st:
+                raise RuntimeError("launch-floor measurement failed")
+            floor_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in fevs)
             isolated = {"B": pt.B, "L": pt.L, "steps": iso, "splits": iso_splits,
                         "us_per_step": round(iso_us, 3), "hbm_gbs": round(iso_gbs, 1),
                         "frac_of_measured_hbm": round(iso_gbs / pk["hbm_gbs"], 4),
                         "kv_bytes_per_step": round(ib / iso),
+                        "launch_floor_us": round(floor_us, 3),
+                        "floor_how": "the same spacer and events around a one-CTA library "
+                                     "kernel (cache reset of a separate small cache): what any "
+                                     "launch costs in this measurement",
                         "how": "mean of per-launch events; a spacer kernel before each launch, "
                                "layers cycled (HBM-cold), split plan for one launch, the host "
                                "ahead of the device"}

@@ -73,6 +73,7 @@ struct alignas(64) K2Params {
     int nitems;                               // work items (query block x head tile(s))
     uint64_t wait_ns;                         // limit of every bounded wait
 };
+static_assert(sizeof(K2Params) <= 4096, "K2Params travels in the 4 KB of kernel parameters");
 
 // ---------------------------------------------------------------- K3
 constexpr int kK3ConsumerWarps = 5;

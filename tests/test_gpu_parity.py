@@ -117,6 +117,9 @@ def test_decode_on_prefilled_cache(qa, oracle_mod, B, L, Hq, Hkv, D):
     ((130, 5), 16, 2, 64, 2, 140),                      # group 8 (two head groups per kv head)
     ((100, 256), 4, 4, 128, 2, 260),                    # group 1 (multi-head)
     (tuple(range(1, 45, 4)), 4, 2, 64, 2, 50),          # 11 sequences: several prefill launches
+    # CTA-pair prefill (144 four-head items) with sequence ends inside a warp's
+    # 32 rows (direct stores) next to whole warps (TMA stores of the output)
+    ((700, 333, 1100), 32, 8, 128, 2, 1110),
 ])
 def test_prefill_then_decode_matches_oracle(qa, oracle_mod, lens, Hq, Hkv, D, steps, cap):
     B = len(lens)
