@@ -325,7 +325,7 @@ int qa_decode_splits(qa_cache *cache, int layer, int batch);
  * are merged in distributed shared memory), kept in a fixed 256-byte array in
  * the library's device code that every GPU loading the library holds until
  * the process exits.  The first call on a device looks up that array's
- * address (no allocation); make that first call before any stream capture.
+ * address (no allocation).
  * Every call shares the array: calls that may overlap on the GPU (different
  * streams without ordering) race on it.  The error word is zero at load and
  * is cleared only by qa_noalloc_get_device_error, so it keeps the first error
