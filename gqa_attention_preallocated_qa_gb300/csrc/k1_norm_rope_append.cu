@@ -247,6 +247,27 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
         bulk_g2s(dst + qbytes + kvbytes, p.v + tok * p.Hkv * D, kvbytes, b);
     };
     if (lane == 0 && t < p.T) load(t, 0);
+    // Sequence and position of a token, and its row of the (cos, sin) table for
+    // this lane's 8 dims.  The next token's row is loaded while the warp works
+    // on the current one, so its latency stays off the token's path.
+    auto locate = [&](int64_t tok, int &bb, int &pp) {
+        int b = 0;
+        while (b + 1 < p.nseq && tok >= p.cu[b + 1]) ++b;
+        bb = b;
+        pp = p.start[b] + static_cast<int>(tok - p.cu[b]);
+    };
+    auto rope_row = [&](int pp, float4 (&c)[4]) {
+        const float4 *tab = reinterpret_cast<const float4 *>(
+            p.rope + static_cast<int64_t>(pp < p.cap ? pp : 0) * (D / 2) + 8 * (sub % HALF));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[e] = __ldg(tab + e);
+    };
+    int b_cur = 0, pos_cur = 0;
+    float4 rope_cur[4];
+    if (t < p.T) {
+        locate(t, b_cur, pos_cur);
+        rope_row(pos_cur, rope_cur);
+    }
     int abort_flag = 0;  // each warp gives up on its own
     int i = 0;
     bool ok = true;
@@ -254,22 +275,24 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
         const int s = i & 1;
         const int64_t tn = t + stride;
         if (lane == 0 && tn < p.T) load(tn, s ^ 1);  // the warp is done with that stage
+        int b_nx = 0, pos_nx = 0;
+        float4 rope_nx[4];
+        if (tn < p.T) {
+            locate(tn, b_nx, pos_nx);
+            rope_row(pos_nx, rope_nx);
+        }
         ok = mbar_wait(bar0 + 8 * s, (i >> 1) & 1, &abort_flag, p.err, kKernK1, 2);
         ok = __all_sync(FULL, ok);
         if (!ok) break;
-        int b = 0;
-        while (b + 1 < p.nseq && t >= p.cu[b + 1]) ++b;
-        const int pos = p.start[b] + static_cast<int>(t - p.cu[b]);
+        const int b = b_cur, pos = pos_cur;
         const bool in_cap = pos < p.cap;  // always, after host validation
         if (!in_cap && lane == 0) set_error(p.err, kErrBounds, kKernK1, 1);
-        const float4 *tab = reinterpret_cast<const float4 *>(
-            p.rope + static_cast<int64_t>(in_cap ? pos : 0) * (D / 2) + 8 * (sub % HALF));
         // (cos, sin) of this lane's 8 dims as pairs, the sines signed for its half
         float2 cs2[4], sn2[4];
         const float sgn = (sub % LPR) < HALF ? -1.f : 1.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float4 c4 = __ldg(tab + e);
+            const float4 c4 = rope_cur[e];
             cs2[e] = make_float2(c4.x, c4.z);
             sn2[e] = make_float2(sgn * c4.y, sgn * c4.w);
         }
@@ -313,6 +336,10 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
         // The warp's reads of the stage come before the next bulk copy overwrites it.
         fence_proxy_async_smem();
         __syncwarp();
+        b_cur = b_nx;
+        pos_cur = pos_nx;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) rope_cur[e] = rope_nx[e];
     }
     if (lane == 0) {
         // A copy requested for a token that was not reached (the loop gave up):
