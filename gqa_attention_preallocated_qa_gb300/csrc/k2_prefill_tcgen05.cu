@@ -773,9 +773,7 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(t, sv, j > 0);
-                        // O_t of the CTA's last item is final (earlier items' outputs
-                        // are read when the next item's first S_t arrives)
-                        if (!more) mma_commit_pair(smem_u32(&bar_pv[t]), kBoth);
+                        if (!more) mma_commit_pair(smem_u32(&bar_pv[t]), kBoth);  // O_t of the item is final
                         if (t == 1) {
                             mma_commit_pair(smem_u32(&bar_kv_empty[sv]), kBoth);
                             ++committed;
