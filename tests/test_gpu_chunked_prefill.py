@@ -125,6 +125,14 @@ def test_chunked_prefill_qwen3_geometry(qa, oracle_mod):
                heads=(0, 5, 17, 31), rows_per_chunk=12)
 
 
+def test_chunked_prefill_on_cta_pairs(qa, oracle_mod):
+    # The second chunk has 96 four-head items (two sequences x 6 query blocks x
+    # 8 kv heads): the CTA-pair prefill, at start offsets off the tile grid.
+    chunks = [(300, 250), (700, 701)]
+    run_chunks(qa, oracle_mod, chunks, 32, 8, 128, 1010, seed=71, decode_steps=2,
+               heads=(0, 3, 13, 30), rows_per_chunk=10)
+
+
 def test_chunked_prefill_one_tile_per_cta(qa, oracle_mod):
     # G = 1: a CTA has a single query tile (no head pair); D = 64.
     chunks = [(10, 0), (60, 7), (2, 130)]

@@ -120,6 +120,7 @@ def test_decode_on_prefilled_cache(qa, oracle_mod, B, L, Hq, Hkv, D):
     # CTA-pair prefill (144 four-head items) with sequence ends inside a warp's
     # 32 rows (direct stores) next to whole warps (TMA stores of the output)
     ((700, 333, 1100), 32, 8, 128, 2, 1110),
+    ((1100, 700), 32, 4, 128, 2, 1110),                 # group 8 on CTA pairs (120 items)
 ])
 def test_prefill_then_decode_matches_oracle(qa, oracle_mod, lens, Hq, Hkv, D, steps, cap):
     B = len(lens)
