@@ -547,7 +547,7 @@ struct K2CLayout {
     static constexpr int kQBoxBytes = 128 * 128;         // 128 rows x 64 bf16
     static constexpr int kQTileBytes = 2 * kQBoxBytes;   // 128 rows x D
     static constexpr int kQBytes = 2 * kQTileBytes;      // this CTA's two tiles of one item
-    static constexpr int kQSlots = 2;                    // items k and k + 1
+    static constexpr int kQSlots = 2;                    // item k's Q in slot k mod kQSlots
     static constexpr int kKBoxBytes = 64 * 128;          // 64 keys x 64 bf16
     static constexpr int kHalfBytes = 2 * kKBoxBytes;    // this CTA's half of a K or V tile
     static constexpr int kStages = 4;                    // ring of halves: 2 key tiles
@@ -663,15 +663,17 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
         // A warp of its own, so its waits never hold up the K/V copies: each
         // item's Q tiles load as soon as their slot is free, about an item ahead.
         int no_abort = 0;
+        constexpr int QS = Lay::kQSlots;
         if (lane == 0) {
             prefetch_tmap(&p.tm_q);
             int nq = 0;
             K2Item it;
             for (int k = 0; k2p_item<kWindow>(p, k, it, 1); ++k) {
-                // Q slot k mod 2 is free once item k - 2's last S MMAs are done.
-                const int qs = k & 1;
-                if (k >= 2 && !mbar_wait(smem_u32(&bar_qfree[qs]), ((k >> 1) - 1) & 1, &no_abort,
-                                         p.err, kKernK2, 40, p.wait_ns))
+                // Q slot k mod kQSlots is free once the last S MMAs of the item
+                // before that used it are done.
+                const int qs = k % QS;
+                if (k >= QS && !mbar_wait(smem_u32(&bar_qfree[qs]), ((k / QS) - 1) & 1, &no_abort,
+                                          p.err, kKernK2, 40, p.wait_ns))
                     break;
                 const uint32_t bq = smem_u32(&bar_q[qs]);
                 if (rank == 0) mbar_expect_tx(bq, 2 * Lay::kQBytes);
@@ -694,8 +696,8 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
             }
             if (rank == 0) {
                 int dummy = 0;
-                for (int i = nq > 2 ? nq - 2 : 0; i < nq; ++i)
-                    mbar_wait(smem_u32(&bar_q[i & 1]), (i >> 1) & 1, &dummy, p.err, kKernK2, 43,
+                for (int i = nq > QS ? nq - QS : 0; i < nq; ++i)
+                    mbar_wait(smem_u32(&bar_q[i % QS]), (i / QS) & 1, &dummy, p.err, kKernK2, 43,
                               p.wait_ns);
             }
         }
@@ -736,8 +738,8 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
             bool ok = true;
             K2Item it;
             for (int k = 0; ok && k2p_item<kWindow>(p, k, it, 1); ++k) {
-                const int qs = k & 1;
-                ok = mbar_wait(smem_u32(&bar_q[qs]), (k >> 1) & 1, &s_abort, p.err, kKernK2, 44,
+                const int qs = k % Lay::kQSlots;
+                ok = mbar_wait(smem_u32(&bar_q[qs]), (k / Lay::kQSlots) & 1, &s_abort, p.err, kKernK2, 44,
                                p.wait_ns);
                 dQ[0] = sdesc_sw128(sQ + qs * Lay::kQBytes, 16, 1024);
                 dQ[1] = sdesc_sw128(sQ + qs * Lay::kQBytes + Lay::kQTileBytes, 16, 1024);
@@ -801,8 +803,9 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
             for (uint32_t i = committed > NS ? committed - NS : 0; i < committed; ++i)
                 mbar_wait(smem_u32(&bar_kv_empty[i % NS]), (i / NS) & 1, &dummy, p.err, kKernK2,
                           49, p.wait_ns);
-            for (int i = nqfree > 2 ? nqfree - 2 : 0; i < nqfree; ++i)
-                mbar_wait(smem_u32(&bar_qfree[i & 1]), (i >> 1) & 1, &dummy, p.err, kKernK2, 50,
+            for (int i = nqfree > Lay::kQSlots ? nqfree - Lay::kQSlots : 0; i < nqfree; ++i)
+                mbar_wait(smem_u32(&bar_qfree[i % Lay::kQSlots]), (i / Lay::kQSlots) & 1, &dummy, p.err,
+                          kKernK2, 50,
                           p.wait_ns);
         }
     } else {
