@@ -87,7 +87,7 @@ def test_cuda_graph_of_a_two_layer_decode_step_replays_at_every_position(qa, ora
     ws = [(dev(i.wq), dev(i.wk)) for i in inps]
     g_cache = prefilled(qa, 2, prompt, cap, inps)
     e_cache = prefilled(qa, 2, prompt, cap, inps)
-    # the oracle follows both layers step by step: every replay is judged by it
+    # the oracle follows both layers step by step: every replay is checked against it
     lays = []
     for inp in inps:
         lay = oracle_mod.OracleLayer(oracle_mod.Geometry(4, HQ, HKV, D, cap))
@@ -181,7 +181,7 @@ def test_multi_layer_device_length_loop_reads_settled_positions_early(qa, oracle
     # Six layers decoded step by step, as a model's layer loop does: when a step
     # of layer l is launched, no launch still running writes layer l (the ones in
     # flight are other layers'), so the kernel reads its positions at once and
-    # overlaps the previous launch.  Every output is judged by the oracle, and
+    # overlaps the previous launch.  Every output is checked against the oracle, and
     # the device lengths advance exactly.
     layers, prompt, cap, steps = 6, (300, 700), 800, 3
     inps = [layer_inputs(91 + l, prompt, HQ, HKV, D, steps) for l in range(layers)]
