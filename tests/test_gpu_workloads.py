@@ -34,7 +34,8 @@ def qa():
 
 
 def sample_rows(L, rng, extra=12):
-    rows = {0, 1, 2, 63, 64, 127, 128, 129, 255, 256, 511, 512, 1023, 1024, 1535, 2046, 2047}
+    rows = {0, 1, 2, 63, 64, 127, 128, 129, 255, 256, 511, 512, 1023, 1024, 1535, 2046, 2047,
+            4095, 4096, 6143, 8190, 8191}
     rows = {r for r in rows if r < L} | {L - 1}
     rows |= set(rng.integers(0, L, size=extra).tolist())
     return sorted(rows)
@@ -226,6 +227,44 @@ def test_decode_sweep_point(qa, oracle_mod, pt):
                     want[b, h] = oracle_mod.attend(qn, Kf, Vf)[0]
         assert_parity(got, want, pt.name)
         assert qa.qa_cache_lengths(c.h, 0, pt.B) == [pt.L + 1] * pt.B
+        assert c.device_error() == (0, 0)
+    finally:
+        c.free()
+
+
+# Long prompts: up to 64 key tiles per query block, so every ring and Q slot of
+# the prefill goes through many phases.  The first geometry runs the CTA-pair
+# prefill (704 four-head items), the second the one-CTA form (head_dim 64).
+@pytest.mark.parametrize("lens,Hq,Hkv,D", [((8192, 3000), 32, 8, 128), ((6000,), 16, 2, 64)])
+def test_long_prompts_sampled_rows_and_decode(qa, oracle_mod, lens, Hq, Hkv, D):
+    from gqa_attention_preallocated_qa_gb300.inputs import layer_inputs
+    steps = 2
+    cap = max(lens) + steps
+    inp = layer_inputs(91, lens, Hq, Hkv, D, steps)
+    rng = np.random.default_rng(91)
+    c = GpuCache(qa, 1, len(lens), Hq, Hkv, D, cap)
+    try:
+        c.poison()
+        q, k, v, wq, wk = (dev(a) for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+        out = torch.empty_like(q)
+        qa.qa_prefill(c.h, 0, list(lens), q, k, v, wq, wk, out)
+        douts = []
+        for s in range(steps):
+            o = torch.empty_like(dev(inp.dq[s]))
+            qa.qa_decode_step(c.h, 0, len(lens), dev(inp.dq[s]), dev(inp.dk[s]), dev(inp.dv[s]),
+                              wq, wk, o)
+            douts.append(o)
+        torch.cuda.synchronize()
+        lay = oracle_mod.OracleLayer(oracle_mod.Geometry(len(lens), Hq, Hkv, D, cap))
+        qp = lay.prefill_transform(lens, F(inp.q), F(inp.k), F(inp.v), F(inp.wq), F(inp.wk))
+        check_prefill_rows(lay, None, qp, f64(out), lens, rng, heads=(0, Hq // 2 - 1, Hq - 1))
+        for s in range(steps):
+            qd = lay.decode_transform(F(inp.dq[s]), F(inp.dk[s]), F(inp.dv[s]), F(inp.wq),
+                                      F(inp.wk))
+            want = np.array([[lay.attend_cached(b, h, qd[b, h]) for h in range(Hq)]
+                             for b in range(len(lens))])
+            assert_parity(f64(douts[s]), want, f"decode step {s} after long prompts")
+        check_cache(c, lay, [L + steps for L in lens])
         assert c.device_error() == (0, 0)
     finally:
         c.free()
