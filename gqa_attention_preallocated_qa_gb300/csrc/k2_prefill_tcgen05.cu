@@ -7,11 +7,12 @@
 // the order of the arithmetic differs from the definition ("reorderings are
 // affordable", same guide, "Numerics").
 //
-// The kernel is persistent: one CTA per SM walks a fixed share of the work
-// items (described below).  An item is one 128-row block of a sequence's new
-// tokens (a whole prompt, or a chunk appended after the tokens the layer
-// already holds) for one or two query heads of a kv head; with two, both heads
-// share every K/V tile.  S_t = Q_t K_j^T (both operands K-major, 128-byte
+// Two persistent forms walk fixed shares of the work items.  An item is one
+// 128-row block of a sequence's new tokens (a whole prompt, or a chunk appended
+// after the tokens the layer already holds) for some query heads of a kv head,
+// all of which share every K/V tile: in the one-CTA form (one CTA per SM) one
+// or two heads, in the CTA-pair form (two SMs, tcgen05.mma.cta_group::2; head
+// dim 128, group sizes 4 and 8) four.  S_t = Q_t K_j^T (both operands K-major, 128-byte
 // swizzled smem); the softmax threads read their row of S_t with tcgen05.ld,
 // compute p = 2^(s*c - m*c) in fp32, write P as bf16 over the first 64 columns
 // of S_t, rescale O_t when the running max grew, and signal; O_t += P_t V_j
