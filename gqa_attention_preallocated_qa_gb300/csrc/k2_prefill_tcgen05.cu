@@ -1004,8 +1004,11 @@ static int k2c_clusters() {
         if (known != 0) return known > 0 ? known : 0;
     }
     int n = 0;
+    bool failed = false;
     if (cudaFuncSetAttribute(k2c_prefill_kernel<kWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             K2CLayout::kSmemBytes) == cudaSuccess) {
+                             K2CLayout::kSmemBytes) != cudaSuccess) {
+        failed = true;
+    } else {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(K2CLayout::kThreads);
@@ -1017,9 +1020,12 @@ static int k2c_clusters() {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, k2c_prefill_kernel<kWindow>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k2c_prefill_kernel<kWindow>, &cfg) != cudaSuccess) {
+            n = 0;
+            failed = true;
+        }
     }
-    cudaGetLastError();  // a failed query leaves no sticky error behind
+    if (failed) cudaGetLastError();  // the failed query's error is not left for the caller
     if (dev < 32) cache[dev].store(n > 0 ? n : -1, std::memory_order_release);
     return n;
 }
