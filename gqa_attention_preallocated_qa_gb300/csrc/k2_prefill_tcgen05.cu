@@ -54,33 +54,55 @@ constexpr float kRescaleLog2 = 8.f;
 
 
 // Heaviest-first work order: query blocks with more key tiles start first.
-__device__ __forceinline__ bool k2_decode_item(const K2Params &p, int idx, int &b, int &kvh,
-                                               int &pair, int &qb) {
-    for (int lvl = p.max_qblocks - 1; lvl >= 0; --lvl) {
-        int eligible = 0;
-        for (int s = 0; s < p.nseq; ++s) eligible += ((p.len[s] + 127) / 128 > lvl);
-        const int cnt = eligible * p.Hkv * p.npairs;
-        if (idx < cnt) {
-            const int per_seq = p.Hkv * p.npairs;
-            int which = idx / per_seq;
-            const int rem = idx % per_seq;
-            for (int s = 0; s < p.nseq; ++s) {
-                if ((p.len[s] + 127) / 128 > lvl) {
-                    if (which == 0) {
-                        b = s;
-                        break;
-                    }
-                    --which;
-                }
-            }
-            kvh = rem / p.npairs;
-            pair = rem % p.npairs;
-            qb = lvl;
-            return true;
-        }
-        idx -= cnt;
+// Items are listed by level (query block qb, highest first), then by sequence
+// among those with a block at that level, then kv head, then head group.
+// Every role walks its items in increasing index order, so a walk keeps the
+// level it is at (its first item's index and its item count) and enters each
+// level once: decoding an item costs a few comparisons, not a pass over every
+// level above it.
+struct K2Walk {
+    int lvl = -1;  // level of the last item decoded (-1: not started)
+    int base = 0;  // index of the level's first item
+    int cnt = 0;   // items at the level
+};
+
+// Sequences with a query block at level lvl (len > 128 lvl).
+__device__ __forceinline__ int k2_level_seqs(const K2Params &p, int lvl) {
+    int e = 0;
+#pragma unroll
+    for (int s = 0; s < kMaxSeqPerLaunch; ++s) e += (s < p.nseq && p.len[s] > lvl * 128) ? 1 : 0;
+    return e;
+}
+
+// Item idx (idx never below the walk's last item) as sequence, kv head, head
+// group and query block.
+__device__ __forceinline__ bool k2_decode_item(const K2Params &p, int idx, K2Walk &w, int &b,
+                                               int &kvh, int &pair, int &qb) {
+    const int per_seq = p.Hkv * p.npairs;
+    if (w.lvl < 0) {
+        w.lvl = p.max_qblocks - 1;
+        w.base = 0;
+        w.cnt = k2_level_seqs(p, w.lvl) * per_seq;
     }
-    return false;
+    while (idx >= w.base + w.cnt) {
+        w.base += w.cnt;
+        if (--w.lvl < 0) return false;
+        w.cnt = k2_level_seqs(p, w.lvl) * per_seq;
+    }
+    const int off = idx - w.base;
+    int which = off / per_seq;
+    const int rem = off - which * per_seq;
+    b = 0;
+#pragma unroll
+    for (int s = 0; s < kMaxSeqPerLaunch; ++s) {
+        const bool has = s < p.nseq && p.len[s] > w.lvl * 128;
+        if (has && which == 0) b = s;
+        which -= has ? 1 : 0;
+    }
+    kvh = rem / p.npairs;
+    pair = rem - kvh * p.npairs;
+    qb = w.lvl;
+    return true;
 }
 
 // ==================================================================== the kernel
@@ -132,15 +154,17 @@ struct K2Item {
     int row0;         // row of the block's row 0 in q' / out
 };
 
-// The k-th item of this CTA (false once its share is done); with shift 1 the
-// two CTAs of a cluster take the same items (one per cluster).
+// The k-th item of this CTA (false once its share is done; k never below the
+// walk's last call); with shift 1 the two CTAs of a cluster take the same
+// items (one per cluster).
 template <bool kWindow>
-__device__ __forceinline__ bool k2p_item(const K2Params &p, int k, K2Item &it, int shift = 0) {
+__device__ __forceinline__ bool k2p_item(const K2Params &p, int k, K2Walk &w, K2Item &it,
+                                         int shift = 0) {
     const int G = gridDim.x >> shift, c = blockIdx.x >> shift;
     const int idx = k * G + ((k & 1) ? G - 1 - c : c);
     if (idx >= p.nitems) return false;
     int pair = 0;
-    if (!k2_decode_item(p, idx, it.b, it.kvh, pair, it.qb)) return false;
+    if (!k2_decode_item(p, idx, w, it.b, it.kvh, pair, it.qb)) return false;
     it.h0 = it.kvh * p.G + p.hpi * pair;
     it.L = p.len[it.b];
     it.qmin = p.start[it.b] + it.qb * 128;
@@ -204,8 +228,9 @@ __global__ void __launch_bounds__(K2PLayout<D>::kThreads, 1)
             uint32_t g = 0;  // K/V copies requested (K and V of each key tile, in order)
             int nq = 0;      // items whose Q tiles were requested
             bool ok = true;
+            K2Walk walk;
             K2Item it;
-            for (int k = 0; ok && k2p_item<kWindow>(p, k, it); ++k) {
+            for (int k = 0; ok && k2p_item<kWindow>(p, k, walk, it); ++k) {
                 // The Q buffers are free once the previous item's last S MMAs are done.
                 if (nq > 0 && !mbar_wait(smem_u32(&bar_qfree), (nq - 1) & 1, &s_abort, p.err,
                                          kKernK2, 20, p.wait_ns))
@@ -292,8 +317,9 @@ __global__ void __launch_bounds__(K2PLayout<D>::kThreads, 1)
             uint32_t committed = 0;  // ring slots handed back (one per copy, in order)
             int nq = 0, nqfree = 0;
             bool ok = true;
+            K2Walk walk;
             K2Item it;
-            for (int k = 0; ok && k2p_item<kWindow>(p, k, it); ++k) {
+            for (int k = 0; ok && k2p_item<kWindow>(p, k, walk, it); ++k) {
                 ok = mbar_wait(smem_u32(&bar_q), nq & 1, &s_abort, p.err, kKernK2, 24, p.wait_ns);
                 ++nq;
                 if (ok)
@@ -376,8 +402,9 @@ __global__ void __launch_bounds__(K2PLayout<D>::kThreads, 1)
             uint32_t iter = 0;
             int nitem = 0;
             bool ok = true;
+            K2Walk walk;
             K2Item it;
-            for (int k = 0; ok && k2p_item<kWindow>(p, k, it); ++k) {
+            for (int k = 0; ok && k2p_item<kWindow>(p, k, walk, it); ++k) {
                 const int qpos = it.qmin + r;  // this row's position
                 // mref: the row's reference max (raw scores); it moves only when the
                 // row max exceeds it by more than kRescaleLog2 / c, so O is rescaled
@@ -622,8 +649,9 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
             const uint32_t withheld = (p.fault && pair_id == 0) ? 1u : 0xffffffffu;
             uint32_t g = 0;
             bool ok = true;
+            K2Walk walk;
             K2Item it;
-            for (int k = 0; ok && k2p_item<kWindow>(p, k, it, 1); ++k) {
+            for (int k = 0; ok && k2p_item<kWindow>(p, k, walk, it, 1); ++k) {
                 prefetch_tmap(&p.tm_k[it.b]);
                 prefetch_tmap(&p.tm_v[it.b]);
                 for (int idx = 0; idx < 2 * it.nkv; ++idx, ++g) {
@@ -668,8 +696,9 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&p.tm_q);
             int nq = 0;
+            K2Walk walk;
             K2Item it;
-            for (int k = 0; k2p_item<kWindow>(p, k, it, 1); ++k) {
+            for (int k = 0; k2p_item<kWindow>(p, k, walk, it, 1); ++k) {
                 // Q slot k mod kQSlots is free once the last S MMAs of the item
                 // before that used it are done.
                 const int qs = k % QS;
@@ -689,7 +718,7 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
                 // The next item's Q tiles into L2 meanwhile: a short item leaves
                 // less time than a copy from HBM takes.
                 K2Item nx;
-                if (k2p_item<kWindow>(p, k + 1, nx, 1))
+                if (k2p_item<kWindow>(p, k + 1, walk, nx, 1))
                     for (int t = 0; t < 2; ++t)
                         for (int x = 0; x < 2; ++x)
                             tma_prefetch_3d(&p.tm_q, x * 64, nx.h0 + 2 * static_cast<int>(rank) + t,
@@ -737,8 +766,9 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
             uint32_t g = 0, iter = 0, committed = 0;
             int nq = 0, nqfree = 0;
             bool ok = true;
+            K2Walk walk;
             K2Item it;
-            for (int k = 0; ok && k2p_item<kWindow>(p, k, it, 1); ++k) {
+            for (int k = 0; ok && k2p_item<kWindow>(p, k, walk, it, 1); ++k) {
                 const int qs = k % Lay::kQSlots;
                 ok = mbar_wait(smem_u32(&bar_q[qs]), (k / Lay::kQSlots) & 1, &s_abort, p.err, kKernK2, 44,
                                p.wait_ns);
@@ -821,8 +851,9 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
         uint32_t iter = 0;
         bool ok = true;
         int nitem = 0;
+        K2Walk walk;
         K2Item it;
-        for (int k = 0; ok && k2p_item<kWindow>(p, k, it, 1); ++k) {
+        for (int k = 0; ok && k2p_item<kWindow>(p, k, walk, it, 1); ++k) {
             const int qpos = it.qmin + r;
             float mref = -INFINITY, l = 0.f;  // as in the one-CTA form
             for (int j = 0; j < it.nkv; ++j, ++iter) {
