@@ -218,6 +218,10 @@ __global__ void __launch_bounds__(kK1TWarps * 32, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane % LPR, grp = lane / LPR;
+    // When the prefill attention kernel follows (launched as a programmatic
+    // dependent), its set-up may start now; it reads q' and the cache only
+    // after this grid has finished.
+    if (p.signal_early) griddep_launch_dependents();
     const uint32_t qbytes = static_cast<uint32_t>(p.Hq) * D * 2;
     const uint32_t kvbytes = static_cast<uint32_t>(p.Hkv) * D * 2;
     const uint32_t stage_bytes = (qbytes + 2 * kvbytes + 127) & ~127u;

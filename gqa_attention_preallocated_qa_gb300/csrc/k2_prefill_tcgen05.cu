@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(K2PLayout<D>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    griddep_wait();  // as in the CTA-pair form: global data only after this
 
     if (warp == Lay::kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
@@ -639,6 +640,10 @@ __global__ void __launch_bounds__(K2CLayout::kThreads, 1)
     cluster_sync_all();  // both CTAs' barriers initialised, tensor memory allocated
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    // Launched as a programmatic dependent: the set-up above may overlap the
+    // previous kernel's end (the norm/RoPE/append kernel, which signals at
+    // its start); every read and write of global data comes after this wait.
+    griddep_wait();
 
     if (warp == Lay::kTmaWarp) {
         // ------------------------------------------------------------ K/V producer (both CTAs)
@@ -1074,13 +1079,15 @@ static cudaError_t launch_k2c(const K2Params &p, int items4, int clusters, cudaS
     cfg.blockDim = dim3(K2CLayout::kThreads);
     cfg.dynamicSmemBytes = K2CLayout::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k2c_prefill_kernel<kWindow>, q);
 }
 
@@ -1116,8 +1123,17 @@ static cudaError_t launch_k2_t(const K2Params &p, int nitems, cudaStream_t strea
         q.npairs = p.G;
         q.nitems = nitems / p.npairs * q.npairs;
     }
-    k2p_prefill_kernel<D, kWindow><<<std::min(q.nitems, sms), Lay::kThreads, smem, stream>>>(q);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(std::min(q.nitems, sms), 1, 1);
+    cfg.blockDim = dim3(Lay::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k2p_prefill_kernel<D, kWindow>, q);
 }
 
 cudaError_t launch_k2(const K2Params &p, int D, int nitems, cudaStream_t stream) {

@@ -261,9 +261,11 @@ K1Params make_k1(qa_cache *c, int layer, const void *q, const void *k, const voi
 }
 
 // K1 over all prompt rows, in launches of up to kMaxSeqPerLaunch sequences.
+// then_k2: the prefill attention launches follow at once on the stream; K1
+// then lets them start their set-up early (programmatic dependent launch).
 qa_status run_k1(qa_cache *c, int layer, int batch, const int32_t *lens, const void *q,
                  const void *k, const void *v, const void *wq, const void *wk, void *qp,
-                 cudaStream_t s) {
+                 cudaStream_t s, bool then_k2) {
     const qa_config &g = c->cfg;
     const int D = g.head_dim;
     int64_t row0 = 0;
@@ -282,6 +284,7 @@ qa_status run_k1(qa_cache *c, int layer, int batch, const int32_t *lens, const v
             p.start[i] = cur[s0 + i];
         }
         p.T = p.cu[n];
+        p.signal_early = then_k2 ? 1 : 0;
         if (p.T > 0) {
             if (qa::launch_k1(p, D, s) != cudaSuccess) return QA_ERR_CUDA;
             g_order.barrier(s);
@@ -588,7 +591,7 @@ QA_API qa_status qa_prefill_transform(qa_cache *c, int layer, int batch,
                                  qprime_out, &T);
     if (st != QA_OK) return st;
     st = run_k1(c, layer, batch, prompt_lens, q, k, v, q_norm_w, k_norm_w, qprime_out,
-                static_cast<cudaStream_t>(stream));
+                static_cast<cudaStream_t>(stream), false);
     if (st != QA_OK) return st;
     for (int b = 0; b < batch; ++b)
         c->lens_host[static_cast<size_t>(layer) * c->cfg.max_batch + b] += prompt_lens[b];
@@ -620,10 +623,15 @@ QA_API qa_status qa_prefill(qa_cache *c, int layer, int batch, const int32_t *pr
     if (st != QA_OK) return st;
     // K1 stages the normed, rotated queries in `out`; K2 reads them back and
     // overwrites every row with its attention output (each CTA owns its rows).
-    st = run_k1(c, layer, batch, prompt_lens, q, k, v, q_norm_w, k_norm_w, out, s);
+    st = run_k1(c, layer, batch, prompt_lens, q, k, v, q_norm_w, k_norm_w, out, s, true);
     if (st != QA_OK) return st;
     st = launch_k2s(c, k2s, s);
-    if (st != QA_OK) return st;
+    if (st != QA_OK) {
+        // A K1 launch that signalled early is no longer followed by a kernel
+        // that waits for it: let it finish before anything else is enqueued.
+        cudaStreamSynchronize(s);
+        return st;
+    }
     for (int b = 0; b < batch; ++b)
         c->lens_host[static_cast<size_t>(layer) * g.max_batch + b] += prompt_lens[b];
     return QA_OK;

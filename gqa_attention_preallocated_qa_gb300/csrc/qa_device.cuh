@@ -175,6 +175,14 @@ __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1
                  "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
+// Programmatic dependent launch: let the next kernel on the stream start
+// (its own wait still orders its memory accesses after this grid's end) ...
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and wait until the previous kernel has finished and its writes are
+// visible (returns at once when this grid was not launched as a dependent).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

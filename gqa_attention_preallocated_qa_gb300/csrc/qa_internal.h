@@ -46,6 +46,7 @@ struct K1Params {
     int64_t seq_stride, head_stride;     // cache strides in elements
     int T, Hq, Hkv, cap, nseq;
     int seq_slot0;                       // cache slot of the first sequence of this launch
+    int signal_early;                    // 1: let the next kernel (prefill attention) start at once
     float eps;
     int cu[kMaxSeqPerLaunch + 1];        // row offsets of the sequences (relative to q/k/v)
     int start[kMaxSeqPerLaunch];         // position of each sequence's first new token
