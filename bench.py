@@ -554,7 +554,7 @@ def run_e2e(args, qa, h, w, inp, stream):
 
 def kernel_source_digest(kernel: str) -> str:
     """sha256 (first 16 hex digits) over the kernel's source file and the
-    device headers it includes, with comments and whitespace removed (a
+    headers of its own that it includes, with comments and whitespace removed (a
     comment edit does not change the kernel the counters were taken on)."""
     import hashlib
     import re
@@ -562,7 +562,8 @@ def kernel_source_digest(kernel: str) -> str:
     src = {"k3_decode": "k3_decode_splitkv.cu", "k3_multi": "k3_decode_splitkv.cu",
            "k2_prefill": "k2_prefill_tcgen05.cu", "k1_norm": "k1_norm_rope_append.cu"}[kernel]
     h = hashlib.sha256()
-    for name in (src, "qa_device.cuh", "qa_internal.h"):
+    extra = ("k2_items.h",) if kernel == "k2_prefill" else ()
+    for name in (src, "qa_device.cuh", "qa_internal.h") + extra:
         with open(os.path.join(csrc, name)) as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments

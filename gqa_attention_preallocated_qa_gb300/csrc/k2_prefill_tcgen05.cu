@@ -31,6 +31,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "k2_items.h"
 #include "qa_device.cuh"
 
 namespace qa {
@@ -52,58 +53,6 @@ __device__ __forceinline__ float k2_ex2(float x) {
 // powers of two (in the exp2 domain).
 constexpr float kRescaleLog2 = 8.f;
 
-
-// Heaviest-first work order: query blocks with more key tiles start first.
-// Items are listed by level (query block qb, highest first), then by sequence
-// among those with a block at that level, then kv head, then head group.
-// Every role walks its items in increasing index order, so a walk keeps the
-// level it is at (its first item's index and its item count) and enters each
-// level once: decoding an item costs a few comparisons, not a pass over every
-// level above it.
-struct K2Walk {
-    int lvl = -1;  // level of the last item decoded (-1: not started)
-    int base = 0;  // index of the level's first item
-    int cnt = 0;   // items at the level
-};
-
-// Sequences with a query block at level lvl (len > 128 lvl).
-__device__ __forceinline__ int k2_level_seqs(const K2Params &p, int lvl) {
-    int e = 0;
-#pragma unroll
-    for (int s = 0; s < kMaxSeqPerLaunch; ++s) e += (s < p.nseq && p.len[s] > lvl * 128) ? 1 : 0;
-    return e;
-}
-
-// Item idx (idx never below the walk's last item) as sequence, kv head, head
-// group and query block.
-__device__ __forceinline__ bool k2_decode_item(const K2Params &p, int idx, K2Walk &w, int &b,
-                                               int &kvh, int &pair, int &qb) {
-    const int per_seq = p.Hkv * p.npairs;
-    if (w.lvl < 0) {
-        w.lvl = p.max_qblocks - 1;
-        w.base = 0;
-        w.cnt = k2_level_seqs(p, w.lvl) * per_seq;
-    }
-    while (idx >= w.base + w.cnt) {
-        w.base += w.cnt;
-        if (--w.lvl < 0) return false;
-        w.cnt = k2_level_seqs(p, w.lvl) * per_seq;
-    }
-    const int off = idx - w.base;
-    int which = off / per_seq;
-    const int rem = off - which * per_seq;
-    b = 0;
-#pragma unroll
-    for (int s = 0; s < kMaxSeqPerLaunch; ++s) {
-        const bool has = s < p.nseq && p.len[s] > w.lvl * 128;
-        if (has && which == 0) b = s;
-        which -= has ? 1 : 0;
-    }
-    kvh = rem / p.npairs;
-    pair = rem - kvh * p.npairs;
-    qb = w.lvl;
-    return true;
-}
 
 // ==================================================================== the kernel
 // One CTA per SM walks a fixed share of the work items.  An item is one
@@ -143,36 +92,13 @@ struct K2PLayout {
     static constexpr int kTmaWarp = 8, kMmaWarp = 9;
 };
 
-// Geometry of one work item, the same in every role.
-struct K2Item {
-    int b, kvh, qb;   // sequence, kv head, query block
-    int h0;           // first query head of the item
-    int L;            // new tokens of the sequence
-    int qmin;         // position of the block's row 0
-    int j0, nkv;      // first key tile and number of key tiles
-    int jmask;        // key tiles from this one on may hold keys past a row's position
-    int row0;         // row of the block's row 0 in q' / out
-};
-
-// The k-th item of this CTA (false once its share is done; k never below the
-// walk's last call); with shift 1 the two CTAs of a cluster take the same
-// items (one per cluster).
+// The k-th item of this CTA in the snake order (false once its share is done;
+// k never below the walk's last call); with shift 1 the two CTAs of a cluster
+// take the same items (one per cluster).
 template <bool kWindow>
 __device__ __forceinline__ bool k2p_item(const K2Params &p, int k, K2Walk &w, K2Item &it,
                                          int shift = 0) {
-    const int G = gridDim.x >> shift, c = blockIdx.x >> shift;
-    const int idx = k * G + ((k & 1) ? G - 1 - c : c);
-    if (idx >= p.nitems) return false;
-    int pair = 0;
-    if (!k2_decode_item(p, idx, w, it.b, it.kvh, pair, it.qb)) return false;
-    it.h0 = it.kvh * p.G + p.hpi * pair;
-    it.L = p.len[it.b];
-    it.qmin = p.start[it.b] + it.qb * 128;
-    it.j0 = kWindow ? max(0, it.qmin + 1 - p.window) / 128 : 0;
-    it.nkv = (it.qmin + min(127, it.L - 1 - it.qb * 128)) / 128 + 1 - it.j0;
-    it.jmask = it.qmin / 128;
-    it.row0 = p.cu[it.b] + it.qb * 128;
-    return true;
+    return k2_item_at<kWindow>(p, k2_snake_index(k, gridDim.x >> shift, blockIdx.x >> shift), w, it);
 }
 
 template <int D, bool kWindow>
