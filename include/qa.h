@@ -115,7 +115,11 @@ qa_status qa_cache_reset(qa_cache *cache, void *stream);
  * out[t][h] = sum_{j<=i} softmax_j(q'_t,h . K_j / sqrt(D)) V_j over sequence
  * b's cached keys 0..i, q' = RoPE(RMSNorm(q)), kv head h / (Hq/Hkv).
  * Work: when some L_b exceeds 8, K1 writes q' into out and k', v into the
- * cache, then K2 (one launch per 8 sequences) computes the attention.  When
+ * cache, then K2 (one launch per 8 sequences) computes the attention.  K2
+ * starts its set-up while K1 ends (programmatic dependent launch) and reads
+ * or writes global memory only once the kernel before it has finished, so
+ * the call is ordered after earlier work on the stream as a plain launch
+ * would be.  When
  * every L_b is at most 8 (a verify step of speculative decoding, a short
  * append), the decode kernel's multi-token form does all of it in one launch
  * per 64 sequences that have new tokens (each streams its cache once for all
