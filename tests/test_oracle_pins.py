@@ -340,3 +340,50 @@ def test_attend_cached_after_decode_transform_matches_brute_force_and_decode(ora
                 np.testing.assert_allclose(got, brute[bcu[i] + prompt_lens[i] + s, h],
                                            rtol=1e-9, atol=1e-12)
     assert list(a.lens) == [L + steps for L in prompt_lens]
+
+
+def test_prefill_transform_outputs_match_brute_force(oracle_mod):
+    # The transform the GPU's K1 is judged against: q' rows, the cache's K and V
+    # slots and the lengths, each from the complex-rotation formulation above
+    # (positions restart at 0 in every sequence; slots past a length untouched).
+    lens, Hq, Hkv, D, cap = (3, 6, 1), 4, 2, 16, 8
+    inp = layer_inputs(41, lens, Hq, Hkv, D, steps=0)
+    q, k, v, wq, wk = (_f(a) for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+    lay = oracle_mod.OracleLayer(_geom(oracle_mod, len(lens), Hq, Hkv, D, cap))
+    qp = lay.prefill_transform(lens, q, k, v, wq, wk)
+    half = D // 2
+    inv_freq = 1.0 / 1e6 ** (np.arange(0, D, 2, dtype=np.float64) / D)
+
+    def norm_rot(x, w, L):
+        y = w * x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + 1e-6)
+        z = (y[..., :half] + 1j * y[..., half:]) * np.exp(1j * np.arange(L)[:, None, None] * inv_freq)
+        return np.concatenate([z.real, z.imag], axis=-1)
+
+    t0 = 0
+    for b, L in enumerate(lens):
+        np.testing.assert_allclose(qp[t0:t0 + L], norm_rot(q[t0:t0 + L], wq, L), rtol=1e-12, atol=1e-14)
+        kr = norm_rot(k[t0:t0 + L], wk, L)             # [L, Hkv, D]
+        for h in range(Hkv):
+            np.testing.assert_allclose(lay.Kc[b, h, :L], kr[:, h], rtol=1e-12, atol=1e-14)
+            np.testing.assert_array_equal(lay.Vc[b, h, :L], v[t0:t0 + L, h])
+            assert not lay.Kc[b, h, L:].any() and not lay.Vc[b, h, L:].any()
+        t0 += L
+    assert list(lay.lens) == list(lens)
+
+
+def test_set_cache_restores_a_layer(oracle_mod):
+    # A layer loaded with another layer's cache and lengths decodes the next
+    # token exactly as that layer does.
+    lens, Hq, Hkv, D, cap = (5, 2), 4, 2, 16, 7
+    inp = layer_inputs(43, lens, Hq, Hkv, D, steps=1)
+    q, k, v, wq, wk = (_f(a) for a in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+    a = oracle_mod.OracleLayer(_geom(oracle_mod, 2, Hq, Hkv, D, cap))
+    a.prefill(lens, q, k, v, wq, wk)
+    b = oracle_mod.OracleLayer(_geom(oracle_mod, 2, Hq, Hkv, D, cap))
+    b.set_cache(a.Kc, a.Vc, a.lens)
+    step = [_f(x[0]) for x in (inp.dq, inp.dk, inp.dv)]
+    _, out_a = a.decode(*step, wq, wk)
+    _, out_b = b.decode(*step, wq, wk)
+    np.testing.assert_array_equal(out_a, out_b)
+    np.testing.assert_array_equal(a.Kc, b.Kc)
+    assert list(b.lens) == [n + 1 for n in lens]
